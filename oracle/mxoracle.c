@@ -1,0 +1,290 @@
+/*
+ * mxoracle.c -- plain CPU oracle for the block-scaled (MX) matrix product.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing in the product path links, loads or
+ * calls this file; only the tests, the smoke check and the benchmark's CPU
+ * baseline do.  It shares no code, header, table or constant with the CUDA
+ * path.
+ *
+ * What it computes (the plain definition, no blocking or fusion):
+ *
+ *   ref[i][j]   = sum_{k<K} e4m3(A[i][k]) * e8m0(As[i][k/32])
+ *                         * e4m3(B[k][j]) * e8m0(Bs[j][k/32])
+ *   bound[i][j] = sum_{k<K} | same term |
+ *
+ * accumulated in IEEE double, k ascending.
+ *
+ * Sources:
+ *   - "TLX API Quick Reference", section "Matrix Multiply (MMA)", row
+ *     `tlx.async_dot_scaled`: the scaled product D = (A*scale_A) @ (B*scale_B)
+ *     + D with FP8 operands.
+ *   - "Tensor core operations", sections "2-CTA Scaled MMA" and "TMEM-backed
+ *     MX Scales": operands in format "e4m3", one uint8 scale tensor per
+ *     operand.
+ *   - OCP Microscaling Formats (MX) specification v1.0, element format E4M3
+ *     (bias 7, subnormals, max 448, S.1111.111 = NaN, no infinities) and
+ *     scale format E8M0 (2^(s-127), s = 255 is NaN); one scale per block of
+ *     32 consecutive elements along the reduction dimension.
+ *
+ * Layouts (all row-major, no padding):
+ *   A  : M x K bytes        As : M x (K/32) bytes
+ *   B  : K x N bytes        Bs : N x (K/32) bytes
+ *
+ * Build: gcc -O2 -std=c11 -fPIC -shared -pthread -ffp-contract=off
+ * (-ffp-contract=off keeps every multiply and add separately rounded on
+ * every host, so the result does not depend on whether the compiler fuses.)
+ *
+ * Parity of the GPU path against this oracle is governed by a tolerance; the
+ * order in which the GPU accumulates is not modelled here.
+ */
+#include <math.h>
+#include <pthread.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+/* ---------------------------------------------------------------------- */
+/* Element and scale decoders, written from the format definitions.       */
+/* ---------------------------------------------------------------------- */
+
+/* E4M3: bit 7 sign, bits 6..3 exponent E (bias 7), bits 2..0 mantissa m.
+ *   E == 0          : (-1)^s * m * 2^-9            (subnormal, m/8 * 2^-6)
+ *   E != 0          : (-1)^s * (1 + m/8) * 2^(E-7)
+ *   E == 15, m == 7 : NaN (no infinities in this format)                  */
+double mxo_e4m3(uint8_t code) {
+  int s = (code >> 7) & 1;
+  int e = (code >> 3) & 15;
+  int m = code & 7;
+  double v;
+  if (e == 15 && m == 7) return NAN;
+  if (e == 0)
+    v = ldexp((double)m, -9);
+  else
+    v = ldexp(8.0 + (double)m, e - 7 - 3);
+  return s ? -v : v;
+}
+
+/* E8M0: an unsigned biased exponent with no sign and no mantissa.
+ *   s in [0, 254] : 2^(s - 127)     s == 255 : NaN                        */
+double mxo_e8m0(uint8_t code) {
+  if (code == 255) return NAN;
+  return ldexp(1.0, (int)code - 127);
+}
+
+/* ---------------------------------------------------------------------- */
+/* The product, for a set of full output rows.                             */
+/* ---------------------------------------------------------------------- */
+
+typedef struct {
+  int64_t M, N, K;
+  const uint8_t *A, *As, *B, *Bs;
+  const int64_t *rows; /* which rows of C to produce */
+  int64_t nrows;
+  double *ref, *bound; /* nrows x N each */
+  const double *lut_e4m3, *lut_e8m0;
+  int64_t r_begin, r_end; /* this worker's share of `rows` */
+} rows_job;
+
+static void *rows_worker(void *arg) {
+  rows_job *jb = (rows_job *)arg;
+  const int64_t N = jb->N, K = jb->K, KB = K / 32;
+  for (int64_t r = jb->r_begin; r < jb->r_end; ++r) {
+    const int64_t i = jb->rows[r];
+    double *acc = jb->ref + r * N;
+    double *bnd = jb->bound + r * N;
+    for (int64_t j = 0; j < N; ++j) {
+      acc[j] = 0.0;
+      bnd[j] = 0.0;
+    }
+    for (int64_t k = 0; k < K; ++k) {
+      /* a = e4m3(A[i][k]) * e8m0(As[i][k/32]) */
+      const double a = jb->lut_e4m3[jb->A[i * K + k]] *
+                       jb->lut_e8m0[jb->As[i * KB + k / 32]];
+      const uint8_t *brow = jb->B + k * N;
+      for (int64_t j = 0; j < N; ++j) {
+        /* b = e4m3(B[k][j]) * e8m0(Bs[j][k/32]) */
+        const double b =
+            jb->lut_e4m3[brow[j]] * jb->lut_e8m0[jb->Bs[j * KB + k / 32]];
+        const double t = a * b;
+        acc[j] += t;
+        bnd[j] += fabs(t);
+      }
+    }
+  }
+  return NULL;
+}
+
+static void build_luts(double *l4, double *l8) {
+  for (int c = 0; c < 256; ++c) {
+    l4[c] = mxo_e4m3((uint8_t)c);
+    l8[c] = mxo_e8m0((uint8_t)c);
+  }
+}
+
+/* Full rows `rows[0..nrows)` of the product.  ref and bound are nrows x N.
+ * Returns 0 on success, -1 on a bad argument. */
+int mxo_rows(int64_t M, int64_t N, int64_t K, const uint8_t *A,
+             const uint8_t *As, const uint8_t *B, const uint8_t *Bs,
+             int64_t nrows, const int64_t *rows, double *ref, double *bound,
+             int nthreads) {
+  if (M < 0 || N < 0 || K < 0 || K % 32 != 0 || nrows < 0) return -1;
+  for (int64_t r = 0; r < nrows; ++r)
+    if (rows[r] < 0 || rows[r] >= M) return -1;
+  double l4[256], l8[256];
+  build_luts(l4, l8);
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > nrows) nthreads = nrows > 0 ? (int)nrows : 1;
+  rows_job *jobs = (rows_job *)calloc((size_t)nthreads, sizeof(rows_job));
+  pthread_t *tid = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+  if (!jobs || !tid) {
+    free(jobs);
+    free(tid);
+    return -1;
+  }
+  for (int t = 0; t < nthreads; ++t) {
+    rows_job *jb = &jobs[t];
+    jb->M = M; jb->N = N; jb->K = K;
+    jb->A = A; jb->As = As; jb->B = B; jb->Bs = Bs;
+    jb->rows = rows; jb->nrows = nrows;
+    jb->ref = ref; jb->bound = bound;
+    jb->lut_e4m3 = l4; jb->lut_e8m0 = l8;
+    jb->r_begin = nrows * t / nthreads;
+    jb->r_end = nrows * (t + 1) / nthreads;
+  }
+  int started = 0;
+  for (int t = 1; t < nthreads; ++t) {
+    if (pthread_create(&tid[t], NULL, rows_worker, &jobs[t]) != 0) break;
+    started = t;
+  }
+  rows_worker(&jobs[0]);
+  for (int t = 1; t <= started; ++t) pthread_join(tid[t], NULL);
+  /* any share whose thread could not start runs here */
+  for (int t = started + 1; t < nthreads; ++t) rows_worker(&jobs[t]);
+  free(jobs);
+  free(tid);
+  return 0;
+}
+
+/* ---------------------------------------------------------------------- */
+/* The product at individual points (i, j): for checking sampled outputs.  */
+/* ---------------------------------------------------------------------- */
+
+typedef struct {
+  int64_t N, K;
+  const uint8_t *A, *As, *B, *Bs;
+  const int64_t *I, *J;
+  double *ref, *bound;
+  const double *lut_e4m3, *lut_e8m0;
+  int64_t p_begin, p_end;
+} points_job;
+
+static void *points_worker(void *arg) {
+  points_job *jb = (points_job *)arg;
+  const int64_t N = jb->N, K = jb->K, KB = K / 32;
+  for (int64_t p = jb->p_begin; p < jb->p_end; ++p) {
+    const int64_t i = jb->I[p], j = jb->J[p];
+    double acc = 0.0, bnd = 0.0;
+    for (int64_t k = 0; k < K; ++k) {
+      const double a = jb->lut_e4m3[jb->A[i * K + k]] *
+                       jb->lut_e8m0[jb->As[i * KB + k / 32]];
+      const double b = jb->lut_e4m3[jb->B[k * N + j]] *
+                       jb->lut_e8m0[jb->Bs[j * KB + k / 32]];
+      const double t = a * b;
+      acc += t;
+      bnd += fabs(t);
+    }
+    jb->ref[p] = acc;
+    jb->bound[p] = bnd;
+  }
+  return NULL;
+}
+
+int mxo_points(int64_t M, int64_t N, int64_t K, const uint8_t *A,
+               const uint8_t *As, const uint8_t *B, const uint8_t *Bs,
+               int64_t npts, const int64_t *I, const int64_t *J, double *ref,
+               double *bound, int nthreads) {
+  if (M < 0 || N < 0 || K < 0 || K % 32 != 0 || npts < 0) return -1;
+  for (int64_t p = 0; p < npts; ++p)
+    if (I[p] < 0 || I[p] >= M || J[p] < 0 || J[p] >= N) return -1;
+  double l4[256], l8[256];
+  build_luts(l4, l8);
+  if (nthreads < 1) nthreads = 1;
+  if (nthreads > npts) nthreads = npts > 0 ? (int)npts : 1;
+  points_job *jobs = (points_job *)calloc((size_t)nthreads, sizeof(points_job));
+  pthread_t *tid = (pthread_t *)calloc((size_t)nthreads, sizeof(pthread_t));
+  if (!jobs || !tid) {
+    free(jobs);
+    free(tid);
+    return -1;
+  }
+  for (int t = 0; t < nthreads; ++t) {
+    points_job *jb = &jobs[t];
+    jb->N = N; jb->K = K;
+    jb->A = A; jb->As = As; jb->B = B; jb->Bs = Bs;
+    jb->I = I; jb->J = J;
+    jb->ref = ref; jb->bound = bound;
+    jb->lut_e4m3 = l4; jb->lut_e8m0 = l8;
+    jb->p_begin = npts * t / nthreads;
+    jb->p_end = npts * (t + 1) / nthreads;
+  }
+  int started = 0;
+  for (int t = 1; t < nthreads; ++t) {
+    if (pthread_create(&tid[t], NULL, points_worker, &jobs[t]) != 0) break;
+    started = t;
+  }
+  points_worker(&jobs[0]);
+  for (int t = 1; t <= started; ++t) pthread_join(tid[t], NULL);
+  for (int t = started + 1; t < nthreads; ++t) points_worker(&jobs[t]);
+  free(jobs);
+  free(tid);
+  return 0;
+}
+
+/* ---------------------------------------------------------------------- */
+/* Output rounding: double -> binary32 / bfloat16, round to nearest even.  */
+/* ---------------------------------------------------------------------- */
+
+/* binary32: the C conversion rounds to nearest-even under the default
+ * floating-point environment (overflow gives +-inf). */
+float mxo_round_f32(double x) { return (float)x; }
+
+/* bfloat16 (1 sign, 8 exponent bits, 7 stored mantissa bits), written out
+ * from its definition: keep 8 significant bits, round to nearest, ties to
+ * even, values past the largest finite bfloat16 become infinities, results
+ * below 2^-126 keep 8 - (extra exponent) bits (gradual underflow).
+ * Returns the 16-bit pattern. */
+uint16_t mxo_round_bf16(double x) {
+  uint16_t sign = signbit(x) ? 0x8000u : 0u;
+  double ax = fabs(x);
+  if (isnan(x)) return (uint16_t)(sign | 0x7FC0u);
+  if (isinf(x)) return (uint16_t)(sign | 0x7F80u);
+  if (ax == 0.0) return sign;
+  int e;
+  (void)frexp(ax, &e); /* ax = f * 2^e, f in [0.5, 1) -> unbiased exp e-1 */
+  int ue = e - 1;
+  if (ue < -126) ue = -126; /* subnormal range: fixed quantum 2^-133 */
+  /* quantum of the 8-bit significand at this exponent */
+  double q = ldexp(1.0, ue - 7);
+  double n = nearbyint(ax / q); /* ax/q is exact: a power-of-2 scaling */
+  double r = n * q;             /* rounded magnitude (may carry to 2^(ue+1)) */
+  if (r == 0.0) return sign;    /* underflow to a signed zero */
+  /* largest finite bfloat16: (2 - 2^-7) * 2^127 */
+  if (r > ldexp(255.0, 127 - 7)) return (uint16_t)(sign | 0x7F80u);
+  /* encode r */
+  int re;
+  (void)frexp(r, &re);
+  int rexp = re - 1;
+  uint16_t bits;
+  if (rexp < -126) {
+    /* subnormal: r = mant * 2^-133 with mant < 128 */
+    bits = (uint16_t)(int)ldexp(r, 133);
+  } else {
+    double frac = ldexp(r, -rexp) - 1.0; /* in [0,1) */
+    bits = (uint16_t)(((rexp + 127) << 7) | (int)ldexp(frac, 7));
+  }
+  return (uint16_t)(sign | bits);
+}
+
+void mxo_round_bf16_array(const double *x, uint16_t *out, int64_t n) {
+  for (int64_t i = 0; i < n; ++i) out[i] = mxo_round_bf16(x[i]);
+}

@@ -1,0 +1,274 @@
+"""Pins for the CPU oracle: each test checks the oracle against something other
+than itself -- values worked by hand from the format definitions, an
+independent library decode, closed forms, exact integer and exact-rational
+arithmetic, and identities the definition implies.
+
+Together they are chosen so that a plausible slip anywhere in the oracle (a
+wrong bias or sign in a decoder, a dropped subnormal, a scale indexed by the
+wrong row/column or block, a transposed operand, a lost term of the sum)
+fails at least one of them.
+"""
+from fractions import Fraction
+from pathlib import Path
+
+import numpy as np
+import pytest
+import torch
+
+import mx_inputs as mi
+import oracle
+
+GOLDEN = Path(__file__).parent / "golden"
+
+
+def _golden_values():
+    rows = []
+    for line in (GOLDEN / "e4m3_e8m0_values.txt").read_text().splitlines():
+        if not line.strip() or line.startswith("#"):
+            continue
+        fmt, code, val = line.split()
+        rows.append((fmt, int(code, 16), float(val)))
+    return rows
+
+
+@pytest.mark.parametrize("fmt,code,val", _golden_values())
+def test_decoder_spot_values(fmt, code, val):
+    got = oracle.e4m3(code) if fmt == "e4m3" else oracle.e8m0(code)
+    if np.isnan(val):
+        assert np.isnan(got)
+    else:
+        assert got == val
+        assert np.signbit(got) == np.signbit(val)
+
+
+def test_e4m3_all_codes_match_library_decode():
+    # torch's float8_e4m3fn is an independent implementation of the same format
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    lib = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    ours = np.array([oracle.e4m3(c) for c in range(256)])
+    nan = np.isnan(lib)
+    assert np.array_equal(nan, np.isnan(ours))
+    assert set(np.nonzero(nan)[0].tolist()) == {0x7F, 0xFF}
+    assert np.array_equal(lib[~nan], ours[~nan])
+    assert np.array_equal(np.signbit(lib[~nan]), np.signbit(ours[~nan]))
+    # 254 finite codes, max 448, smallest positive 2^-9 (subnormal)
+    fin = ours[~nan]
+    assert fin.max() == 448.0 and fin.min() == -448.0
+    assert fin[fin > 0].min() == 2.0 ** -9
+
+
+def test_e8m0_all_codes_closed_form():
+    for s in range(255):
+        assert oracle.e8m0(s) == float(Fraction(2) ** (s - 127))
+    assert np.isnan(oracle.e8m0(255))
+
+
+def _tiny_cases():
+    cases = []
+    for line in (GOLDEN / "tiny_cases.txt").read_text().splitlines():
+        if not line.strip() or line.startswith("#"):
+            continue
+        name, K, a, b, exact, f32 = [x.strip() for x in line.split("|")]
+        cases.append((name, int(K), a, b, float(exact), float(f32)))
+    return cases
+
+
+def _operand_from_blocks(spec: str, K: int):
+    codes = np.zeros(K, dtype=np.uint8)
+    scales = np.zeros(K // 32, dtype=np.uint8)
+    for kb, blk in enumerate(spec.split(",")):
+        code, sc = blk.split(":")
+        if "@0" in code:
+            codes[kb * 32] = int(code.split("@")[0], 16)
+        else:
+            codes[kb * 32:(kb + 1) * 32] = int(code, 16)
+        scales[kb] = int(sc)
+    return codes, scales
+
+
+@pytest.mark.parametrize("name,K,a,b,exact,f32", _tiny_cases())
+def test_hand_computed_tiny_cases(name, K, a, b, exact, f32):
+    ac, asc = _operand_from_blocks(a, K)
+    bc, bsc = _operand_from_blocks(b, K)
+    A = ac.reshape(1, K)
+    B = bc.reshape(K, 1)
+    ref, bound = oracle.rows(A, asc.reshape(1, -1), B, bsc.reshape(1, -1))
+    assert ref[0, 0] == exact
+    assert float(oracle.round_f32(ref)[0, 0]) == f32
+    # every case here has terms of one sign within each block: bound = sum |terms|
+    assert bound[0, 0] >= abs(ref[0, 0])
+
+
+def _decode_lib(codes: np.ndarray) -> np.ndarray:
+    return torch.from_numpy(np.ascontiguousarray(codes)).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+
+
+def test_all_scales_127_is_plain_fp8_matmul():
+    p = mi.random_problem(37, 45, 160, seed=3, kind="codes", scale_lo=127, scale_hi=127)
+    ref, bound = oracle.rows(p.A, p.As, p.B, p.Bs)
+    lib = _decode_lib(p.A.numpy()) @ _decode_lib(p.B.numpy())
+    # same exact products; only the summation order may differ
+    assert np.all(np.abs(ref - lib) <= 1e-13 * bound)
+
+
+def test_exact_small_integers_equal_int64_matmul():
+    p = mi.random_problem(29, 51, 4096, seed=5, kind="int")
+    ai = _decode_lib(p.A.numpy()).astype(np.int64)
+    bi = _decode_lib(p.B.numpy()).astype(np.int64)
+    assert np.array_equal(_decode_lib(p.A.numpy()), ai.astype(np.float64))
+    ref, _ = oracle.rows(p.A, p.As, p.B, p.Bs)
+    assert np.array_equal(ref, (ai @ bi).astype(np.float64))
+
+
+def test_brute_force_exact_rationals_tiny():
+    # every finite code and extreme scales, summed exactly with Fractions
+    g = torch.Generator().manual_seed(11)
+    M, N, K = 3, 4, 64
+    A = mi.finite_codes(M * K, g).reshape(M, K).numpy()
+    B = mi.finite_codes(K * N, g).reshape(K, N).numpy()
+    choices = np.array([0, 1, 120, 127, 134, 253, 254], dtype=np.uint8)
+    As = choices[torch.randint(0, len(choices), (M, K // 32), generator=g).numpy()]
+    Bs = choices[torch.randint(0, len(choices), (N, K // 32), generator=g).numpy()]
+    ref, bound = oracle.rows(A, As, B, Bs)
+    da, db = _decode_lib(A), _decode_lib(B)
+    for i in range(M):
+        for j in range(N):
+            exact = Fraction(0)
+            absum = Fraction(0)
+            for k in range(K):
+                t = (Fraction(da[i, k]) * Fraction(2) ** (int(As[i, k // 32]) - 127)
+                     * Fraction(db[k, j]) * Fraction(2) ** (int(Bs[j, k // 32]) - 127))
+                exact += t
+                absum += abs(t)
+            assert float(absum) == pytest.approx(bound[i, j], rel=1e-15)
+            # double accumulation: error at most K * 2^-53 * sum|t|
+            assert abs(Fraction(ref[i, j]) - exact) <= Fraction(K, 2 ** 53) * absum
+
+
+def test_scale_shift_linearity_rows_columns_blocks():
+    p = mi.random_problem(16, 24, 128, seed=7, kind="normal", scale_lo=124, scale_hi=130)
+    ref, _ = oracle.rows(p.A, p.As, p.B, p.Bs)
+    # one row of A_scale shifted by d multiplies that row of C by exactly 2^d
+    i, d = 5, 3
+    As2 = p.As.clone()
+    As2[i] += d
+    r2, _ = oracle.rows(p.A, As2, p.B, p.Bs)
+    assert np.array_equal(r2[i], ref[i] * 2.0 ** d)
+    assert np.array_equal(np.delete(r2, i, 0), np.delete(ref, i, 0))
+    # one row of B_scale (= column j of B) shifted by d: column j scales by 2^d
+    j, d = 17, -4
+    Bs2 = p.Bs.clone()
+    Bs2[j] = (Bs2[j].to(torch.int32) + d).to(torch.uint8)
+    r3, _ = oracle.rows(p.A, p.As, p.B, Bs2)
+    assert np.array_equal(r3[:, j], ref[:, j] * 2.0 ** d)
+    assert np.array_equal(np.delete(r3, j, 1), np.delete(ref, j, 1))
+    # a single k-block: only that block's contribution scales
+    kb, d = 2, 2
+    A_blk = p.A.clone()
+    keep = torch.zeros_like(A_blk)
+    keep[:, kb * 32:(kb + 1) * 32] = A_blk[:, kb * 32:(kb + 1) * 32]
+    c_blk, _ = oracle.rows(keep, p.As, p.B, p.Bs)
+    As3 = p.As.clone()
+    As3[:, kb] += d
+    c_blk2, _ = oracle.rows(keep, As3, p.B, p.Bs)
+    assert np.array_equal(c_blk2, c_blk * 2.0 ** d)
+
+
+def test_transpose_symmetry():
+    # C^T = (B^T with scales Bs) x (A^T with scales As): roles swapped
+    p = mi.random_problem(19, 33, 96, seed=9, kind="codes")
+    ref, _ = oracle.rows(p.A, p.As, p.B, p.Bs)
+    refT, _ = oracle.rows(p.B.t().contiguous(), p.Bs, p.A.t().contiguous(), p.As)
+    assert np.array_equal(refT, ref.T)
+
+
+def test_k_split_additivity_and_use_acc():
+    p = mi.random_problem(12, 20, 256, seed=13, kind="codes")
+    full, bfull = oracle.rows(p.A, p.As, p.B, p.Bs)
+    half = 128
+    a1, a2 = p.A[:, :half].contiguous(), p.A[:, half:].contiguous()
+    s1, s2 = p.As[:, :half // 32].contiguous(), p.As[:, half // 32:].contiguous()
+    b1, b2 = p.B[:half].contiguous(), p.B[half:].contiguous()
+    t1, t2 = p.Bs[:, :half // 32].contiguous(), p.Bs[:, half // 32:].contiguous()
+    r1, bd1 = oracle.rows(a1, s1, b1, t1)
+    r2, bd2 = oracle.rows(a2, s2, b2, t2, c_in=r1)
+    assert np.all(np.abs(r2 - full) <= 1e-14 * bfull)
+    # with use_acc the bound counts |C_in| itself, which is at most C_in's own bound
+    assert np.all(bd2 <= bfull * (1 + 1e-14))
+    r2_alone, bd2_alone = oracle.rows(a2, s2, b2, t2)
+    assert np.array_equal(r2, r2_alone + r1)
+    assert np.array_equal(bd2, bd2_alone + np.abs(r1))
+
+
+def test_points_match_rows():
+    p = mi.random_problem(40, 50, 192, seed=17, kind="codes")
+    ref, bound = oracle.rows(p.A, p.As, p.B, p.Bs)
+    I = np.array([0, 39, 7, 20, 39])
+    J = np.array([0, 49, 31, 0, 1])
+    r, b = oracle.points(p.A, p.As, p.B, p.Bs, I, J)
+    assert np.array_equal(r, ref[I, J]) and np.array_equal(b, bound[I, J])
+
+
+def test_round_bf16_matches_library_on_binary32_inputs():
+    # for inputs exactly representable in binary32, torch's fp32 -> bf16
+    # conversion (round to nearest even) is an independent reference
+    g = torch.Generator().manual_seed(19)
+    x = torch.randn(20000, generator=g, dtype=torch.float32) * torch.pow(
+        2.0, torch.randint(-140, 130, (20000,), generator=g).to(torch.float32))
+    extra = torch.tensor([0.0, -0.0, 1.0, 1.00390625, 1.01171875, 1.0078125, 3.3895314e38,
+                          3.39e38, float("inf"), -float("inf"), 1e-40, -3e-39], dtype=torch.float32)
+    x = torch.cat([x, extra])
+    lib = x.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    ours = oracle.round_bf16_bits(x.to(torch.float64).numpy())
+    assert np.array_equal(lib, ours)
+
+
+def test_round_bf16_ties_from_double():
+    # 1 + 2^-8 is a tie between 1 and 1 + 2^-7: nearest even is 1.0
+    # 1 + 2^-8 + 2^-40 is above the tie: rounds up (a binary32 first step
+    # would have lost the 2^-40 and rounded down)
+    assert oracle.round_bf16_bits([1.0 + 2 ** -8])[0] == 0x3F80
+    assert oracle.round_bf16_bits([1.0 + 2 ** -8 + 2 ** -40])[0] == 0x3F81
+    assert oracle.round_bf16_bits([1.0 + 3 * 2 ** -8])[0] == 0x3F82
+
+
+def test_accept_flags_a_wrong_element():
+    p = mi.random_problem(8, 8, 64, seed=23, kind="normal")
+    ref, bound = oracle.rows(p.A, p.As, p.B, p.Bs)
+    out = oracle.round_f32(ref)
+    assert oracle.accept(out, ref, bound, "f32")["ok"]
+    bad = out.copy()
+    bad[3, 4] += 1e-3 * bound[3, 4]
+    st = oracle.accept(bad, ref, bound, "f32")
+    assert not st["ok"] and st["first_bad"] == [3, 4]
+    # bf16: 2^-8 relative slack
+    bits = oracle.round_bf16_bits(ref)
+    assert oracle.accept(bits, ref, bound, "bf16")["ok"]
+
+
+def test_accept_overflow_class():
+    ref = np.array([1e45, 1.0])
+    bound = np.array([2e45, 1.0])
+    assert oracle.accept(np.array([np.inf, 1.0]), ref, bound, "f32")["ok"]
+    assert oracle.accept(np.array([np.nan, 1.0]), ref, bound, "f32")["ok"]
+    assert not oracle.accept(np.array([np.inf, np.nan]), ref, bound, "f32")["ok"]
+
+
+def test_quantizer_recipe_roundtrip():
+    # the generator's quantizer must give finite codes with |code value| <= 448
+    # and reproduce each block within one E4M3 half-ulp after rescaling
+    g = torch.Generator().manual_seed(29)
+    x = torch.randn(64, 256, generator=g)
+    codes, sc = mi.quantize_rows(x)
+    dec = _decode_lib(codes.numpy())
+    assert np.isfinite(dec).all() and np.abs(dec).max() <= 448
+    scale = 2.0 ** (sc.numpy().astype(np.float64) - 127)
+    recon = dec * np.repeat(scale, 32, axis=1)
+    rel = np.abs(recon - x.numpy()) / np.repeat(scale, 32, axis=1)
+    # E4M3 has 3 mantissa bits: half-ulp of a value v is <= |v| * 2^-4,
+    # plus the subnormal quantum 2^-10 for small codes
+    assert np.all(rel <= np.abs(dec) * 2 ** -4 + 2 ** -10 + 1e-12)
+    # the block maximum lands in [224, 448] (pre-rounding it is in (224, 448]):
+    # the scale is the smallest power of two that fits the block
+    blkmax = np.abs(dec).reshape(64, 8, 32).max(axis=2)
+    assert np.all((blkmax >= 224) & (blkmax <= 448))
