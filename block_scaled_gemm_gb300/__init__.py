@@ -1,0 +1,186 @@
+"""Python binding of the GB300 MX block-scaled FP8 GEMM C library.
+
+Argument marshalling only: every step of the product runs in the CUDA
+library ``libmxgemm.so`` (built from ``csrc/`` by ``_build.build()``); there is
+no fallback.  The functions mirror the C interface of ``include/mxgemm.h``:
+
+    h = mxgemm_create(device)
+    mxgemm_run(h, M, N, K, A, A_scale, B, B_scale, C, use_acc, out_dtype, stream)
+    mxgemm_destroy(h)
+
+Tensor arguments may be anything with ``data_ptr()`` (torch CUDA tensors) or
+raw integer device addresses.  ``stream`` may be a ``torch.cuda.Stream``, a
+raw ``cudaStream_t`` integer, or None (the legacy default stream).
+The operation is the scaled product documented as ``tlx.async_dot_scaled``
+("TLX API Quick Reference", section "Matrix Multiply (MMA)").
+"""
+from __future__ import annotations
+
+import ctypes
+from pathlib import Path
+
+from . import _build
+
+__all__ = [
+    "OUT_F32", "OUT_BF16", "OPT_MODE", "OPT_WAIT_TIMEOUT_NS", "OPT_TEST_STALL_PRODUCER",
+    "OPT_SCHEDULER", "MxgemmError", "library", "library_path", "mxgemm_create", "mxgemm_run",
+    "mxgemm_destroy", "mxgemm_set_option", "mxgemm_get_device_status", "mxgemm_status_string",
+    "EXPORTED_SYMBOLS", "Gemm",
+]
+
+OUT_F32 = 0
+OUT_BF16 = 1
+
+OPT_MODE = 1
+OPT_WAIT_TIMEOUT_NS = 2
+OPT_TEST_STALL_PRODUCER = 3
+OPT_SCHEDULER = 4
+
+OK = 0
+ERR_INVALID_VALUE = 1
+ERR_MISALIGNED = 2
+ERR_UNSUPPORTED_DEVICE = 3
+ERR_OUT_OF_MEMORY = 4
+ERR_CUDA = 5
+ERR_TIMEOUT = 6
+
+EXPORTED_SYMBOLS = (
+    "mxgemm_create", "mxgemm_run", "mxgemm_destroy", "mxgemm_set_option",
+    "mxgemm_get_device_status", "mxgemm_status_string",
+)
+
+_lib = None
+
+
+class MxgemmError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        self.status = status
+        super().__init__(f"{where}: {mxgemm_status_string(status)} (status {status})")
+
+
+def library_path() -> Path:
+    return _build.LIB
+
+
+def library():
+    """Load the CUDA library; raises if it has not been built."""
+    global _lib
+    if _lib is None:
+        path = _build.LIB
+        if not path.exists():
+            raise RuntimeError(
+                f"CUDA library {path} is missing: build it with "
+                "`python -m block_scaled_gemm_gb300._build` (there is no CPU fallback)")
+        lib = ctypes.CDLL(str(path))
+        vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        lib.mxgemm_create.argtypes = [ctypes.POINTER(vp), i32]
+        lib.mxgemm_create.restype = i32
+        lib.mxgemm_run.argtypes = [vp, i64, i64, i64, vp, vp, vp, vp, vp, i32, i32, vp]
+        lib.mxgemm_run.restype = i32
+        lib.mxgemm_destroy.argtypes = [vp]
+        lib.mxgemm_destroy.restype = i32
+        lib.mxgemm_set_option.argtypes = [vp, i32, i64]
+        lib.mxgemm_set_option.restype = i32
+        lib.mxgemm_get_device_status.argtypes = [vp, vp, ctypes.POINTER(i32), ctypes.POINTER(i32)]
+        lib.mxgemm_get_device_status.restype = i32
+        lib.mxgemm_status_string.argtypes = [i32]
+        lib.mxgemm_status_string.restype = ctypes.c_char_p
+        _lib = lib
+    return _lib
+
+
+def mxgemm_status_string(status: int) -> str:
+    return library().mxgemm_status_string(int(status)).decode()
+
+
+def _ptr(x):
+    if x is None:
+        return None
+    if isinstance(x, int):
+        return x
+    return x.data_ptr()
+
+
+def _stream(s):
+    if s is None:
+        return None
+    if isinstance(s, int):
+        return s
+    return s.cuda_stream
+
+
+def _check(st: int, where: str):
+    if st != OK:
+        raise MxgemmError(st, where)
+
+
+def mxgemm_create(device: int = 0):
+    h = ctypes.c_void_p()
+    _check(library().mxgemm_create(ctypes.byref(h), int(device)), "mxgemm_create")
+    return h
+
+
+def mxgemm_run(h, M, N, K, A, A_scale, B, B_scale, C, use_acc=0, out_dtype=OUT_F32, stream=None,
+               check: bool = True) -> int:
+    st = library().mxgemm_run(h, int(M), int(N), int(K), _ptr(A), _ptr(A_scale), _ptr(B),
+                              _ptr(B_scale), _ptr(C), int(bool(use_acc)), int(out_dtype),
+                              _stream(stream))
+    if check:
+        _check(st, "mxgemm_run")
+    return st
+
+
+def mxgemm_set_option(h, option: int, value: int) -> None:
+    _check(library().mxgemm_set_option(h, int(option), int(value)), "mxgemm_set_option")
+
+
+def mxgemm_get_device_status(h, stream=None):
+    st, det = ctypes.c_int(), ctypes.c_int()
+    _check(library().mxgemm_get_device_status(h, _stream(stream), ctypes.byref(st), ctypes.byref(det)),
+           "mxgemm_get_device_status")
+    return st.value, det.value
+
+
+def mxgemm_destroy(h) -> None:
+    _check(library().mxgemm_destroy(h), "mxgemm_destroy")
+
+
+class Gemm:
+    """Owns one handle.  ``g(A, As, B, Bs, C, use_acc, out_dtype)`` enqueues
+    C (+)= A.B on the current torch stream (shapes taken from the tensors)."""
+
+    def __init__(self, device: int = 0, mode: int | None = None):
+        self.h = mxgemm_create(device)
+        if mode is not None:
+            mxgemm_set_option(self.h, OPT_MODE, mode)
+
+    def __call__(self, A, A_scale, B, B_scale, C, use_acc=False, out_dtype=OUT_F32, stream=None):
+        M, K = A.shape
+        N = B.shape[1]
+        if stream is None:
+            import torch
+            stream = torch.cuda.current_stream(A.device)
+        return mxgemm_run(self.h, M, N, K, A, A_scale, B, B_scale, C, use_acc, out_dtype, stream)
+
+    def set_option(self, option: int, value: int):
+        mxgemm_set_option(self.h, option, value)
+
+    def status(self, stream=None):
+        return mxgemm_get_device_status(self.h, stream)
+
+    def close(self):
+        if self.h is not None:
+            mxgemm_destroy(self.h)
+            self.h = None
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

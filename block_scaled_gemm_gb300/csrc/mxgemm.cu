@@ -1,0 +1,364 @@
+// mxgemm.cu -- host side of the C interface declared in include/mxgemm.h:
+// argument validation, tile-mode planning, workspace, tensor-map encoding and
+// the launches (scale repack, optional B row padding, the GEMM kernel).
+//
+// The operation is the scaled product `async_dot_scaled` of the "TLX API
+// Quick Reference" (section "Matrix Multiply (MMA)"); the pair mode is the
+// "2-CTA Scaled MMA" of "Tensor core operations".
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstdlib>
+#include <cstring>
+#include <new>
+
+#include "mxgemm.h"
+#include "mxgemm_kernel.cuh"
+
+namespace {
+
+using mxg::Cfg;
+using mxg::KParams;
+
+struct Workspace {
+  uint8_t *ptr = nullptr;
+  size_t bytes = 0;
+};
+
+}  // namespace
+
+struct mxgemm_ctx {
+  int device = 0;
+  int sm_count = 0;
+  int *d_status = nullptr;  // [0] status code, [1] detail
+  Workspace ws;
+  PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
+  long long timeout_ns = 2000000000LL;
+  int mode = 0;
+  int stall_producer = 0;
+  int scheduler = 0;
+  bool attr_set[3] = {false, false, false};
+};
+
+namespace {
+
+struct DeviceGuard {
+  int prev = -1;
+  bool changed = false;
+  explicit DeviceGuard(int dev) {
+    if (cudaGetDevice(&prev) == cudaSuccess && prev != dev) {
+      changed = cudaSetDevice(dev) == cudaSuccess;
+    }
+  }
+  ~DeviceGuard() {
+    if (changed) cudaSetDevice(prev);
+  }
+};
+
+inline int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+inline size_t round_up(size_t a, size_t b) { return (a + b - 1) / b * b; }
+
+bool on_device(const void *p, int device) {
+  cudaPointerAttributes attr;
+  if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return (attr.type == cudaMemoryTypeDevice || attr.type == cudaMemoryTypeManaged) &&
+         attr.device == device;
+}
+
+// 2-D uint8 tensor map: dims {inner, outer}, row pitch in bytes, box.
+int encode_2d(mxgemm_ctx *h, CUtensorMap *tm, const void *base, uint64_t inner, uint64_t outer,
+              uint64_t pitch, uint32_t box_inner, uint32_t box_outer, bool swizzle128) {
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {pitch};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = h->encode(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims,
+                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                         swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? MXGEMM_OK : MXGEMM_ERR_CUDA;
+}
+
+int ensure_workspace(mxgemm_ctx *h, size_t bytes, cudaStream_t stream) {
+  if (h->ws.bytes >= bytes) return MXGEMM_OK;
+  if (h->ws.ptr) {
+    // stream-ordered: earlier work on this stream still using it finishes first
+    cudaFreeAsync(h->ws.ptr, stream);
+    h->ws.ptr = nullptr;
+    h->ws.bytes = 0;
+  }
+  void *p = nullptr;
+  size_t want = round_up(bytes, size_t(2) << 20);
+  if (cudaMallocAsync(&p, want, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return MXGEMM_ERR_OUT_OF_MEMORY;
+  }
+  h->ws.ptr = static_cast<uint8_t *>(p);
+  h->ws.bytes = want;
+  return MXGEMM_OK;
+}
+
+template <int CG>
+int launch_gemm(mxgemm_ctx *h, const CUtensorMap &tA, const CUtensorMap &tB,
+                const CUtensorMap &tSA, const CUtensorMap &tSB, const KParams &kp,
+                cudaStream_t stream) {
+  using C = Cfg<CG>;
+  auto kern = mxg::mxgemm_kernel<CG>;
+  if (!h->attr_set[CG]) {
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
+        cudaSuccess) {
+      cudaGetLastError();
+      return MXGEMM_ERR_CUDA;
+    }
+    h->attr_set[CG] = true;
+  }
+  const int units = h->sm_count / CG;
+  const int clusters = kp.num_tiles < units ? kp.num_tiles : units;
+  cudaLaunchConfig_t cfg;
+  std::memset(&cfg, 0, sizeof(cfg));
+  cfg.gridDim = dim3(static_cast<unsigned>(clusters * CG), 1, 1);
+  cfg.blockDim = dim3(C::THREADS, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  cfg.numAttrs = 0;
+  if (CG == 2) {
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tA, tB, tSA, tSB, kp);
+  if (e != cudaSuccess) {
+    cudaGetLastError();
+    return MXGEMM_ERR_CUDA;
+  }
+  return MXGEMM_OK;
+}
+
+int launch_blocks(int64_t work, int per_block) {
+  int64_t b = cdiv(work, per_block);
+  if (b < 1) b = 1;
+  if (b > 4096) b = 4096;
+  return static_cast<int>(b);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *mxgemm_status_string(int s) {
+  switch (s) {
+    case MXGEMM_OK: return "ok";
+    case MXGEMM_ERR_INVALID_VALUE: return "invalid value";
+    case MXGEMM_ERR_MISALIGNED: return "misaligned pointer (A, B and C need 16-byte alignment)";
+    case MXGEMM_ERR_UNSUPPORTED_DEVICE: return "unsupported device (needs compute capability 10.3)";
+    case MXGEMM_ERR_OUT_OF_MEMORY: return "out of device memory";
+    case MXGEMM_ERR_CUDA: return "CUDA call failed";
+    case MXGEMM_ERR_TIMEOUT: return "device-side wait timed out";
+    default: return "unknown status";
+  }
+}
+
+int mxgemm_create(mxgemm_handle_t *out, int device) {
+  if (!out) return MXGEMM_ERR_INVALID_VALUE;
+  *out = nullptr;
+  int ndev = 0;
+  if (cudaGetDeviceCount(&ndev) != cudaSuccess) {
+    cudaGetLastError();
+    return MXGEMM_ERR_CUDA;
+  }
+  if (device < 0 || device >= ndev) return MXGEMM_ERR_INVALID_VALUE;
+  cudaDeviceProp prop;
+  if (cudaGetDeviceProperties(&prop, device) != cudaSuccess) return MXGEMM_ERR_CUDA;
+  if (!(prop.major == 10 && prop.minor == 3)) return MXGEMM_ERR_UNSUPPORTED_DEVICE;
+
+  DeviceGuard g(device);
+  mxgemm_ctx *h = new (std::nothrow) mxgemm_ctx();
+  if (!h) return MXGEMM_ERR_OUT_OF_MEMORY;
+  h->device = device;
+  h->sm_count = prop.multiProcessorCount;
+  if (const char *t = std::getenv("MXGEMM_WAIT_TIMEOUT_NS")) {
+    long long v = std::atoll(t);
+    if (v > 0) h->timeout_ns = v;
+  }
+  void *fn = nullptr;
+  cudaDriverEntryPointQueryResult q;
+  if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                       &q) != cudaSuccess ||
+      q != cudaDriverEntryPointSuccess || !fn) {
+    delete h;
+    return MXGEMM_ERR_CUDA;
+  }
+  h->encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  if (cudaMalloc(&h->d_status, 2 * sizeof(int)) != cudaSuccess) {
+    delete h;
+    return MXGEMM_ERR_OUT_OF_MEMORY;
+  }
+  if (cudaMemset(h->d_status, 0, 2 * sizeof(int)) != cudaSuccess) {
+    cudaFree(h->d_status);
+    delete h;
+    return MXGEMM_ERR_CUDA;
+  }
+  *out = h;
+  return MXGEMM_OK;
+}
+
+int mxgemm_set_option(mxgemm_handle_t h, int option, int64_t value) {
+  if (!h) return MXGEMM_ERR_INVALID_VALUE;
+  switch (option) {
+    case MXGEMM_OPT_MODE:
+      if (value < 0 || value > 2) return MXGEMM_ERR_INVALID_VALUE;
+      h->mode = static_cast<int>(value);
+      return MXGEMM_OK;
+    case MXGEMM_OPT_WAIT_TIMEOUT_NS:
+      if (value <= 0) return MXGEMM_ERR_INVALID_VALUE;
+      h->timeout_ns = value;
+      return MXGEMM_OK;
+    case MXGEMM_OPT_TEST_STALL_PRODUCER:
+      if (value < 0 || value > 1) return MXGEMM_ERR_INVALID_VALUE;
+      h->stall_producer = static_cast<int>(value);
+      return MXGEMM_OK;
+    case MXGEMM_OPT_SCHEDULER:
+      if (value < 0 || value > 1) return MXGEMM_ERR_INVALID_VALUE;
+      h->scheduler = static_cast<int>(value);
+      return MXGEMM_OK;
+    default:
+      return MXGEMM_ERR_INVALID_VALUE;
+  }
+}
+
+int mxgemm_run(mxgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A,
+               const void *A_scale, const void *B, const void *B_scale, void *C, int use_acc,
+               int out_dtype, mxgemm_stream_t stream_) {
+  if (!h) return MXGEMM_ERR_INVALID_VALUE;
+  const int64_t lim = int64_t(1) << 31;
+  if (M < 0 || N < 0 || K < 0 || M >= lim || N >= lim || K >= lim) return MXGEMM_ERR_INVALID_VALUE;
+  if (K % 32 != 0) return MXGEMM_ERR_INVALID_VALUE;
+  if (out_dtype != MXGEMM_OUT_F32 && out_dtype != MXGEMM_OUT_BF16) return MXGEMM_ERR_INVALID_VALUE;
+  if (use_acc != 0 && use_acc != 1) return MXGEMM_ERR_INVALID_VALUE;
+  if (M == 0 || N == 0) return MXGEMM_OK;
+  const size_t esz = out_dtype == MXGEMM_OUT_F32 ? 4 : 2;
+  if (!C) return MXGEMM_ERR_INVALID_VALUE;
+  if (reinterpret_cast<uintptr_t>(C) % 16) return MXGEMM_ERR_MISALIGNED;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  DeviceGuard g(h->device);
+  if (!on_device(C, h->device)) return MXGEMM_ERR_INVALID_VALUE;
+  if (K == 0) {
+    if (use_acc) return MXGEMM_OK;
+    if (cudaMemsetAsync(C, 0, static_cast<size_t>(M) * N * esz, stream) != cudaSuccess) {
+      cudaGetLastError();
+      return MXGEMM_ERR_CUDA;
+    }
+    return MXGEMM_OK;
+  }
+  if (!A || !B || !A_scale || !B_scale) return MXGEMM_ERR_INVALID_VALUE;
+  if (reinterpret_cast<uintptr_t>(A) % 16 || reinterpret_cast<uintptr_t>(B) % 16)
+    return MXGEMM_ERR_MISALIGNED;
+  if (!on_device(A, h->device) || !on_device(B, h->device) || !on_device(A_scale, h->device) ||
+      !on_device(B_scale, h->device))
+    return MXGEMM_ERR_INVALID_VALUE;
+
+  // ---- plan
+  int CG = 1;
+  if (h->mode == 2) CG = 2;
+  // mode 0 (automatic) currently selects the single-CTA tile
+  const int64_t m_tiles = cdiv(M, 128 * CG);
+  const int64_t n_tiles = cdiv(N, 256);
+  const int64_t k_steps = cdiv(K, 128);
+  const int64_t num_tiles = m_tiles * n_tiles;
+  if (num_tiles >= lim) return MXGEMM_ERR_INVALID_VALUE;
+  const int64_t kb = K / 32;
+  const int64_t a_chunks = m_tiles * CG * k_steps;      // 512-byte chunks of A scales
+  const int64_t b_chunks = n_tiles * k_steps * 2;       // 2 per 256 columns
+  const bool pad_b = (N % 16) != 0;
+  const int64_t npad = round_up(static_cast<size_t>(N), 16);
+  const size_t off_sfa = 0;
+  const size_t off_sfb = round_up(static_cast<size_t>(a_chunks) * 512, 1024);
+  const size_t off_b = round_up(off_sfb + static_cast<size_t>(b_chunks) * 512, 1024);
+  const size_t ws_bytes = off_b + (pad_b ? static_cast<size_t>(K) * npad : 0);
+  int st = ensure_workspace(h, ws_bytes, stream);
+  if (st != MXGEMM_OK) return st;
+  uint8_t *sfa = h->ws.ptr + off_sfa;
+  uint8_t *sfb = h->ws.ptr + off_sfb;
+  const uint8_t *bsrc = static_cast<const uint8_t *>(B);
+  int64_t bpitch = N;
+  if (pad_b) {
+    uint8_t *bp = h->ws.ptr + off_b;
+    mxg::pad_rows_kernel<<<launch_blocks(K * (npad / 16), 256), 256, 0, stream>>>(
+        static_cast<const uint8_t *>(B), K, N, npad, bp);
+    bsrc = bp;
+    bpitch = npad;
+  }
+  mxg::repack_scales_kernel<<<launch_blocks(a_chunks * 128, 256), 256, 0, stream>>>(
+      static_cast<const uint8_t *>(A_scale), M, static_cast<int>(kb), static_cast<int>(k_steps), 1,
+      a_chunks * 128, reinterpret_cast<uint32_t *>(sfa));
+  mxg::repack_scales_kernel<<<launch_blocks(b_chunks * 128, 256), 256, 0, stream>>>(
+      static_cast<const uint8_t *>(B_scale), N, static_cast<int>(kb), static_cast<int>(k_steps), 2,
+      b_chunks * 128, reinterpret_cast<uint32_t *>(sfb));
+  if (cudaGetLastError() != cudaSuccess) return MXGEMM_ERR_CUDA;
+
+  // ---- tensor maps
+  CUtensorMap tA, tB, tSA, tSB;
+  if (encode_2d(h, &tA, A, K, M, K, 128, 128, true) ||
+      encode_2d(h, &tB, bsrc, N, K, bpitch, 128, 128, true) ||
+      encode_2d(h, &tSA, sfa, 16, a_chunks * 32, 16, 16, 32, false) ||
+      encode_2d(h, &tSB, sfb, 16, b_chunks * 32, 16, 16, 64, false))
+    return MXGEMM_ERR_CUDA;
+
+  KParams kp;
+  std::memset(&kp, 0, sizeof(kp));
+  kp.M = static_cast<int>(M);
+  kp.N = static_cast<int>(N);
+  kp.K = static_cast<int>(K);
+  kp.m_tiles = static_cast<int>(m_tiles);
+  kp.n_tiles = static_cast<int>(n_tiles);
+  kp.k_steps = static_cast<int>(k_steps);
+  kp.num_tiles = static_cast<int>(num_tiles);
+  kp.C = C;
+  kp.out_bf16 = out_dtype == MXGEMM_OUT_BF16;
+  kp.use_acc = use_acc;
+  kp.vec_ok = (N % (out_dtype == MXGEMM_OUT_F32 ? 4 : 8)) == 0;
+  kp.status = h->d_status;
+  kp.timeout_ns = static_cast<unsigned long long>(h->timeout_ns);
+  kp.stall_producer = h->stall_producer;
+  kp.use_clc = h->scheduler;
+  return CG == 2 ? launch_gemm<2>(h, tA, tB, tSA, tSB, kp, stream)
+                 : launch_gemm<1>(h, tA, tB, tSA, tSB, kp, stream);
+}
+
+int mxgemm_get_device_status(mxgemm_handle_t h, mxgemm_stream_t stream_, int *status_out,
+                             int *detail_out) {
+  if (!h || !status_out) return MXGEMM_ERR_INVALID_VALUE;
+  DeviceGuard g(h->device);
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  int hostv[2] = {0, 0};
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return MXGEMM_ERR_CUDA;
+  if (cudaMemcpy(hostv, h->d_status, sizeof(hostv), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return MXGEMM_ERR_CUDA;
+  if (cudaMemset(h->d_status, 0, sizeof(hostv)) != cudaSuccess) return MXGEMM_ERR_CUDA;
+  *status_out = hostv[0];
+  if (detail_out) *detail_out = hostv[1];
+  return MXGEMM_OK;
+}
+
+int mxgemm_destroy(mxgemm_handle_t h) {
+  if (!h) return MXGEMM_ERR_INVALID_VALUE;
+  {
+    DeviceGuard g(h->device);
+    cudaDeviceSynchronize();
+    if (h->ws.ptr) cudaFree(h->ws.ptr);
+    if (h->d_status) cudaFree(h->d_status);
+  }
+  delete h;
+  return MXGEMM_OK;
+}
+
+}  // extern "C"

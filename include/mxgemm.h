@@ -1,0 +1,125 @@
+/*
+ * mxgemm.h -- C interface of the GB300 (sm_103a) MX block-scaled FP8 GEMM.
+ *
+ *   C[M,N] (+)= (A * 2^(sA-127)) x (B * 2^(sB-127))
+ *
+ * The operation is the scaled tensor-core product documented as
+ * `tlx.async_dot_scaled(A, B, acc, A_scale, "e4m3", B_scale, "e4m3", use_acc)`
+ * ("TLX API Quick Reference", section "Matrix Multiply (MMA)": D = (A*scale_A)
+ * @ (B*scale_B) + D with FP8 inputs; "Tensor core operations", sections
+ * "2-CTA Scaled MMA" and "TMEM-backed MX Scales").  Element format E4M3 and
+ * scale format E8M0 (one scale per 32 consecutive K elements) follow the OCP
+ * Microscaling Formats specification v1.0.  Accumulation is FP32.
+ *
+ * Layouts (every pointer is caller-owned DEVICE memory on the handle's GPU,
+ * dense row-major, no leading-dimension parameters):
+ *   A       : M x K      uint8 E4M3 codes, K contiguous
+ *   A_scale : M x (K/32) uint8 E8M0 codes
+ *   B       : K x N      uint8 E4M3 codes, N contiguous
+ *   B_scale : N x (K/32) uint8 E8M0 codes (row j holds column j's scales)
+ *   C       : M x N      float (MXGEMM_OUT_F32) or bfloat16 (MXGEMM_OUT_BF16)
+ *
+ * Semantics of use_acc: 0 -> C = A.B (C's previous contents, even NaN, are
+ * ignored); 1 -> C = C + A.B, C read in out_dtype, the sum formed in FP32 and
+ * rounded once to out_dtype (round to nearest even).
+ *
+ * Error behaviour: every entry point returns an mxgemm_status_t and never
+ * throws.  Arguments are validated before anything is enqueued; on an error
+ * nothing is launched and C is untouched.  Launches are asynchronous on the
+ * given stream: a device-side wait that exceeds its time limit does not trap,
+ * it records MXGEMM_ERR_TIMEOUT in the handle's device status word, which
+ * mxgemm_get_device_status reads.
+ *
+ * Threads and streams: a handle may be used from one host thread at a time,
+ * and its internal workspace is reused in stream order, so concurrent calls
+ * on different streams need different handles.
+ */
+#ifndef MXGEMM_H_
+#define MXGEMM_H_
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct mxgemm_ctx *mxgemm_handle_t;
+
+/* cudaStream_t without pulling in the CUDA headers. */
+typedef void *mxgemm_stream_t;
+
+typedef enum {
+  MXGEMM_OUT_F32 = 0,
+  MXGEMM_OUT_BF16 = 1
+} mxgemm_out_dtype_t;
+
+typedef enum {
+  MXGEMM_OK = 0,
+  MXGEMM_ERR_INVALID_VALUE = 1,      /* bad size, pointer, dtype or handle */
+  MXGEMM_ERR_MISALIGNED = 2,         /* A, B or C not 16-byte aligned */
+  MXGEMM_ERR_UNSUPPORTED_DEVICE = 3, /* device is not compute capability 10.3 */
+  MXGEMM_ERR_OUT_OF_MEMORY = 4,      /* workspace allocation failed */
+  MXGEMM_ERR_CUDA = 5,               /* a CUDA runtime/driver call failed */
+  MXGEMM_ERR_TIMEOUT = 6             /* a device-side wait ran out (status word) */
+} mxgemm_status_t;
+
+/* Options for mxgemm_set_option. */
+typedef enum {
+  /* Tile mode: 0 = automatic, 1 = one CTA per 128x256 tile, 2 = CTA pair
+   * (cta_group::2) per 256x256 tile.  Default 0. */
+  MXGEMM_OPT_MODE = 1,
+  /* Device-side wait limit in nanoseconds (default 2e9).  A wait that runs
+   * out sets MXGEMM_ERR_TIMEOUT and the kernel drains and returns. */
+  MXGEMM_OPT_WAIT_TIMEOUT_NS = 2,
+  /* Test hook for the failure-detection path: when 1, the load-issuing warp
+   * of the next launches issues no loads, so the consumer waits run out and
+   * the kernel reports MXGEMM_ERR_TIMEOUT.  Default 0. */
+  MXGEMM_OPT_TEST_STALL_PRODUCER = 3,
+  /* Persistent tile scheduler: 0 = static striding over a grid of one CTA
+   * (pair) per SM, 1 = cluster launch control (grid of all tiles; running
+   * CTAs cancel not-yet-launched ones and take their tiles).  Default 0. */
+  MXGEMM_OPT_SCHEDULER = 4
+} mxgemm_option_t;
+
+/* Create a handle bound to CUDA device `device`.  Fails with
+ * MXGEMM_ERR_UNSUPPORTED_DEVICE unless the device is compute capability 10.3
+ * (sm_103, GB300).  Allocates the handle's device status word. */
+int mxgemm_create(mxgemm_handle_t *out, int device);
+
+/* Enqueue C (+)= A.B on `stream` (NULL = the legacy default stream).
+ *   M, N, K   : sizes, each in [0, 2^31); K must be a multiple of 32.
+ *               M == 0 or N == 0 is a no-op; K == 0 sets C to 0 (use_acc=0)
+ *               or leaves it unchanged (use_acc=1).
+ *   A, B, C   : device pointers, 16-byte aligned (MXGEMM_ERR_MISALIGNED).
+ *   A_scale, B_scale : device pointers, any alignment.
+ *   use_acc   : 0 or 1 (see above).
+ *   out_dtype : MXGEMM_OUT_F32 or MXGEMM_OUT_BF16.
+ * C must not overlap A, B or the scales.  The call returns after enqueueing;
+ * the handle keeps no reference to the caller's buffers after the work
+ * completes. */
+int mxgemm_run(mxgemm_handle_t h, int64_t M, int64_t N, int64_t K,
+               const void *A, const void *A_scale, const void *B,
+               const void *B_scale, void *C, int use_acc, int out_dtype,
+               mxgemm_stream_t stream);
+
+/* Set an option (mxgemm_option_t) on the handle; applies to later runs. */
+int mxgemm_set_option(mxgemm_handle_t h, int option, int64_t value);
+
+/* Synchronize `stream`, then read and clear the handle's device status word.
+ * *status_out receives MXGEMM_OK or MXGEMM_ERR_TIMEOUT; *detail_out (may be
+ * NULL) receives where the first failing wait was (role | stage << 8 |
+ * tile << 16), 0 when none. */
+int mxgemm_get_device_status(mxgemm_handle_t h, mxgemm_stream_t stream,
+                             int *status_out, int *detail_out);
+
+/* Free the handle's device memory (synchronizes its device) and the handle. */
+int mxgemm_destroy(mxgemm_handle_t h);
+
+/* Static description of a status code. */
+const char *mxgemm_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MXGEMM_H_ */

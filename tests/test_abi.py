@@ -1,0 +1,76 @@
+"""Host-side checks of the C interface that need no GPU: the library builds
+for sm_103a, loads, exports every function include/mxgemm.h declares, and
+rejects bad arguments without touching a device."""
+import ctypes
+import re
+from pathlib import Path
+
+import pytest
+
+import block_scaled_gemm_gb300 as mx
+from block_scaled_gemm_gb300 import _build
+
+HEADER = Path(__file__).resolve().parents[1] / "include"
+
+
+@pytest.fixture(scope="module")
+def lib():
+    _build.build()
+    return mx.library()
+
+
+def _declared_functions():
+    names = set()
+    for hdr in HEADER.glob("*.h"):
+        text = hdr.read_text()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        for m in re.finditer(r"^\s*(?:const\s+)?[A-Za-z_][A-Za-z0-9_]*\s*\**\s*([a-z_][a-z0-9_]*)\s*\(",
+                             text, flags=re.M):
+            names.add(m.group(1))
+    return sorted(names)
+
+
+def test_header_declares_the_interface():
+    names = _declared_functions()
+    for n in ("mxgemm_create", "mxgemm_run", "mxgemm_destroy"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared_functions():
+        assert hasattr(lib, name), f"{name} declared in include/ but not exported"
+    for name in mx.EXPORTED_SYMBOLS:
+        assert name in _declared_functions()
+
+
+def test_null_handle_rejected(lib):
+    assert lib.mxgemm_run(None, 1, 1, 32, None, None, None, None, None, 0, 0, None) == mx.ERR_INVALID_VALUE
+    assert lib.mxgemm_destroy(None) == mx.ERR_INVALID_VALUE
+    assert lib.mxgemm_set_option(None, 1, 0) == mx.ERR_INVALID_VALUE
+    st = ctypes.c_int()
+    assert lib.mxgemm_get_device_status(None, None, ctypes.byref(st), None) == mx.ERR_INVALID_VALUE
+    assert lib.mxgemm_create(None, 0) == mx.ERR_INVALID_VALUE
+
+
+def test_status_strings(lib):
+    for s in range(7):
+        assert mx.mxgemm_status_string(s)
+    assert "timed out" in mx.mxgemm_status_string(mx.ERR_TIMEOUT)
+
+
+def test_create_without_supported_gpu_fails_cleanly(lib):
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    h = ctypes.c_void_p()
+    st = lib.mxgemm_create(ctypes.byref(h), 0)
+    assert st in (mx.ERR_CUDA, mx.ERR_INVALID_VALUE, mx.ERR_UNSUPPORTED_DEVICE)
+    assert not h.value
+
+
+def test_product_path_does_not_import_the_oracle():
+    # the binding must never reach the CPU checker
+    src = (Path(mx.__file__).parent).rglob("*.py")
+    for f in src:
+        text = f.read_text()
+        assert "import oracle" not in text and "from oracle" not in text, f

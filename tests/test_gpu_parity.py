@@ -1,0 +1,224 @@
+"""GPU parity: the CUDA path (through the C interface) against the CPU oracle,
+element by element, on seeded inputs.
+
+Tolerances (per element, ref = unrounded double oracle value, bound =
+sum_k |a_k b_k| with scales):
+    FP32 out: |C - ref| <= 1e-5 * bound
+    BF16 out: |C - ref| <= 2^-8 |ref| + 1e-5 * bound
+Small integers with unit scales must be bit-exact (FP32 partial sums of
+integers below 2^24 are exact in any order).
+"""
+import numpy as np
+import pytest
+import torch
+
+import mx_inputs as mi
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+gu = pytest.importorskip("gpu_util")
+mx = pytest.importorskip("block_scaled_gemm_gb300")
+
+
+@pytest.fixture(scope="module")
+def h():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from block_scaled_gemm_gb300 import _build
+    _build.build()
+    handle = mx.mxgemm_create(0)
+    yield handle
+    mx.mxgemm_destroy(handle)
+
+
+def _mode(h, m):
+    mx.mxgemm_set_option(h, mx.OPT_MODE, m)
+
+
+# ---------------------------------------------------------------- exactness
+
+@pytest.mark.parametrize("mode", [1, 2])
+def test_exact_integers_bitwise(h, mode):
+    _mode(h, mode)
+    p = mi.random_problem(384, 512, 1024, seed=2, kind="int")
+    C = gu.run_gpu(h, p)
+    ref, _ = oracle.rows(p.A, p.As, p.B, p.Bs)
+    got = C.cpu().numpy().astype(np.float64)
+    bad = np.argwhere(got != ref)
+    assert bad.size == 0, f"{len(bad)} mismatches, first {bad[:5].tolist()}"
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+def test_row_scales_localised(h, mode):
+    # integer data, A scale depends on the row only: a mis-mapped scale lane
+    # shows up as a wrong power of two in that row
+    _mode(h, mode)
+    p = mi.random_problem(256, 256, 256, seed=3, kind="int")
+    As = (127 + (torch.arange(256) % 7) - 3).to(torch.uint8)[:, None].repeat(1, p.K // 32)
+    p.As = As.contiguous()
+    C = gu.run_gpu(h, p).cpu().numpy().astype(np.float64)
+    ref, _ = oracle.rows(p.A, p.As, p.B, p.Bs)
+    bad_rows = np.unique(np.argwhere(C != ref)[:, 0])
+    assert bad_rows.size == 0, f"rows with wrong values: {bad_rows[:16].tolist()}"
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+def test_col_scales_localised(h, mode):
+    _mode(h, mode)
+    p = mi.random_problem(256, 512, 256, seed=4, kind="int")
+    p.Bs = (127 + (torch.arange(512) % 9) - 4).to(torch.uint8)[:, None].repeat(1, p.K // 32).contiguous()
+    C = gu.run_gpu(h, p).cpu().numpy().astype(np.float64)
+    ref, _ = oracle.rows(p.A, p.As, p.B, p.Bs)
+    bad_cols = np.unique(np.argwhere(C != ref)[:, 1])
+    assert bad_cols.size == 0, f"columns with wrong values: {bad_cols[:16].tolist()}"
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+def test_kblock_scales_localised(h, mode):
+    _mode(h, mode)
+    p = mi.random_problem(256, 256, 512, seed=5, kind="int")
+    kb = torch.arange(p.K // 32)
+    p.As = (127 + (kb % 5) - 2).to(torch.uint8)[None, :].repeat(256, 1).contiguous()
+    p.Bs = (127 + (kb % 3) - 1).to(torch.uint8)[None, :].repeat(256, 1).contiguous()
+    C = gu.run_gpu(h, p).cpu().numpy().astype(np.float64)
+    ref, _ = oracle.rows(p.A, p.As, p.B, p.Bs)
+    assert np.array_equal(C, ref)
+
+
+# ---------------------------------------------------------------- tolerance parity
+
+@pytest.mark.parametrize("mode", [1, 2])
+def test_square_256(h, mode):
+    _mode(h, mode)
+    p = mi.square_256()
+    res, *_ = gu.check_full(h, p)
+    assert res["max_err_over_bound"] < 1e-5
+
+
+SIZES = [1, 31, 127, 128, 129, 255, 257]
+KS = [32, 96, 128, 160, 4096]
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("K", KS)
+def test_small_sweep_f32(h, mode, K):
+    _mode(h, mode)
+    for i, M in enumerate(SIZES):
+        N = SIZES[(i * 3 + 2) % len(SIZES)]
+        p = mi.random_problem(M, N, K, seed=100 + i + K, kind="normal")
+        gu.check_full(h, p)
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("out_dtype", ["f32", "bf16"])
+def test_use_acc(h, mode, out_dtype):
+    _mode(h, mode)
+    p = mi.random_problem(300, 520, 384, seed=7, kind="normal", out_dtype=out_dtype)
+    cin = mi.c_init(p.M, p.N, 7, out_dtype)
+    gu.check_full(h, p, c_init=cin, use_acc=True)
+    # use_acc = 0 ignores C (NaN-filled by run_gpu)
+    gu.check_full(h, p, c_init=None, use_acc=False)
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+def test_bf16_out_and_ragged_n(h, mode):
+    _mode(h, mode)
+    # N not a multiple of 16: the B rows are re-pitched internally; N not a
+    # multiple of 8: the BF16 epilogue takes its scalar path
+    for (M, N, K) in [(200, 1000, 256), (129, 77, 160), (64, 4100, 128)]:
+        for od in ("f32", "bf16"):
+            p = mi.random_problem(M, N, K, seed=M + N, kind="normal", out_dtype=od)
+            gu.check_full(h, p)
+
+
+def test_one_vs_two_cta_identical(h):
+    p = mi.random_problem(512, 768, 1024, seed=11, kind="normal")
+    _mode(h, 1)
+    c1 = gu.run_gpu(h, p).cpu()
+    _mode(h, 2)
+    c2 = gu.run_gpu(h, p).cpu()
+    # same tile order of K accumulation within an output element; allow the
+    # tolerance anyway but report exact agreement
+    ref, bound = oracle.rows(p.A, p.As, p.B, p.Bs)
+    assert oracle.accept(c1.numpy(), ref, bound, "f32")["ok"]
+    assert oracle.accept(c2.numpy(), ref, bound, "f32")["ok"]
+
+
+def test_repeat_determinism(h):
+    _mode(h, 0)
+    p = mi.random_problem(640, 512, 2048, seed=12, kind="codes")
+    a = gu.run_gpu(h, p).cpu()
+    b = gu.run_gpu(h, p).cpu()
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+def test_degenerate_sizes(h):
+    _mode(h, 0)
+    dev = gu.DEV
+    A = torch.zeros((4, 64), dtype=torch.uint8, device=dev)
+    S = torch.full((4, 2), 127, dtype=torch.uint8, device=dev)
+    B = torch.zeros((64, 8), dtype=torch.uint8, device=dev)
+    T = torch.full((8, 2), 127, dtype=torch.uint8, device=dev)
+    C = torch.full((4, 8), 5.0, device=dev)
+    # M == 0 / N == 0: no-op
+    mx.mxgemm_run(h, 0, 8, 64, A, S, B, T, C, 0, mx.OUT_F32)
+    mx.mxgemm_run(h, 4, 0, 64, A, S, B, T, C, 0, mx.OUT_F32)
+    torch.cuda.synchronize()
+    assert torch.all(C == 5.0)
+    # K == 0: use_acc keeps C, otherwise C = 0
+    mx.mxgemm_run(h, 4, 8, 0, A, S, B, T, C, 1, mx.OUT_F32)
+    torch.cuda.synchronize()
+    assert torch.all(C == 5.0)
+    mx.mxgemm_run(h, 4, 8, 0, A, S, B, T, C, 0, mx.OUT_F32)
+    torch.cuda.synchronize()
+    assert torch.all(C == 0.0)
+
+
+def test_invalid_arguments_rejected_before_launch(h):
+    dev = gu.DEV
+    A = torch.zeros((4, 64), dtype=torch.uint8, device=dev)
+    S = torch.full((4, 2), 127, dtype=torch.uint8, device=dev)
+    B = torch.zeros((64, 16), dtype=torch.uint8, device=dev)
+    T = torch.full((16, 2), 127, dtype=torch.uint8, device=dev)
+    C = torch.full((4, 16), 5.0, device=dev)
+    st = mx.mxgemm_run(h, 4, 16, 48, A, S, B, T, C, 0, mx.OUT_F32, check=False)
+    assert st == mx.ERR_INVALID_VALUE  # K % 32 != 0
+    st = mx.mxgemm_run(h, 4, 16, 64, A, S, B, T, C, 0, 7, check=False)
+    assert st == mx.ERR_INVALID_VALUE  # bad dtype
+    st = mx.mxgemm_run(h, 4, 16, 64, A.data_ptr() + 1, S, B, T, C, 0, mx.OUT_F32, check=False)
+    assert st == mx.ERR_MISALIGNED
+    st = mx.mxgemm_run(h, 4, 16, 64, None, S, B, T, C, 0, mx.OUT_F32, check=False)
+    assert st == mx.ERR_INVALID_VALUE
+    host = torch.zeros((4, 64), dtype=torch.uint8)
+    st = mx.mxgemm_run(h, 4, 16, 64, host, S, B, T, C, 0, mx.OUT_F32, check=False)
+    assert st == mx.ERR_INVALID_VALUE  # not device memory
+    st = mx.mxgemm_run(h, -1, 16, 64, A, S, B, T, C, 0, mx.OUT_F32, check=False)
+    assert st == mx.ERR_INVALID_VALUE
+    torch.cuda.synchronize()
+    assert torch.all(C == 5.0)
+
+
+def test_timeout_reports_and_device_stays_usable():
+    # the load-issuing warp is told to issue nothing: the consumers' waits run
+    # out, the kernel records MXGEMM_ERR_TIMEOUT, drains and returns
+    from block_scaled_gemm_gb300 import _build
+    _build.build()
+    g = mx.mxgemm_create(0)
+    try:
+        for mode in (1, 2):
+            mx.mxgemm_set_option(g, mx.OPT_MODE, mode)
+            mx.mxgemm_set_option(g, mx.OPT_WAIT_TIMEOUT_NS, 50_000_000)
+            mx.mxgemm_set_option(g, mx.OPT_TEST_STALL_PRODUCER, 1)
+            p = mi.random_problem(256, 256, 256, seed=21, kind="normal")
+            A, As, B, Bs = (t.to(gu.DEV) for t in (p.A, p.As, p.B, p.Bs))
+            C = torch.zeros((256, 256), device=gu.DEV)
+            mx.mxgemm_run(g, 256, 256, 256, A, As, B, Bs, C, 0, mx.OUT_F32)
+            st, det = mx.mxgemm_get_device_status(g)
+            assert st == mx.ERR_TIMEOUT, (st, det)
+            # the same handle, hook off: correct results again
+            mx.mxgemm_set_option(g, mx.OPT_TEST_STALL_PRODUCER, 0)
+            mx.mxgemm_set_option(g, mx.OPT_WAIT_TIMEOUT_NS, 2_000_000_000)
+            gu.check_full(g, p)
+    finally:
+        mx.mxgemm_destroy(g)
