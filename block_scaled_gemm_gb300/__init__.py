@@ -25,7 +25,7 @@ __all__ = [
     "OUT_F32", "OUT_BF16", "OPT_MODE", "OPT_WAIT_TIMEOUT_NS", "OPT_TEST_STALL_PRODUCER",
     "OPT_SCHEDULER", "MxgemmError", "library", "library_path", "mxgemm_create", "mxgemm_run",
     "mxgemm_destroy", "mxgemm_set_option", "mxgemm_get_device_status", "mxgemm_status_string",
-    "EXPORTED_SYMBOLS", "Gemm",
+    "mxgemm_set_profile_events", "mxgemm_get_launch_count", "EXPORTED_SYMBOLS", "Gemm",
 ]
 
 OUT_F32 = 0
@@ -46,7 +46,8 @@ ERR_TIMEOUT = 6
 
 EXPORTED_SYMBOLS = (
     "mxgemm_create", "mxgemm_run", "mxgemm_destroy", "mxgemm_set_option",
-    "mxgemm_get_device_status", "mxgemm_status_string",
+    "mxgemm_get_device_status", "mxgemm_status_string", "mxgemm_set_profile_events",
+    "mxgemm_get_launch_count",
 )
 
 _lib = None
@@ -83,6 +84,10 @@ def library():
         lib.mxgemm_set_option.restype = i32
         lib.mxgemm_get_device_status.argtypes = [vp, vp, ctypes.POINTER(i32), ctypes.POINTER(i32)]
         lib.mxgemm_get_device_status.restype = i32
+        lib.mxgemm_set_profile_events.argtypes = [vp, vp, vp]
+        lib.mxgemm_set_profile_events.restype = i32
+        lib.mxgemm_get_launch_count.argtypes = [vp, ctypes.POINTER(i64)]
+        lib.mxgemm_get_launch_count.restype = i32
         lib.mxgemm_status_string.argtypes = [i32]
         lib.mxgemm_status_string.restype = ctypes.c_char_p
         _lib = lib
@@ -139,6 +144,24 @@ def mxgemm_get_device_status(h, stream=None):
     _check(library().mxgemm_get_device_status(h, _stream(stream), ctypes.byref(st), ctypes.byref(det)),
            "mxgemm_get_device_status")
     return st.value, det.value
+
+
+def mxgemm_set_profile_events(h, ev_before, ev_after) -> None:
+    """Record these CUDA events (torch.cuda.Event, raw handles or None)
+    around the GEMM kernel launch of later runs.  torch events must already
+    have been recorded once (torch creates the CUDA event lazily)."""
+    def raw(e):
+        if e is None or isinstance(e, int):
+            return e
+        return e.cuda_event
+    _check(library().mxgemm_set_profile_events(h, raw(ev_before), raw(ev_after)),
+           "mxgemm_set_profile_events")
+
+
+def mxgemm_get_launch_count(h) -> int:
+    n = ctypes.c_int64()
+    _check(library().mxgemm_get_launch_count(h, ctypes.byref(n)), "mxgemm_get_launch_count")
+    return n.value
 
 
 def mxgemm_destroy(h) -> None:

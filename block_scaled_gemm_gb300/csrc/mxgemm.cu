@@ -40,6 +40,9 @@ struct mxgemm_ctx {
   int stall_producer = 0;
   int scheduler = 0;
   bool attr_set[3] = {false, false, false};
+  cudaEvent_t prof_before = nullptr;
+  cudaEvent_t prof_after = nullptr;
+  int64_t launches = 0;
 };
 
 namespace {
@@ -70,17 +73,17 @@ bool on_device(const void *p, int device) {
          attr.device == device;
 }
 
-// 2-D uint8 tensor map: dims {inner, outer}, row pitch in bytes, box.
-int encode_2d(mxgemm_ctx *h, CUtensorMap *tm, const void *base, uint64_t inner, uint64_t outer,
-              uint64_t pitch, uint32_t box_inner, uint32_t box_outer, bool swizzle128) {
+// 2-D tensor map: dims {inner, outer} in elements, row pitch in bytes, box.
+int encode_2d(mxgemm_ctx *h, CUtensorMap *tm, CUtensorMapDataType dt, const void *base,
+              uint64_t inner, uint64_t outer, uint64_t pitch, uint32_t box_inner,
+              uint32_t box_outer, CUtensorMapSwizzle swz) {
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {pitch};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = h->encode(tm, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims,
-                         strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                         swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
-                         CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = h->encode(tm, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
+                         CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS ? MXGEMM_OK : MXGEMM_ERR_CUDA;
 }
 
@@ -105,8 +108,8 @@ int ensure_workspace(mxgemm_ctx *h, size_t bytes, cudaStream_t stream) {
 
 template <int CG>
 int launch_gemm(mxgemm_ctx *h, const CUtensorMap &tA, const CUtensorMap &tB,
-                const CUtensorMap &tSA, const CUtensorMap &tSB, const KParams &kp,
-                cudaStream_t stream) {
+                const CUtensorMap &tSA, const CUtensorMap &tSB, const CUtensorMap &tC,
+                const KParams &kp, cudaStream_t stream) {
   using C = Cfg<CG>;
   auto kern = mxg::mxgemm_kernel<CG>;
   if (!h->attr_set[CG]) {
@@ -135,8 +138,17 @@ int launch_gemm(mxgemm_ctx *h, const CUtensorMap &tA, const CUtensorMap &tB,
     cfg.attrs = attr;
     cfg.numAttrs = 1;
   }
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tA, tB, tSA, tSB, kp);
+  if (h->prof_before && cudaEventRecord(h->prof_before, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return MXGEMM_ERR_CUDA;
+  }
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tA, tB, tSA, tSB, tC, kp);
   if (e != cudaSuccess) {
+    cudaGetLastError();
+    return MXGEMM_ERR_CUDA;
+  }
+  ++h->launches;
+  if (h->prof_after && cudaEventRecord(h->prof_after, stream) != cudaSuccess) {
     cudaGetLastError();
     return MXGEMM_ERR_CUDA;
   }
@@ -296,21 +308,38 @@ int mxgemm_run(mxgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A
         static_cast<const uint8_t *>(B), K, N, npad, bp);
     bsrc = bp;
     bpitch = npad;
+    ++h->launches;
   }
-  mxg::repack_scales_kernel<<<launch_blocks(a_chunks * 128, 256), 256, 0, stream>>>(
-      static_cast<const uint8_t *>(A_scale), M, static_cast<int>(kb), static_cast<int>(k_steps), 1,
-      a_chunks * 128, reinterpret_cast<uint32_t *>(sfa));
-  mxg::repack_scales_kernel<<<launch_blocks(b_chunks * 128, 256), 256, 0, stream>>>(
-      static_cast<const uint8_t *>(B_scale), N, static_cast<int>(kb), static_cast<int>(k_steps), 2,
-      b_chunks * 128, reinterpret_cast<uint32_t *>(sfb));
+  mxg::RepackArgs ra{static_cast<const uint8_t *>(A_scale), reinterpret_cast<uint32_t *>(sfa), M,
+                     static_cast<int>(kb), static_cast<int>(k_steps), 1,
+                     static_cast<int>(m_tiles * CG), static_cast<int>(cdiv(k_steps, 16))};
+  mxg::RepackArgs rb{static_cast<const uint8_t *>(B_scale), reinterpret_cast<uint32_t *>(sfb), N,
+                     static_cast<int>(kb), static_cast<int>(k_steps), 2,
+                     static_cast<int>(n_tiles * 2), static_cast<int>(cdiv(k_steps, 16))};
+  const int blocks_a = ra.row_blocks * ra.kgroups;
+  const int blocks_b = rb.row_blocks * rb.kgroups;
+  mxg::repack_scales_kernel<<<blocks_a + blocks_b, mxg::kRepackThreads, 0, stream>>>(ra, rb, blocks_a);
+  h->launches += 1;
   if (cudaGetLastError() != cudaSuccess) return MXGEMM_ERR_CUDA;
 
   // ---- tensor maps
-  CUtensorMap tA, tB, tSA, tSB;
-  if (encode_2d(h, &tA, A, K, M, K, 128, 128, true) ||
-      encode_2d(h, &tB, bsrc, N, K, bpitch, 128, 128, true) ||
-      encode_2d(h, &tSA, sfa, 16, a_chunks * 32, 16, 16, 32, false) ||
-      encode_2d(h, &tSB, sfb, 16, b_chunks * 32, 16, 16, 64, false))
+  CUtensorMap tA, tB, tSA, tSB, tC;
+  const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  if (encode_2d(h, &tA, u8, A, K, M, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      encode_2d(h, &tB, u8, bsrc, N, K, bpitch, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      encode_2d(h, &tSA, u8, sfa, 16, a_chunks * 32, 16, 16, 32, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      encode_2d(h, &tSB, u8, sfb, 16, b_chunks * 32, 16, 16, 64, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return MXGEMM_ERR_CUDA;
+  // C: stored through TMA (64-byte-wide boxes, 32 rows) when its row pitch
+  // allows it; otherwise the kernel stores directly and tC is unused.
+  const bool tma_store = (static_cast<size_t>(N) * esz) % 16 == 0;
+  std::memset(&tC, 0, sizeof(tC));
+  if (tma_store &&
+      encode_2d(h, &tC,
+                out_dtype == MXGEMM_OUT_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                            : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                C, N, M, static_cast<uint64_t>(N) * esz, static_cast<uint32_t>(64 / esz), 32,
+                CU_TENSOR_MAP_SWIZZLE_64B))
     return MXGEMM_ERR_CUDA;
 
   KParams kp;
@@ -326,12 +355,13 @@ int mxgemm_run(mxgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A
   kp.out_bf16 = out_dtype == MXGEMM_OUT_BF16;
   kp.use_acc = use_acc;
   kp.vec_ok = (N % (out_dtype == MXGEMM_OUT_F32 ? 4 : 8)) == 0;
+  kp.tma_store = tma_store;
   kp.status = h->d_status;
   kp.timeout_ns = static_cast<unsigned long long>(h->timeout_ns);
   kp.stall_producer = h->stall_producer;
   kp.use_clc = h->scheduler;
-  return CG == 2 ? launch_gemm<2>(h, tA, tB, tSA, tSB, kp, stream)
-                 : launch_gemm<1>(h, tA, tB, tSA, tSB, kp, stream);
+  return CG == 2 ? launch_gemm<2>(h, tA, tB, tSA, tSB, tC, kp, stream)
+                 : launch_gemm<1>(h, tA, tB, tSA, tSB, tC, kp, stream);
 }
 
 int mxgemm_get_device_status(mxgemm_handle_t h, mxgemm_stream_t stream_, int *status_out,
@@ -346,6 +376,19 @@ int mxgemm_get_device_status(mxgemm_handle_t h, mxgemm_stream_t stream_, int *st
   if (cudaMemset(h->d_status, 0, sizeof(hostv)) != cudaSuccess) return MXGEMM_ERR_CUDA;
   *status_out = hostv[0];
   if (detail_out) *detail_out = hostv[1];
+  return MXGEMM_OK;
+}
+
+int mxgemm_set_profile_events(mxgemm_handle_t h, void *ev_before, void *ev_after) {
+  if (!h) return MXGEMM_ERR_INVALID_VALUE;
+  h->prof_before = static_cast<cudaEvent_t>(ev_before);
+  h->prof_after = static_cast<cudaEvent_t>(ev_after);
+  return MXGEMM_OK;
+}
+
+int mxgemm_get_launch_count(mxgemm_handle_t h, int64_t *count_out) {
+  if (!h || !count_out) return MXGEMM_ERR_INVALID_VALUE;
+  *count_out = h->launches;
   return MXGEMM_OK;
 }
 

@@ -61,7 +61,10 @@ struct Cfg {
   static constexpr int OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;
   static constexpr int NUM_BARS = 2 * STAGES + 3;  // full[], empty[], acc_full, acc_empty, final
   static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
-  static constexpr int SMEM_BYTES = OFF_MISC + 16 + 1024;  // + slack for 1 KB alignment
+  // epilogue staging: one 32-row x 64-byte buffer per epilogue warp
+  static constexpr int EPI_BUF = 2048;
+  static constexpr int OFF_EPI = (OFF_MISC + 16 + 1023) / 1024 * 1024;
+  static constexpr int SMEM_BYTES = OFF_EPI + 8 * EPI_BUF + 1024;  // + slack for 1 KB alignment
   static constexpr int TM_ACC = 0;
   static constexpr int TM_SFA = BN;               // STAGES x 4 columns
   static constexpr int TM_SFB = BN + 4 * STAGES;  // STAGES x 8 columns
@@ -83,6 +86,7 @@ struct KParams {
   int out_bf16;
   int use_acc;
   int vec_ok;     // rows of C allow 16-byte vector access
+  int tma_store;  // C's row pitch is a multiple of 16 bytes: stores go through TMA
   int *status;    // [0] code, [1] detail
   unsigned long long timeout_ns;
   int stall_producer;
@@ -148,7 +152,8 @@ template <int CG>
 __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
     mxgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const __grid_constant__ CUtensorMap tmSFA,
-                  const __grid_constant__ CUtensorMap tmSFB, const KParams p) {
+                  const __grid_constant__ CUtensorMap tmSFB, const __grid_constant__ CUtensorMap tmC,
+                  const KParams p) {
   using C = Cfg<CG>;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -183,6 +188,7 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
     tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmSFA);
     tma_prefetch_desc(&tmSFB);
+    if (p.tma_store) tma_prefetch_desc(&tmC);
   }
   if (warp == 1) {
     tmem_alloc<CG>(smem_u32(tmem_slot), C::TM_COLS);
@@ -198,111 +204,134 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
   const int first_tile = blockIdx.x / CG;
   const int tile_stride = gridDim.x / CG;
 
+  // The producer and MMA loops are unrolled over the ring stages: with the
+  // stage index a compile-time constant every shared-memory address, TMEM
+  // column and barrier of a step is a constant offset from a base, which
+  // keeps the single issuing thread fast enough to hold the tensor pipe busy
+  // (a rolled loop with a runtime stage index cost about 30% of MMA rate).
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      int stage = 0;
       uint32_t phase = 0;
-      bool ok = true;
-      if (!p.stall_producer) {
-        for (int t = first_tile; ok && t < p.num_tiles; t += tile_stride) {
-          int mt, nt;
-          tile_coords(t, p.m_tiles, p.n_tiles, mt, nt);
-          const int row0 = mt * (128 * CG) + 128 * (int)rank;  // this CTA's A rows
-          const int mblk = mt * CG + (int)rank;                  // its 128-row block
-          const int col0 = nt * 256;
-          for (int ks = 0; ks < p.k_steps; ++ks) {
-            if (!wait_phase<CL>(bar_empty + 8 * stage, phase ^ 1u, wc, 0x01 | (stage << 8))) {
+      int nst = 0;           // next stage to fill ...
+      uint32_t nph = 0;      // ... and the ring phase it belongs to
+      int t = first_tile, ks = 0;
+      bool ok = !p.stall_producer && t < p.num_tiles;
+      int mt = 0, nt = 0;
+      if (ok) tile_coords(t, p.m_tiles, p.n_tiles, mt, nt);
+      while (ok) {
+#pragma unroll
+        for (int st = 0; st < C::STAGES; ++st) {
+          if (ok) {
+            if (!wait_phase<CL>(bar_empty + 8 * st, phase ^ 1u, wc, 0x01 | (st << 8))) {
               ok = false;
-              break;
-            }
-            const uint32_t fb = bar_full + 8 * stage;
-            const uint32_t sA = base + C::OFF_A + stage * C::A_BYTES;
-            const uint32_t sB = base + C::OFF_B + stage * C::B_BYTES;
-            const uint32_t sSA = base + C::OFF_SFA + stage * C::SFA_BYTES;
-            const uint32_t sSB = base + C::OFF_SFB + stage * C::SFB_BYTES;
-            const int k0 = ks * 128;
-            if constexpr (CG == 1) {
-              mbar_arrive_expect_tx(fb, C::STAGE_TX);
-              tma_load_2d(sA, &tmA, k0, row0, fb);
-              tma_load_2d(sB, &tmB, col0, k0, fb);
-              tma_load_2d(sB + 16384, &tmB, col0 + 128, k0, fb);
-              tma_load_2d(sSA, &tmSFA, 0, (mblk * p.k_steps + ks) * 32, fb);
-              tma_load_2d(sSB, &tmSFB, 0, (nt * p.k_steps + ks) * 64, fb);
             } else {
-              if (rank == 0) mbar_arrive_expect_tx(fb, C::STAGE_TX);
-              const uint32_t fbl = mapa_shared(fb, 0);  // leader's barrier
-              tma_load_2d_pair(sA, &tmA, k0, row0, fbl);
-              tma_load_2d_pair(sB, &tmB, col0 + 128 * (int)rank, k0, fbl);
-              tma_load_2d_pair(sSA, &tmSFA, 0, (mblk * p.k_steps + ks) * 32, fbl);
-              tma_load_2d_pair(sSB, &tmSFB, 0, (nt * p.k_steps + ks) * 64, fbl);
-            }
-            if (++stage == C::STAGES) {
-              stage = 0;
-              phase ^= 1u;
+              const uint32_t fb = bar_full + 8 * st;
+              const uint32_t sA = base + C::OFF_A + st * C::A_BYTES;
+              const uint32_t sB = base + C::OFF_B + st * C::B_BYTES;
+              const uint32_t sSA = base + C::OFF_SFA + st * C::SFA_BYTES;
+              const uint32_t sSB = base + C::OFF_SFB + st * C::SFB_BYTES;
+              const int row0 = mt * (128 * CG) + 128 * (int)rank;  // this CTA's A rows
+              const int mblk = mt * CG + (int)rank;                  // its 128-row block
+              const int col0 = nt * 256;
+              const int k0 = ks * 128;
+              if constexpr (CG == 1) {
+                mbar_arrive_expect_tx(fb, C::STAGE_TX);
+                tma_load_2d(sA, &tmA, k0, row0, fb);
+                tma_load_2d(sB, &tmB, col0, k0, fb);
+                tma_load_2d(sB + 16384, &tmB, col0 + 128, k0, fb);
+                tma_load_2d(sSA, &tmSFA, 0, (mblk * p.k_steps + ks) * 32, fb);
+                tma_load_2d(sSB, &tmSFB, 0, (nt * p.k_steps + ks) * 64, fb);
+              } else {
+                if (rank == 0) mbar_arrive_expect_tx(fb, C::STAGE_TX);
+                const uint32_t fbl = mapa_shared(fb, 0);  // leader's barrier
+                tma_load_2d_pair(sA, &tmA, k0, row0, fbl);
+                tma_load_2d_pair(sB, &tmB, col0 + 128 * (int)rank, k0, fbl);
+                tma_load_2d_pair(sSA, &tmSFA, 0, (mblk * p.k_steps + ks) * 32, fbl);
+                tma_load_2d_pair(sSB, &tmSFB, 0, (nt * p.k_steps + ks) * 64, fbl);
+              }
+              nst = (st + 1 == C::STAGES) ? 0 : st + 1;
+              nph = (st + 1 == C::STAGES) ? (phase ^ 1u) : phase;
+              if (++ks == p.k_steps) {
+                ks = 0;
+                t += tile_stride;
+                if (t >= p.num_tiles) ok = false;
+                else tile_coords(t, p.m_tiles, p.n_tiles, mt, nt);
+              }
             }
           }
         }
+        if (ok) phase ^= 1u;
       }
       // Drain: every stage's last fill has been consumed (its MMA commit has
       // arrived) before this CTA may finish.
       for (int i = 0; i < C::STAGES; ++i) {
-        if (!wait_phase<CL>(bar_empty + 8 * stage, phase ^ 1u, wc, 0x11 | (stage << 8))) break;
-        if (++stage == C::STAGES) {
-          stage = 0;
-          phase ^= 1u;
+        if (!wait_phase<CL>(bar_empty + 8 * nst, nph ^ 1u, wc, 0x11 | (nst << 8))) break;
+        if (++nst == C::STAGES) {
+          nst = 0;
+          nph ^= 1u;
         }
       }
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && rank == 0) {
-      int stage = 0;
       uint32_t phase = 0, acc_phase = 0;
-      bool ok = true;
-      for (int t = first_tile; ok && t < p.num_tiles; t += tile_stride) {
-        if (!wait_phase<CL>(bar_acc_empty, acc_phase ^ 1u, wc, 0x02 | ((t & 0xFFFF) << 16))) {
-          ok = false;
-          break;
-        }
+      int t = first_tile, ks = 0;
+      bool ok = t < p.num_tiles;
+      if (ok) {
+        ok = wait_phase<CL>(bar_acc_empty, acc_phase ^ 1u, wc, 0x02 | ((t & 0xFFFF) << 16));
         tc_fence_after();
-        for (int ks = 0; ks < p.k_steps; ++ks) {
-          if (!wait_phase<CL>(bar_full + 8 * stage, phase, wc, 0x03 | (stage << 8))) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t sA = base + C::OFF_A + stage * C::A_BYTES;
-          const uint32_t sB = base + C::OFF_B + stage * C::B_BYTES;
-          const uint32_t sSA = base + C::OFF_SFA + stage * C::SFA_BYTES;
-          const uint32_t sSB = base + C::OFF_SFB + stage * C::SFB_BYTES;
-          const uint32_t tSA = tmem + C::TM_SFA + 4 * stage;
-          const uint32_t tSB = tmem + C::TM_SFB + 8 * stage;
-          // scale chunks: 32 rows x 16 bytes each, no swizzle, 8-row groups 128 B apart
-          tmem_cp_32x128b_x4<CG>(tSA, smem_desc(sSA, 0, 128, 0));
-          tmem_cp_32x128b_x4<CG>(tSB, smem_desc(sSB, 0, 128, 0));
-          tmem_cp_32x128b_x4<CG>(tSB + 4, smem_desc(sSB + 512, 0, 128, 0));
+      }
+      while (ok) {
 #pragma unroll
-          for (int k = 0; k < 4; ++k) {
-            // A: K-major, 128-byte swizzle, 8-row groups 1024 B apart; step 32 B per K=32
-            const uint64_t ad = smem_desc(sA + 32 * k, 0, 1024, 2);
-            // B: N-major, 128-byte swizzle; 128-column chunks 16 KB apart,
-            // 8-row K groups 1024 B apart; step 32 rows (4 KB) per K=32
-            const uint64_t bd = smem_desc(sB + 4096 * k, 16384, 1024, 2);
-            mma_mxf8<CG>(tmem + C::TM_ACC, ad, bd, idesc_mxf8(128 * CG, 256, k, k), tSA, tSB,
-                         (ks | k) != 0);
-          }
-          if constexpr (CG == 1) tc_commit(bar_empty + 8 * stage);
-          else tc_commit_pair(bar_empty + 8 * stage, 0x3);
-          if (++stage == C::STAGES) {
-            stage = 0;
-            phase ^= 1u;
+        for (int st = 0; st < C::STAGES; ++st) {
+          if (ok) {
+            if (!wait_phase<CL>(bar_full + 8 * st, phase, wc, 0x03 | (st << 8))) {
+              ok = false;
+            } else {
+              const uint32_t sA = base + C::OFF_A + st * C::A_BYTES;
+              const uint32_t sB = base + C::OFF_B + st * C::B_BYTES;
+              const uint32_t sSA = base + C::OFF_SFA + st * C::SFA_BYTES;
+              const uint32_t sSB = base + C::OFF_SFB + st * C::SFB_BYTES;
+              const uint32_t tSA = tmem + C::TM_SFA + 4 * st;
+              const uint32_t tSB = tmem + C::TM_SFB + 8 * st;
+              // scale chunks: 32 rows x 16 bytes each, no swizzle, 8-row groups 128 B apart
+              tmem_cp_32x128b_x4<CG>(tSA, smem_desc(sSA, 0, 128, 0));
+              tmem_cp_32x128b_x4<CG>(tSB, smem_desc(sSB, 0, 128, 0));
+              tmem_cp_32x128b_x4<CG>(tSB + 4, smem_desc(sSB + 512, 0, 128, 0));
+              const uint32_t acc0 = ks != 0;
+#pragma unroll
+              for (int k = 0; k < 4; ++k) {
+                // A: K-major, 128-byte swizzle, 8-row groups 1024 B apart; 32 B per K=32
+                const uint64_t ad = smem_desc(sA + 32 * k, 0, 1024, 2);
+                // B: N-major, 128-byte swizzle; 128-column chunks 16 KB apart,
+                // 8-row K groups 1024 B apart; 32 rows (4 KB) per K=32
+                const uint64_t bd = smem_desc(sB + 4096 * k, 16384, 1024, 2);
+                mma_mxf8<CG>(tmem + C::TM_ACC, ad, bd, idesc_mxf8(128 * CG, 256, k, k), tSA, tSB,
+                             acc0 | (k != 0));
+              }
+              if constexpr (CG == 1) tc_commit(bar_empty + 8 * st);
+              else tc_commit_pair(bar_empty + 8 * st, 0x3);
+              if (++ks == p.k_steps) {
+                ks = 0;
+                if constexpr (CG == 1) tc_commit(bar_acc_full);
+                else tc_commit_pair(bar_acc_full, 0x3);
+                acc_phase ^= 1u;
+                t += tile_stride;
+                if (t >= p.num_tiles) {
+                  ok = false;
+                } else if (!wait_phase<CL>(bar_acc_empty, acc_phase ^ 1u, wc,
+                                           0x02 | ((t & 0xFFFF) << 16))) {
+                  ok = false;
+                } else {
+                  tc_fence_after();
+                }
+              }
+            }
           }
         }
-        if (!ok) break;
-        if constexpr (CG == 1) tc_commit(bar_acc_full);
-        else tc_commit_pair(bar_acc_full, 0x3);
-        acc_phase ^= 1u;
+        if (ok) phase ^= 1u;
       }
       // all issued tcgen05 work has finished before TMEM can be released
       if constexpr (CG == 1) tc_commit(bar_final);
@@ -321,6 +350,13 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
     for (int t = first_tile; t < p.num_tiles; t += tile_stride) {
       int mt, nt;
       tile_coords(t, p.m_tiles, p.n_tiles, mt, nt);
+      if (p.use_acc && p.tma_store && lane == 0) {
+        // pull this warp's part of C_in into L2 while the tile's MMAs run
+        const int r0 = mt * (128 * CG) + 128 * (int)rank + 32 * q;
+        const int cw = p.out_bf16 ? 32 : 16;
+        for (int c0 = nt * 256 + 128 * h; c0 < nt * 256 + 128 * h + 128 && c0 < p.N && r0 < p.M; c0 += cw)
+          tma_prefetch_l2_2d(&tmC, c0, r0);
+      }
       int ok = 1;
       if (lane == 0) ok = wait_phase<CL>(bar_acc_full, acc_phase, wc, 0x05 | ((t & 0xFFFF) << 16));
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
@@ -341,78 +377,121 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
       }
       acc_phase ^= 1u;
 
-      const int row = mt * (128 * CG) + 128 * (int)rank + 32 * q + lane;
+      const int row0w = mt * (128 * CG) + 128 * (int)rank + 32 * q;  // this warp's first row
+      const int row = row0w + lane;
       const int colb = nt * 256 + 128 * h;
-      if (row < p.M) {
+      if (p.use_acc && row < p.M) {
+        // C_in: this lane's row, 128 columns (the prefetch below put them in L2)
         if (!p.out_bf16) {
-          float *cp = reinterpret_cast<float *>(p.C) + static_cast<int64_t>(row) * p.N + colb;
-          if (p.vec_ok && colb + 128 <= p.N) {
+          const float *cp = reinterpret_cast<const float *>(p.C) + static_cast<int64_t>(row) * p.N + colb;
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-              float4 o = make_float4(__uint_as_float(v[c >> 3][(c & 7) * 4 + 0]),
-                                     __uint_as_float(v[c >> 3][(c & 7) * 4 + 1]),
-                                     __uint_as_float(v[c >> 3][(c & 7) * 4 + 2]),
-                                     __uint_as_float(v[c >> 3][(c & 7) * 4 + 3]));
-              float4 *dst = reinterpret_cast<float4 *>(cp + 4 * c);
-              if (p.use_acc) {
-                const float4 old = *dst;
-                o.x += old.x;
-                o.y += old.y;
-                o.z += old.z;
-                o.w += old.w;
-              }
-              *dst = o;
-            }
-          } else {
+          for (int c = 0; c < 128; c += 4) {
+            if (p.vec_ok && colb + c + 4 <= p.N) {
+              const float4 o = *reinterpret_cast<const float4 *>(cp + c);
+              v[c >> 5][(c & 31) + 0] = __float_as_uint(__uint_as_float(v[c >> 5][(c & 31) + 0]) + o.x);
+              v[c >> 5][(c & 31) + 1] = __float_as_uint(__uint_as_float(v[c >> 5][(c & 31) + 1]) + o.y);
+              v[c >> 5][(c & 31) + 2] = __float_as_uint(__uint_as_float(v[c >> 5][(c & 31) + 2]) + o.z);
+              v[c >> 5][(c & 31) + 3] = __float_as_uint(__uint_as_float(v[c >> 5][(c & 31) + 3]) + o.w);
+            } else {
 #pragma unroll
-            for (int c = 0; c < 128; ++c) {
-              if (colb + c < p.N) {
-                float o = __uint_as_float(v[c >> 5][c & 31]);
-                if (p.use_acc) o += cp[c];
-                cp[c] = o;
-              }
+              for (int e = 0; e < 4; ++e)
+                if (colb + c + e < p.N)
+                  v[c >> 5][(c & 31) + e] =
+                      __float_as_uint(__uint_as_float(v[c >> 5][(c & 31) + e]) + cp[c + e]);
             }
           }
         } else {
-          __nv_bfloat16 *cp =
-              reinterpret_cast<__nv_bfloat16 *>(p.C) + static_cast<int64_t>(row) * p.N + colb;
-          if (p.vec_ok && colb + 128 <= p.N) {
+          const __nv_bfloat16 *cp =
+              reinterpret_cast<const __nv_bfloat16 *>(p.C) + static_cast<int64_t>(row) * p.N + colb;
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-              uint4 *dst = reinterpret_cast<uint4 *>(cp + 8 * c);
-              float f[8];
-#pragma unroll
-              for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(v[(8 * c + e) >> 5][(8 * c + e) & 31]);
-              if (p.use_acc) {
-                const uint4 old = *dst;
-                const uint32_t ow[4] = {old.x, old.y, old.z, old.w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  f[2 * e] += __uint_as_float(ow[e] << 16);
-                  f[2 * e + 1] += __uint_as_float(ow[e] & 0xFFFF0000u);
-                }
-              }
-              uint32_t w[4];
+          for (int c = 0; c < 128; c += 8) {
+            if (p.vec_ok && colb + c + 8 <= p.N) {
+              const uint4 o = *reinterpret_cast<const uint4 *>(cp + c);
+              const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
 #pragma unroll
               for (int e = 0; e < 4; ++e) {
-                const __nv_bfloat162 b2 = __floats2bfloat162_rn(f[2 * e], f[2 * e + 1]);
-                w[e] = *reinterpret_cast<const uint32_t *>(&b2);
+                v[c >> 5][(c & 31) + 2 * e] = __float_as_uint(
+                    __uint_as_float(v[c >> 5][(c & 31) + 2 * e]) + __uint_as_float(ow[e] << 16));
+                v[c >> 5][(c & 31) + 2 * e + 1] = __float_as_uint(
+                    __uint_as_float(v[c >> 5][(c & 31) + 2 * e + 1]) + __uint_as_float(ow[e] & 0xFFFF0000u));
               }
-              *dst = make_uint4(w[0], w[1], w[2], w[3]);
-            }
-          } else {
+            } else {
 #pragma unroll
-            for (int c = 0; c < 128; ++c) {
-              if (colb + c < p.N) {
-                float o = __uint_as_float(v[c >> 5][c & 31]);
-                if (p.use_acc) o += __bfloat162float(cp[c]);
-                cp[c] = __float2bfloat16_rn(o);
-              }
+              for (int e = 0; e < 8; ++e)
+                if (colb + c + e < p.N)
+                  v[c >> 5][(c & 31) + e] = __float_as_uint(__uint_as_float(v[c >> 5][(c & 31) + e]) +
+                                                            __bfloat162float(cp[c + e]));
             }
           }
         }
       }
+
+      if (p.tma_store) {
+        // 64-byte-wide column chunks through this warp's staging buffer: lane
+        // l writes row l (64-byte swizzle: 16-byte unit u of row r sits at
+        // u ^ ((r >> 1) & 3)), then one lane issues the TMA store, which
+        // clips rows >= M and columns >= N.
+        const uint32_t buf = base + C::OFF_EPI + ew * C::EPI_BUF;
+        const uint32_t rowaddr = buf + lane * 64;
+        const uint32_t swz = (lane >> 1) & 3;
+        constexpr int CHUNKS = 8;  // FP32: 16 columns per chunk; BF16: 32 columns per chunk
+        if (row0w < p.M) {
+#pragma unroll
+          for (int ch = 0; ch < CHUNKS; ++ch) {
+            const int ccols = p.out_bf16 ? 32 : 16;
+            if (p.out_bf16 && ch >= 4) break;
+            const int c0 = colb + ch * ccols;
+            if (c0 >= p.N) break;
+            if (lane == 0) bulk_wait_read_all();
+            __syncwarp();
+            if (!p.out_bf16) {
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                const int c = ch * 16 + 4 * u;
+                st_shared_v4(rowaddr + ((u ^ swz) << 4), v[c >> 5][c & 31], v[c >> 5][(c & 31) + 1],
+                             v[c >> 5][(c & 31) + 2], v[c >> 5][(c & 31) + 3]);
+              }
+            } else {
+#pragma unroll
+              for (int u = 0; u < 4; ++u) {
+                uint32_t w[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                  const int c = (ch & 3) * 32 + 8 * u + 2 * e;
+                  const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[c >> 5][c & 31]),
+                                                                  __uint_as_float(v[c >> 5][(c & 31) + 1]));
+                  w[e] = *reinterpret_cast<const uint32_t *>(&b2);
+                }
+                st_shared_v4(rowaddr + ((u ^ swz) << 4), w[0], w[1], w[2], w[3]);
+              }
+            }
+            fence_proxy_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+              tma_store_2d(&tmC, buf, c0, row0w);
+              bulk_commit_group();
+            }
+          }
+        }
+      } else if (row < p.M) {
+        // C rows not 16-byte aligned: direct stores
+        if (!p.out_bf16) {
+          float *cp = reinterpret_cast<float *>(p.C) + static_cast<int64_t>(row) * p.N + colb;
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (colb + c < p.N) cp[c] = __uint_as_float(v[c >> 5][c & 31]);
+        } else {
+          __nv_bfloat16 *cp =
+              reinterpret_cast<__nv_bfloat16 *>(p.C) + static_cast<int64_t>(row) * p.N + colb;
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (colb + c < p.N) cp[c] = __float2bfloat16_rn(__uint_as_float(v[c >> 5][c & 31]));
+        }
+      }
     }
+    // every store of this warp has completed before the CTA may finish
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
   }
 
   // ------------------------------------------------------------ teardown
@@ -431,27 +510,49 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
 // or K-block is out of range).  This is the 32-row x 16-byte source shape of
 // tcgen05.cp .32x128b.warpx4, which replicates it into the four TMEM lane
 // quarters: TMEM column c+(r/32), lane (r%32) of every quarter, byte j.
-__global__ void repack_scales_kernel(const uint8_t *__restrict__ S, int64_t rows, int kb_count,
-                                     int k_steps, int atoms, int64_t total_words,
-                                     uint32_t *__restrict__ out) {
-  for (int64_t w = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; w < total_words;
-       w += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t g = w >> 7;
-    const int t = static_cast<int>(w & 127);
-    const int a = static_cast<int>(g % atoms);
-    const int64_t rest = g / atoms;
-    const int ks = static_cast<int>(rest % k_steps);
-    const int64_t tile = rest / k_steps;
-    const int r = (t & 3) * 32 + (t >> 2);
-    const int64_t row = (tile * atoms + a) * 128 + r;
-    uint32_t word = 0;
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const int kb = ks * 4 + j;
-      const uint32_t byte = (row < rows && kb < kb_count) ? S[row * kb_count + kb] : 127u;
-      word |= byte << (8 * j);
-    }
-    out[w] = word;
+//
+// One launch repacks both operands.  A CTA takes 128 rows x 64 K-blocks of
+// one operand: coalesced byte reads of the rows into shared memory, then
+// coalesced 4-byte writes of the 16 chunks they form.
+struct RepackArgs {
+  const uint8_t *S;   // scales, rows x kb_count
+  uint32_t *out;      // chunks
+  int64_t rows;
+  int kb_count;
+  int k_steps;
+  int atoms;          // 128-row blocks per tile of this operand
+  int row_blocks;     // 128-row blocks to produce (tiles * atoms)
+  int kgroups;        // ceil(k_steps / 16)
+};
+
+constexpr int kRepackThreads = 512;
+
+__global__ void __launch_bounds__(kRepackThreads)
+    repack_scales_kernel(RepackArgs a0, RepackArgs a1, int blocks0) {
+  __shared__ uint32_t tile[128 * 16];  // 128 rows x 64 bytes
+  const bool second = static_cast<int>(blockIdx.x) >= blocks0;
+  const RepackArgs a = second ? a1 : a0;
+  const int b = second ? static_cast<int>(blockIdx.x) - blocks0 : static_cast<int>(blockIdx.x);
+  const int rb = b / a.kgroups;          // 128-row block
+  const int kg = b - rb * a.kgroups;     // group of 16 K steps
+  const int64_t row0 = static_cast<int64_t>(rb) * 128;
+  const int kb0 = kg * 64;
+  uint8_t *t8 = reinterpret_cast<uint8_t *>(tile);
+  for (int i = threadIdx.x; i < 128 * 64; i += kRepackThreads) {
+    const int r = i >> 6, c = i & 63;
+    const int64_t row = row0 + r;
+    const int kb = kb0 + c;
+    t8[i] = (row < a.rows && kb < a.kb_count) ? a.S[row * a.kb_count + kb] : static_cast<uint8_t>(127);
+  }
+  __syncthreads();
+  const int tile_idx = rb / a.atoms, at = rb - tile_idx * a.atoms;
+  const int nks = min(16, a.k_steps - kg * 16);
+  for (int i = threadIdx.x; i < nks * 128; i += kRepackThreads) {
+    const int ksl = i >> 7, w = i & 127;
+    const int r = (w & 3) * 32 + (w >> 2);
+    const int ks = kg * 16 + ksl;
+    const int64_t g = (static_cast<int64_t>(tile_idx) * a.k_steps + ks) * a.atoms + at;
+    a.out[g * 128 + w] = tile[r * 16 + ksl];
   }
 }
 

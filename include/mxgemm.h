@@ -112,6 +112,18 @@ int mxgemm_set_option(mxgemm_handle_t h, int option, int64_t value);
 int mxgemm_get_device_status(mxgemm_handle_t h, mxgemm_stream_t stream,
                              int *status_out, int *detail_out);
 
+/* Timing hook: record the CUDA events `ev_before` and `ev_after`
+ * (cudaEvent_t handles created by the caller; either may be NULL) on the
+ * run's stream immediately before and after the GEMM kernel launch of every
+ * later mxgemm_run on this handle, so that the kernel alone can be timed
+ * with the caller's events.  Passing NULL, NULL turns the hook off.  The
+ * handle does not own the events. */
+int mxgemm_set_profile_events(mxgemm_handle_t h, void *ev_before, void *ev_after);
+
+/* Number of kernels this handle has launched so far (the GEMM kernel and its
+ * prepasses), in *count_out. */
+int mxgemm_get_launch_count(mxgemm_handle_t h, int64_t *count_out);
+
 /* Free the handle's device memory (synchronizes its device) and the handle. */
 int mxgemm_destroy(mxgemm_handle_t h);
 
