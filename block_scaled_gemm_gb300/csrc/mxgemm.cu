@@ -27,6 +27,38 @@ struct Workspace {
   size_t bytes = 0;
 };
 
+// Everything a run needs besides its launches, keyed by the run's arguments.
+// Repeated calls on the same buffers (a serving or training loop) skip the
+// pointer checks and tensor-map encoding.
+struct Plan {
+  bool valid = false;
+  // key
+  int64_t M = 0, N = 0, K = 0;
+  const void *A = nullptr, *As = nullptr, *B = nullptr, *Bs = nullptr;
+  void *C = nullptr;
+  int use_acc = 0, out_dtype = 0, mode = 0, stall = 0, sched = 0;
+  long long timeout_ns = 0;
+  uint8_t *ws = nullptr;
+  // value
+  int CG = 1;
+  bool pad_b = false;
+  int64_t npad = 0;
+  CUtensorMap tA, tB, tSA, tSB, tC;
+  KParams kp;
+  mxg::RepackArgs ra, rb;
+  int blocks_a = 0, blocks_b = 0;
+
+  bool matches(int64_t M_, int64_t N_, int64_t K_, const void *A_, const void *As_, const void *B_,
+               const void *Bs_, void *C_, int ua, int od, int md, int sl, int sc, long long to,
+               uint8_t *w) const {
+    return valid && M == M_ && N == N_ && K == K_ && A == A_ && As == As_ && B == B_ &&
+           Bs == Bs_ && C == C_ && use_acc == ua && out_dtype == od && mode == md &&
+           stall == sl && sched == sc && timeout_ns == to && ws == w;
+  }
+};
+
+constexpr int kPlanCache = 8;
+
 }  // namespace
 
 struct mxgemm_ctx {
@@ -43,6 +75,8 @@ struct mxgemm_ctx {
   cudaEvent_t prof_before = nullptr;
   cudaEvent_t prof_after = nullptr;
   int64_t launches = 0;
+  Plan plans[kPlanCache];
+  int next_plan = 0;
 };
 
 namespace {
@@ -103,6 +137,7 @@ int ensure_workspace(mxgemm_ctx *h, size_t bytes, cudaStream_t stream) {
   }
   h->ws.ptr = static_cast<uint8_t *>(p);
   h->ws.bytes = want;
+  for (Plan &pl : h->plans) pl.valid = false;
   return MXGEMM_OK;
 }
 
@@ -128,15 +163,19 @@ int launch_gemm(mxgemm_ctx *h, const CUtensorMap &tA, const CUtensorMap &tB,
   cfg.blockDim = dim3(C::THREADS, 1, 1);
   cfg.dynamicSmemBytes = C::SMEM_BYTES;
   cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  cfg.numAttrs = 0;
+  cudaLaunchAttribute attr[2];
+  // the kernel may start while the scale prepass before it finishes; it
+  // waits (griddepcontrol.wait) before touching global memory
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (CG == 2) {
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.numAttrs = 2;
   }
   if (h->prof_before && cudaEventRecord(h->prof_before, stream) != cudaSuccess) {
     cudaGetLastError();
@@ -160,6 +199,74 @@ int launch_blocks(int64_t work, int per_block) {
   if (b < 1) b = 1;
   if (b > 4096) b = 4096;
   return static_cast<int>(b);
+}
+
+// Validate-once work of a run: prepass arguments, tensor maps and kernel
+// parameters, stored in `pl` under the run's key.
+int build_plan(mxgemm_ctx *h, Plan *pl, int64_t M, int64_t N, int64_t K, const void *A,
+               const void *A_scale, const void *B, const void *B_scale, void *C, int use_acc,
+               int out_dtype, int CG, int64_t m_tiles, int64_t n_tiles, int64_t k_steps,
+               int64_t num_tiles, int64_t a_chunks, int64_t b_chunks, bool pad_b, int64_t npad,
+               size_t off_sfb, size_t off_b) {
+  const size_t esz = out_dtype == MXGEMM_OUT_F32 ? 4 : 2;
+  const int64_t kb = K / 32;
+  uint8_t *sfa = h->ws.ptr;
+  uint8_t *sfb = h->ws.ptr + off_sfb;
+  const void *bsrc = pad_b ? static_cast<const void *>(h->ws.ptr + off_b) : B;
+  const int64_t bpitch = pad_b ? npad : N;
+  pl->ra = mxg::RepackArgs{static_cast<const uint8_t *>(A_scale), reinterpret_cast<uint32_t *>(sfa),
+                           M, static_cast<int>(kb), static_cast<int>(k_steps), 1,
+                           static_cast<int>(m_tiles * CG), static_cast<int>(cdiv(k_steps, 16))};
+  pl->rb = mxg::RepackArgs{static_cast<const uint8_t *>(B_scale), reinterpret_cast<uint32_t *>(sfb),
+                           N, static_cast<int>(kb), static_cast<int>(k_steps), 2,
+                           static_cast<int>(n_tiles * 2), static_cast<int>(cdiv(k_steps, 16))};
+  pl->blocks_a = pl->ra.row_blocks * pl->ra.kgroups;
+  pl->blocks_b = pl->rb.row_blocks * pl->rb.kgroups;
+  const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+  if (encode_2d(h, &pl->tA, u8, A, K, M, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      encode_2d(h, &pl->tB, u8, bsrc, N, K, bpitch, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      encode_2d(h, &pl->tSA, u8, sfa, 16, a_chunks * 32, 16, 16, 32, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      encode_2d(h, &pl->tSB, u8, sfb, 16, b_chunks * 32, 16, 16, 64, CU_TENSOR_MAP_SWIZZLE_NONE))
+    return MXGEMM_ERR_CUDA;
+  // C: stored through TMA (64-byte-wide boxes, 32 rows) when its row pitch
+  // allows it; otherwise the kernel stores directly and tC is unused.
+  const bool tma_store = (static_cast<size_t>(N) * esz) % 16 == 0;
+  std::memset(&pl->tC, 0, sizeof(pl->tC));
+  if (tma_store &&
+      encode_2d(h, &pl->tC,
+                out_dtype == MXGEMM_OUT_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                            : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
+                C, N, M, static_cast<uint64_t>(N) * esz, static_cast<uint32_t>(64 / esz), 32,
+                CU_TENSOR_MAP_SWIZZLE_64B))
+    return MXGEMM_ERR_CUDA;
+  KParams &kp = pl->kp;
+  std::memset(&kp, 0, sizeof(kp));
+  kp.M = static_cast<int>(M);
+  kp.N = static_cast<int>(N);
+  kp.K = static_cast<int>(K);
+  kp.m_tiles = static_cast<int>(m_tiles);
+  kp.n_tiles = static_cast<int>(n_tiles);
+  kp.k_steps = static_cast<int>(k_steps);
+  kp.num_tiles = static_cast<int>(num_tiles);
+  kp.C = C;
+  kp.out_bf16 = out_dtype == MXGEMM_OUT_BF16;
+  kp.use_acc = use_acc;
+  kp.vec_ok = (N % (out_dtype == MXGEMM_OUT_F32 ? 4 : 8)) == 0;
+  kp.tma_store = tma_store;
+  kp.status = h->d_status;
+  kp.timeout_ns = static_cast<unsigned long long>(h->timeout_ns);
+  kp.stall_producer = h->stall_producer;
+  kp.use_clc = h->scheduler;
+  pl->CG = CG;
+  pl->pad_b = pad_b;
+  pl->npad = npad;
+  pl->M = M; pl->N = N; pl->K = K;
+  pl->A = A; pl->As = A_scale; pl->B = B; pl->Bs = B_scale; pl->C = C;
+  pl->use_acc = use_acc; pl->out_dtype = out_dtype; pl->mode = h->mode;
+  pl->stall = h->stall_producer; pl->sched = h->scheduler; pl->timeout_ns = h->timeout_ns;
+  pl->ws = h->ws.ptr;
+  pl->valid = true;
+  return MXGEMM_OK;
 }
 
 }  // namespace
@@ -262,8 +369,8 @@ int mxgemm_run(mxgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A
   if (reinterpret_cast<uintptr_t>(C) % 16) return MXGEMM_ERR_MISALIGNED;
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   DeviceGuard g(h->device);
-  if (!on_device(C, h->device)) return MXGEMM_ERR_INVALID_VALUE;
   if (K == 0) {
+    if (!on_device(C, h->device)) return MXGEMM_ERR_INVALID_VALUE;
     if (use_acc) return MXGEMM_OK;
     if (cudaMemsetAsync(C, 0, static_cast<size_t>(M) * N * esz, stream) != cudaSuccess) {
       cudaGetLastError();
@@ -274,11 +381,8 @@ int mxgemm_run(mxgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A
   if (!A || !B || !A_scale || !B_scale) return MXGEMM_ERR_INVALID_VALUE;
   if (reinterpret_cast<uintptr_t>(A) % 16 || reinterpret_cast<uintptr_t>(B) % 16)
     return MXGEMM_ERR_MISALIGNED;
-  if (!on_device(A, h->device) || !on_device(B, h->device) || !on_device(A_scale, h->device) ||
-      !on_device(B_scale, h->device))
-    return MXGEMM_ERR_INVALID_VALUE;
 
-  // ---- plan
+  // workspace size depends only on the shape and mode
   int CG = 1;
   if (h->mode == 2) CG = 2;
   // mode 0 (automatic) currently selects the single-CTA tile
@@ -287,81 +391,50 @@ int mxgemm_run(mxgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A
   const int64_t k_steps = cdiv(K, 128);
   const int64_t num_tiles = m_tiles * n_tiles;
   if (num_tiles >= lim) return MXGEMM_ERR_INVALID_VALUE;
-  const int64_t kb = K / 32;
-  const int64_t a_chunks = m_tiles * CG * k_steps;      // 512-byte chunks of A scales
-  const int64_t b_chunks = n_tiles * k_steps * 2;       // 2 per 256 columns
+  const int64_t a_chunks = m_tiles * CG * k_steps;  // 512-byte chunks of A scales
+  const int64_t b_chunks = n_tiles * k_steps * 2;   // 2 per 256 columns
   const bool pad_b = (N % 16) != 0;
   const int64_t npad = round_up(static_cast<size_t>(N), 16);
-  const size_t off_sfa = 0;
   const size_t off_sfb = round_up(static_cast<size_t>(a_chunks) * 512, 1024);
   const size_t off_b = round_up(off_sfb + static_cast<size_t>(b_chunks) * 512, 1024);
   const size_t ws_bytes = off_b + (pad_b ? static_cast<size_t>(K) * npad : 0);
-  int st = ensure_workspace(h, ws_bytes, stream);
-  if (st != MXGEMM_OK) return st;
-  uint8_t *sfa = h->ws.ptr + off_sfa;
-  uint8_t *sfb = h->ws.ptr + off_sfb;
-  const uint8_t *bsrc = static_cast<const uint8_t *>(B);
-  int64_t bpitch = N;
-  if (pad_b) {
-    uint8_t *bp = h->ws.ptr + off_b;
-    mxg::pad_rows_kernel<<<launch_blocks(K * (npad / 16), 256), 256, 0, stream>>>(
-        static_cast<const uint8_t *>(B), K, N, npad, bp);
-    bsrc = bp;
-    bpitch = npad;
+
+  Plan *plan = nullptr;
+  for (Plan &pl : h->plans)
+    if (pl.matches(M, N, K, A, A_scale, B, B_scale, C, use_acc, out_dtype, h->mode,
+                   h->stall_producer, h->scheduler, h->timeout_ns, h->ws.ptr) &&
+        h->ws.bytes >= ws_bytes) {
+      plan = &pl;
+      break;
+    }
+  if (!plan) {
+    if (!on_device(C, h->device) || !on_device(A, h->device) || !on_device(B, h->device) ||
+        !on_device(A_scale, h->device) || !on_device(B_scale, h->device))
+      return MXGEMM_ERR_INVALID_VALUE;
+    int st = ensure_workspace(h, ws_bytes, stream);
+    if (st != MXGEMM_OK) return st;
+    plan = &h->plans[h->next_plan];
+    h->next_plan = (h->next_plan + 1) % kPlanCache;
+    plan->valid = false;
+    st = build_plan(h, plan, M, N, K, A, A_scale, B, B_scale, C, use_acc, out_dtype, CG, m_tiles,
+                    n_tiles, k_steps, num_tiles, a_chunks, b_chunks, pad_b, npad, off_sfb, off_b);
+    if (st != MXGEMM_OK) return st;
+  }
+
+  // ---- launches: [B re-pitch], scale repack, GEMM
+  if (plan->pad_b) {
+    mxg::pad_rows_kernel<<<launch_blocks(K * (plan->npad / 16), 256), 256, 0, stream>>>(
+        static_cast<const uint8_t *>(B), K, N, plan->npad, h->ws.ptr + off_b);
     ++h->launches;
   }
-  mxg::RepackArgs ra{static_cast<const uint8_t *>(A_scale), reinterpret_cast<uint32_t *>(sfa), M,
-                     static_cast<int>(kb), static_cast<int>(k_steps), 1,
-                     static_cast<int>(m_tiles * CG), static_cast<int>(cdiv(k_steps, 16))};
-  mxg::RepackArgs rb{static_cast<const uint8_t *>(B_scale), reinterpret_cast<uint32_t *>(sfb), N,
-                     static_cast<int>(kb), static_cast<int>(k_steps), 2,
-                     static_cast<int>(n_tiles * 2), static_cast<int>(cdiv(k_steps, 16))};
-  const int blocks_a = ra.row_blocks * ra.kgroups;
-  const int blocks_b = rb.row_blocks * rb.kgroups;
-  mxg::repack_scales_kernel<<<blocks_a + blocks_b, mxg::kRepackThreads, 0, stream>>>(ra, rb, blocks_a);
+  mxg::repack_scales_kernel<<<plan->blocks_a + plan->blocks_b, mxg::kRepackThreads, 0, stream>>>(
+      plan->ra, plan->rb, plan->blocks_a);
   h->launches += 1;
   if (cudaGetLastError() != cudaSuccess) return MXGEMM_ERR_CUDA;
-
-  // ---- tensor maps
-  CUtensorMap tA, tB, tSA, tSB, tC;
-  const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
-  if (encode_2d(h, &tA, u8, A, K, M, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      encode_2d(h, &tB, u8, bsrc, N, K, bpitch, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      encode_2d(h, &tSA, u8, sfa, 16, a_chunks * 32, 16, 16, 32, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-      encode_2d(h, &tSB, u8, sfb, 16, b_chunks * 32, 16, 16, 64, CU_TENSOR_MAP_SWIZZLE_NONE))
-    return MXGEMM_ERR_CUDA;
-  // C: stored through TMA (64-byte-wide boxes, 32 rows) when its row pitch
-  // allows it; otherwise the kernel stores directly and tC is unused.
-  const bool tma_store = (static_cast<size_t>(N) * esz) % 16 == 0;
-  std::memset(&tC, 0, sizeof(tC));
-  if (tma_store &&
-      encode_2d(h, &tC,
-                out_dtype == MXGEMM_OUT_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
-                                            : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                C, N, M, static_cast<uint64_t>(N) * esz, static_cast<uint32_t>(64 / esz), 32,
-                CU_TENSOR_MAP_SWIZZLE_64B))
-    return MXGEMM_ERR_CUDA;
-
-  KParams kp;
-  std::memset(&kp, 0, sizeof(kp));
-  kp.M = static_cast<int>(M);
-  kp.N = static_cast<int>(N);
-  kp.K = static_cast<int>(K);
-  kp.m_tiles = static_cast<int>(m_tiles);
-  kp.n_tiles = static_cast<int>(n_tiles);
-  kp.k_steps = static_cast<int>(k_steps);
-  kp.num_tiles = static_cast<int>(num_tiles);
-  kp.C = C;
-  kp.out_bf16 = out_dtype == MXGEMM_OUT_BF16;
-  kp.use_acc = use_acc;
-  kp.vec_ok = (N % (out_dtype == MXGEMM_OUT_F32 ? 4 : 8)) == 0;
-  kp.tma_store = tma_store;
-  kp.status = h->d_status;
-  kp.timeout_ns = static_cast<unsigned long long>(h->timeout_ns);
-  kp.stall_producer = h->stall_producer;
-  kp.use_clc = h->scheduler;
-  return CG == 2 ? launch_gemm<2>(h, tA, tB, tSA, tSB, tC, kp, stream)
-                 : launch_gemm<1>(h, tA, tB, tSA, tSB, tC, kp, stream);
+  return plan->CG == 2 ? launch_gemm<2>(h, plan->tA, plan->tB, plan->tSA, plan->tSB, plan->tC,
+                                        plan->kp, stream)
+                       : launch_gemm<1>(h, plan->tA, plan->tB, plan->tSA, plan->tSB, plan->tC,
+                                        plan->kp, stream);
 }
 
 int mxgemm_get_device_status(mxgemm_handle_t h, mxgemm_stream_t stream_, int *status_out,

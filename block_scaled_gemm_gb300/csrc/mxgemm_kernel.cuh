@@ -198,6 +198,10 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
   if constexpr (CG == 2) cluster_sync(); else __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
+  // The set-up above overlaps the tail of the scale prepass (programmatic
+  // dependent launch); nothing below reads or writes global memory before
+  // that grid has finished.
+  griddep_wait();
 
   const WaitCtl wc{p.status, abort_flag, p.timeout_ns};
   constexpr bool CL = (CG == 2);
@@ -533,6 +537,7 @@ __global__ void __launch_bounds__(kRepackThreads)
   const bool second = static_cast<int>(blockIdx.x) >= blocks0;
   const RepackArgs a = second ? a1 : a0;
   const int b = second ? static_cast<int>(blockIdx.x) - blocks0 : static_cast<int>(blockIdx.x);
+  griddep_launch_dependents();
   const int rb = b / a.kgroups;          // 128-row block
   const int kg = b - rb * a.kgroups;     // group of 16 K steps
   const int64_t row0 = static_cast<int64_t>(rb) * 128;
@@ -562,6 +567,7 @@ __global__ void pad_rows_kernel(const uint8_t *__restrict__ B, int64_t rows, int
                                 int64_t Npad, uint8_t *__restrict__ out) {
   const int64_t per_row = Npad / 16;
   const int64_t total = rows * per_row;
+  griddep_launch_dependents();
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t r = i / per_row;

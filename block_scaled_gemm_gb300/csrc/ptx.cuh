@@ -306,6 +306,18 @@ __device__ __forceinline__ void cluster_sync() {
   cluster_wait();
 }
 
+// ---------------------------------------------------------------- PDL
+// Programmatic dependent launch: a grid launched with programmatic stream
+// serialization may start before the previous grid in the stream finishes;
+// griddep_wait blocks until that grid has completed and its memory writes
+// are visible.  griddep_launch_dependents lets the next grid start early.
+__device__ __forceinline__ void griddep_wait() {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+__device__ __forceinline__ void griddep_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---------------------------------------------------------------- CLC
 // Ask the hardware to cancel a not-yet-launched cluster and hand its
 // coordinates to this one; the 16-byte response lands at `resp` and its
