@@ -25,7 +25,8 @@ __all__ = [
     "OUT_F32", "OUT_BF16", "OPT_MODE", "OPT_WAIT_TIMEOUT_NS", "OPT_TEST_STALL_PRODUCER",
     "OPT_SCHEDULER", "MxgemmError", "library", "library_path", "mxgemm_create", "mxgemm_run",
     "mxgemm_destroy", "mxgemm_set_option", "mxgemm_get_device_status", "mxgemm_status_string",
-    "mxgemm_set_profile_events", "mxgemm_get_launch_count", "EXPORTED_SYMBOLS", "Gemm",
+    "mxgemm_set_profile_events", "mxgemm_get_launch_count", "mxgemm_run_noalloc",
+    "EXPORTED_SYMBOLS", "Gemm",
 ]
 
 OUT_F32 = 0
@@ -43,11 +44,12 @@ ERR_UNSUPPORTED_DEVICE = 3
 ERR_OUT_OF_MEMORY = 4
 ERR_CUDA = 5
 ERR_TIMEOUT = 6
+ERR_TOO_LARGE = 7
 
 EXPORTED_SYMBOLS = (
     "mxgemm_create", "mxgemm_run", "mxgemm_destroy", "mxgemm_set_option",
     "mxgemm_get_device_status", "mxgemm_status_string", "mxgemm_set_profile_events",
-    "mxgemm_get_launch_count",
+    "mxgemm_get_launch_count", "mxgemm_run_noalloc",
 )
 
 _lib = None
@@ -88,6 +90,8 @@ def library():
         lib.mxgemm_set_profile_events.restype = i32
         lib.mxgemm_get_launch_count.argtypes = [vp, ctypes.POINTER(i64)]
         lib.mxgemm_get_launch_count.restype = i32
+        lib.mxgemm_run_noalloc.argtypes = [i64, i64, i64, vp, vp, vp, vp, vp, i32, i32, vp]
+        lib.mxgemm_run_noalloc.restype = i32
         lib.mxgemm_status_string.argtypes = [i32]
         lib.mxgemm_status_string.restype = ctypes.c_char_p
         _lib = lib
@@ -132,6 +136,18 @@ def mxgemm_run(h, M, N, K, A, A_scale, B, B_scale, C, use_acc=0, out_dtype=OUT_F
                               _stream(stream))
     if check:
         _check(st, "mxgemm_run")
+    return st
+
+
+def mxgemm_run_noalloc(M, N, K, A, A_scale, B, B_scale, C, use_acc=0, out_dtype=OUT_F32,
+                       stream=None, check: bool = True) -> int:
+    """C (+)= A.B on the current device without allocating device memory
+    (fixed 16 MiB scratch shared by all calls; see include/mxgemm.h)."""
+    st = library().mxgemm_run_noalloc(int(M), int(N), int(K), _ptr(A), _ptr(A_scale), _ptr(B),
+                                      _ptr(B_scale), _ptr(C), int(bool(use_acc)), int(out_dtype),
+                                      _stream(stream))
+    if check:
+        _check(st, "mxgemm_run_noalloc")
     return st
 
 

@@ -12,6 +12,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 
 #include "mxgemm.h"
@@ -282,6 +283,8 @@ const char *mxgemm_status_string(int s) {
     case MXGEMM_ERR_OUT_OF_MEMORY: return "out of device memory";
     case MXGEMM_ERR_CUDA: return "CUDA call failed";
     case MXGEMM_ERR_TIMEOUT: return "device-side wait timed out";
+    case MXGEMM_ERR_TOO_LARGE:
+      return "problem needs more scratch than the fixed no-allocation buffer holds";
     default: return "unknown status";
   }
 }
@@ -478,3 +481,170 @@ int mxgemm_destroy(mxgemm_handle_t h) {
 }
 
 }  // extern "C"
+
+// ===========================================================================
+// mxgemm_run_noalloc: the same product without any device allocation.
+//
+// Callers that cannot allocate device memory where they call the GEMM (a
+// plug-in whose host framework owns all device memory, code that must not
+// allocate after start-up, a stream that is being captured) use this entry
+// point.  Its scratch (the repacked scales, and B re-pitched when N % 16 != 0)
+// lives in the file-scope array below, which the CUDA runtime places when it
+// loads this library's device code: every GPU that loads the library holds
+// these kNoAllocScratchBytes until the process exits.
+// ===========================================================================
+
+namespace {
+constexpr size_t kNoAllocScratchBytes = size_t(16) << 20;  // 16 MiB
+}  // namespace
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+static __device__ __align__(256) int g_noalloc_status[2];
+
+namespace {
+
+struct NoAllocDevice {
+  bool ready = false;
+  uint8_t *scratch = nullptr;  // this device's address of g_noalloc_scratch
+  int *status = nullptr;       // this device's address of g_noalloc_status
+  int sm_count = 0;
+  bool attr_set[3] = {false, false, false};
+};
+
+constexpr int kNoAllocMaxDevices = 64;
+NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
+std::mutex g_noalloc_mu;
+PFN_cuTensorMapEncodeTiled_v12000 g_noalloc_encode = nullptr;
+
+// Once per device, with that device current: check it, and look up the
+// device addresses of the scratch arrays (in host code their names are
+// host-side stand-ins, not device addresses).
+int noalloc_setup(int dev, NoAllocDevice **out) {
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (dev < 0 || dev >= kNoAllocMaxDevices) return MXGEMM_ERR_INVALID_VALUE;
+  NoAllocDevice &d = g_noalloc_dev[dev];
+  if (!d.ready) {
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+      cudaGetLastError();
+      return MXGEMM_ERR_CUDA;
+    }
+    if (!(major == 10 && minor == 3)) return MXGEMM_ERR_UNSUPPORTED_DEVICE;
+    if (!g_noalloc_encode) {
+      void *fn = nullptr;
+      cudaDriverEntryPointQueryResult q;
+      if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                           cudaEnableDefault, &q) != cudaSuccess ||
+          q != cudaDriverEntryPointSuccess || !fn) {
+        cudaGetLastError();
+        return MXGEMM_ERR_CUDA;
+      }
+      g_noalloc_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    void *scratch = nullptr, *status = nullptr;
+    if (cudaGetSymbolAddress(&scratch, g_noalloc_scratch) != cudaSuccess ||
+        cudaGetSymbolAddress(&status, g_noalloc_status) != cudaSuccess || !scratch || !status) {
+      cudaGetLastError();
+      return MXGEMM_ERR_CUDA;
+    }
+    d.scratch = static_cast<uint8_t *>(scratch);
+    d.status = static_cast<int *>(status);
+    d.sm_count = sms;
+    d.ready = true;
+  }
+  *out = &d;
+  return MXGEMM_OK;
+}
+
+}  // namespace
+
+extern "C" int mxgemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A,
+                                  const void *A_scale, const void *B, const void *B_scale,
+                                  void *C, int use_acc, int out_dtype, mxgemm_stream_t stream_) {
+  const int64_t lim = int64_t(1) << 31;
+  if (M < 0 || N < 0 || K < 0 || M >= lim || N >= lim || K >= lim) return MXGEMM_ERR_INVALID_VALUE;
+  if (K % 32 != 0) return MXGEMM_ERR_INVALID_VALUE;
+  if (out_dtype != MXGEMM_OUT_F32 && out_dtype != MXGEMM_OUT_BF16) return MXGEMM_ERR_INVALID_VALUE;
+  if (use_acc != 0 && use_acc != 1) return MXGEMM_ERR_INVALID_VALUE;
+  if (M == 0 || N == 0) return MXGEMM_OK;
+  const size_t esz = out_dtype == MXGEMM_OUT_F32 ? 4 : 2;
+  if (!C) return MXGEMM_ERR_INVALID_VALUE;
+  if (reinterpret_cast<uintptr_t>(C) % 16) return MXGEMM_ERR_MISALIGNED;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return MXGEMM_ERR_CUDA;
+  }
+  NoAllocDevice *nd = nullptr;
+  int st = noalloc_setup(dev, &nd);
+  if (st != MXGEMM_OK) return st;
+  if (K == 0) {
+    if (!on_device(C, dev)) return MXGEMM_ERR_INVALID_VALUE;
+    if (use_acc) return MXGEMM_OK;
+    if (cudaMemsetAsync(C, 0, static_cast<size_t>(M) * N * esz, stream) != cudaSuccess) {
+      cudaGetLastError();
+      return MXGEMM_ERR_CUDA;
+    }
+    return MXGEMM_OK;
+  }
+  if (!A || !B || !A_scale || !B_scale) return MXGEMM_ERR_INVALID_VALUE;
+  if (reinterpret_cast<uintptr_t>(A) % 16 || reinterpret_cast<uintptr_t>(B) % 16)
+    return MXGEMM_ERR_MISALIGNED;
+
+  // single-CTA tiles, as the automatic mode of mxgemm_run
+  const int CG = 1;
+  const int64_t m_tiles = cdiv(M, 128 * CG);
+  const int64_t n_tiles = cdiv(N, 256);
+  const int64_t k_steps = cdiv(K, 128);
+  const int64_t num_tiles = m_tiles * n_tiles;
+  if (num_tiles >= lim) return MXGEMM_ERR_INVALID_VALUE;
+  const int64_t a_chunks = m_tiles * CG * k_steps;
+  const int64_t b_chunks = n_tiles * k_steps * 2;
+  const bool pad_b = (N % 16) != 0;
+  const int64_t npad = round_up(static_cast<size_t>(N), 16);
+  const size_t off_sfb = round_up(static_cast<size_t>(a_chunks) * 512, 1024);
+  const size_t off_b = round_up(off_sfb + static_cast<size_t>(b_chunks) * 512, 1024);
+  const size_t ws_bytes = off_b + (pad_b ? static_cast<size_t>(K) * npad : 0);
+  if (ws_bytes > kNoAllocScratchBytes) return MXGEMM_ERR_TOO_LARGE;
+  if (!on_device(C, dev) || !on_device(A, dev) || !on_device(B, dev) ||
+      !on_device(A_scale, dev) || !on_device(B_scale, dev))
+    return MXGEMM_ERR_INVALID_VALUE;
+
+  // A handle-shaped context on the stack that points at the fixed scratch;
+  // nothing in it is allocated or freed.
+  mxgemm_ctx ctx;
+  ctx.device = dev;
+  ctx.sm_count = nd->sm_count;
+  ctx.d_status = nd->status;
+  ctx.ws.ptr = nd->scratch;
+  ctx.ws.bytes = kNoAllocScratchBytes;
+  ctx.encode = g_noalloc_encode;
+  {
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    for (int i = 0; i < 3; ++i) ctx.attr_set[i] = nd->attr_set[i];
+  }
+  Plan plan;
+  st = build_plan(&ctx, &plan, M, N, K, A, A_scale, B, B_scale, C, use_acc, out_dtype, CG, m_tiles,
+                  n_tiles, k_steps, num_tiles, a_chunks, b_chunks, pad_b, npad, off_sfb, off_b);
+  if (st != MXGEMM_OK) return st;
+  // the status word must start each call at zero
+  if (cudaMemsetAsync(nd->status, 0, 2 * sizeof(int), stream) != cudaSuccess) {
+    cudaGetLastError();
+    return MXGEMM_ERR_CUDA;
+  }
+  if (pad_b)
+    mxg::pad_rows_kernel<<<launch_blocks(K * (npad / 16), 256), 256, 0, stream>>>(
+        static_cast<const uint8_t *>(B), K, N, npad, nd->scratch + off_b);
+  mxg::repack_scales_kernel<<<plan.blocks_a + plan.blocks_b, mxg::kRepackThreads, 0, stream>>>(
+      plan.ra, plan.rb, plan.blocks_a);
+  if (cudaGetLastError() != cudaSuccess) return MXGEMM_ERR_CUDA;
+  st = launch_gemm<1>(&ctx, plan.tA, plan.tB, plan.tSA, plan.tSB, plan.tC, plan.kp, stream);
+  {
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    for (int i = 0; i < 3; ++i) nd->attr_set[i] = nd->attr_set[i] || ctx.attr_set[i];
+  }
+  return st;
+}

@@ -60,7 +60,8 @@ typedef enum {
   MXGEMM_ERR_UNSUPPORTED_DEVICE = 3, /* device is not compute capability 10.3 */
   MXGEMM_ERR_OUT_OF_MEMORY = 4,      /* workspace allocation failed */
   MXGEMM_ERR_CUDA = 5,               /* a CUDA runtime/driver call failed */
-  MXGEMM_ERR_TIMEOUT = 6             /* a device-side wait ran out (status word) */
+  MXGEMM_ERR_TIMEOUT = 6,            /* a device-side wait ran out (status word) */
+  MXGEMM_ERR_TOO_LARGE = 7           /* mxgemm_run_noalloc: scratch need above its fixed size */
 } mxgemm_status_t;
 
 /* Options for mxgemm_set_option. */
@@ -126,6 +127,35 @@ int mxgemm_get_launch_count(mxgemm_handle_t h, int64_t *count_out);
 
 /* Free the handle's device memory (synchronizes its device) and the handle. */
 int mxgemm_destroy(mxgemm_handle_t h);
+
+/* The same product as mxgemm_run, for callers that cannot allocate device
+ * memory where they call it: a plug-in whose host framework owns all device
+ * memory, code that must not allocate after start-up, or a stream that is
+ * being captured.  It takes no handle, allocates nothing (no cudaMalloc,
+ * cudaFree or allocating library call) and runs on the current device and
+ * the given stream.  The paper has no counterpart to this entry point.
+ *
+ * Scratch: the repacked scales (and B re-pitched to a 16-byte row pitch when
+ * N % 16 != 0) go to one file-scope device array of 16 MiB, which every GPU
+ * that loads this library holds until the process exits.  A problem needs
+ *   ceil(M/128)*ceil(K/128)*512 rounded up to 1 KiB
+ *   + ceil(N/256)*ceil(K/128)*1024 rounded up to 1 KiB
+ *   + (N % 16 ? K * round_up(N, 16) : 0)  bytes;
+ * more than 16 MiB is rejected with MXGEMM_ERR_TOO_LARGE before anything is
+ * enqueued.  All calls share that array and it keeps the last call's
+ * contents, so calls whose work overlaps on the GPU (different streams, or
+ * different host threads) race and must be serialised by the caller.
+ *
+ * The first call on a device does a one-time set-up for that device (device
+ * check and lookup of the array's device address); make that first call
+ * before starting any stream capture.  Arguments, layouts and use_acc are as
+ * for mxgemm_run; tile mode is automatic.  A device-side wait that runs out
+ * is recorded in an internal status word that this entry point cannot report:
+ * C is then incomplete. */
+int mxgemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A,
+                       const void *A_scale, const void *B, const void *B_scale,
+                       void *C, int use_acc, int out_dtype,
+                       mxgemm_stream_t stream);
 
 /* Static description of a status code. */
 const char *mxgemm_status_string(int status);

@@ -53,7 +53,7 @@ def test_null_handle_rejected(lib):
 
 
 def test_status_strings(lib):
-    for s in range(7):
+    for s in range(8):
         assert mx.mxgemm_status_string(s)
     assert "timed out" in mx.mxgemm_status_string(mx.ERR_TIMEOUT)
 
