@@ -48,8 +48,7 @@ WORKLOAD = "square_4096"
 FP8_OVER_BF16 = 2.0  # nominal dense MXFP8 / BF16 tensor rate (4.5 / 2.25 PFLOP/s)
 FALLBACK_BF16_BURST = 1900.0  # TFLOP/s, used only when MEASURED_PEAKS.json is absent
 KERNEL_SOURCES = ["block_scaled_gemm_gb300/csrc/mxgemm_kernel.cuh",
-                  "block_scaled_gemm_gb300/csrc/ptx.cuh",
-                  "block_scaled_gemm_gb300/csrc/mxgemm.cu"]
+                  "block_scaled_gemm_gb300/csrc/ptx.cuh"]
 PROFILE_SUMMARY = ROOT / "profiles" / "mxgemm_kernel_square_4096.md"
 
 

@@ -17,6 +17,7 @@
 
 #include "mxgemm.h"
 #include "mxgemm_kernel.cuh"
+#include "prepass.cuh"
 
 namespace {
 
@@ -72,7 +73,7 @@ struct mxgemm_ctx {
   int mode = 0;
   int stall_producer = 0;
   int scheduler = 0;
-  bool attr_set[3] = {false, false, false};
+  bool attr_set[3][8] = {};
   cudaEvent_t prof_before = nullptr;
   cudaEvent_t prof_after = nullptr;
   int64_t launches = 0;
@@ -142,19 +143,19 @@ int ensure_workspace(mxgemm_ctx *h, size_t bytes, cudaStream_t stream) {
   return MXGEMM_OK;
 }
 
-template <int CG>
-int launch_gemm(mxgemm_ctx *h, const CUtensorMap &tA, const CUtensorMap &tB,
-                const CUtensorMap &tSA, const CUtensorMap &tSB, const CUtensorMap &tC,
-                const KParams &kp, cudaStream_t stream) {
+template <int CG, int EPI>
+int launch_gemm_epi(mxgemm_ctx *h, const CUtensorMap &tA, const CUtensorMap &tB,
+                    const CUtensorMap &tSA, const CUtensorMap &tSB, const CUtensorMap &tC,
+                    const KParams &kp, cudaStream_t stream) {
   using C = Cfg<CG>;
-  auto kern = mxg::mxgemm_kernel<CG>;
-  if (!h->attr_set[CG]) {
+  auto kern = mxg::mxgemm_kernel<CG, EPI>;
+  if (!h->attr_set[CG][EPI]) {
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
         cudaSuccess) {
       cudaGetLastError();
       return MXGEMM_ERR_CUDA;
     }
-    h->attr_set[CG] = true;
+    h->attr_set[CG][EPI] = true;
   }
   const int units = h->sm_count / CG;
   const int clusters = kp.num_tiles < units ? kp.num_tiles : units;
@@ -195,6 +196,26 @@ int launch_gemm(mxgemm_ctx *h, const CUtensorMap &tA, const CUtensorMap &tB,
   return MXGEMM_OK;
 }
 
+// The kernel instantiation for this run's epilogue (output type, use_acc,
+// TMA or direct stores).
+template <int CG>
+int launch_gemm(mxgemm_ctx *h, const CUtensorMap &tA, const CUtensorMap &tB,
+                const CUtensorMap &tSA, const CUtensorMap &tSB, const CUtensorMap &tC,
+                const KParams &kp, cudaStream_t stream) {
+  const int epi = (kp.out_bf16 ? mxg::kEpiBF16 : 0) | (kp.use_acc ? mxg::kEpiAcc : 0) |
+                  (kp.tma_store ? mxg::kEpiTma : 0);
+  switch (epi) {
+    case 0: return launch_gemm_epi<CG, 0>(h, tA, tB, tSA, tSB, tC, kp, stream);
+    case 1: return launch_gemm_epi<CG, 1>(h, tA, tB, tSA, tSB, tC, kp, stream);
+    case 2: return launch_gemm_epi<CG, 2>(h, tA, tB, tSA, tSB, tC, kp, stream);
+    case 3: return launch_gemm_epi<CG, 3>(h, tA, tB, tSA, tSB, tC, kp, stream);
+    case 4: return launch_gemm_epi<CG, 4>(h, tA, tB, tSA, tSB, tC, kp, stream);
+    case 5: return launch_gemm_epi<CG, 5>(h, tA, tB, tSA, tSB, tC, kp, stream);
+    case 6: return launch_gemm_epi<CG, 6>(h, tA, tB, tSA, tSB, tC, kp, stream);
+    default: return launch_gemm_epi<CG, 7>(h, tA, tB, tSA, tSB, tC, kp, stream);
+  }
+}
+
 int launch_blocks(int64_t work, int per_block) {
   int64_t b = cdiv(work, per_block);
   if (b < 1) b = 1;
@@ -226,8 +247,10 @@ int build_plan(mxgemm_ctx *h, Plan *pl, int64_t M, int64_t N, int64_t K, const v
   const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
   if (encode_2d(h, &pl->tA, u8, A, K, M, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
       encode_2d(h, &pl->tB, u8, bsrc, N, K, bpitch, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      encode_2d(h, &pl->tSA, u8, sfa, 16, a_chunks * 32, 16, 16, 32, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-      encode_2d(h, &pl->tSB, u8, sfb, 16, b_chunks * 32, 16, 16, 64, CU_TENSOR_MAP_SWIZZLE_NONE))
+      // scale chunks are contiguous 512-byte blocks; fetched as rows of 128
+      // bytes (4 rows per chunk) so each chunk is a handful of TMA requests
+      encode_2d(h, &pl->tSA, u8, sfa, 128, a_chunks * 4, 128, 128, 4, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+      encode_2d(h, &pl->tSB, u8, sfb, 128, b_chunks * 4, 128, 128, 8, CU_TENSOR_MAP_SWIZZLE_NONE))
     return MXGEMM_ERR_CUDA;
   // C: stored through TMA (64-byte-wide boxes, 32 rows) when its row pitch
   // allows it; otherwise the kernel stores directly and tC is unused.
@@ -388,7 +411,9 @@ int mxgemm_run(mxgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A
   // workspace size depends only on the shape and mode
   int CG = 1;
   if (h->mode == 2) CG = 2;
-  // mode 0 (automatic) currently selects the single-CTA tile
+  // automatic: the CTA pair halves the B traffic and TMA requests per SM;
+  // measured faster once K is long enough to amortise its per-tile cost
+  else if (h->mode == 0 && M > 128 && K >= 6144) CG = 2;
   const int64_t m_tiles = cdiv(M, 128 * CG);
   const int64_t n_tiles = cdiv(N, 256);
   const int64_t k_steps = cdiv(K, 128);
@@ -508,7 +533,7 @@ struct NoAllocDevice {
   uint8_t *scratch = nullptr;  // this device's address of g_noalloc_scratch
   int *status = nullptr;       // this device's address of g_noalloc_status
   int sm_count = 0;
-  bool attr_set[3] = {false, false, false};
+  bool attr_set[3][8] = {};
 };
 
 constexpr int kNoAllocMaxDevices = 64;
@@ -624,7 +649,8 @@ extern "C" int mxgemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A
   ctx.encode = g_noalloc_encode;
   {
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    for (int i = 0; i < 3; ++i) ctx.attr_set[i] = nd->attr_set[i];
+    for (int i = 0; i < 3; ++i)
+      for (int j = 0; j < 8; ++j) ctx.attr_set[i][j] = nd->attr_set[i][j];
   }
   Plan plan;
   st = build_plan(&ctx, &plan, M, N, K, A, A_scale, B, B_scale, C, use_acc, out_dtype, CG, m_tiles,
@@ -644,7 +670,8 @@ extern "C" int mxgemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A
   st = launch_gemm<1>(&ctx, plan.tA, plan.tB, plan.tSA, plan.tSB, plan.tC, plan.kp, stream);
   {
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
-    for (int i = 0; i < 3; ++i) nd->attr_set[i] = nd->attr_set[i] || ctx.attr_set[i];
+    for (int i = 0; i < 3; ++i)
+      for (int j = 0; j < 8; ++j) nd->attr_set[i][j] = nd->attr_set[i][j] || ctx.attr_set[i][j];
   }
   return st;
 }

@@ -148,13 +148,23 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const 
   }
 }
 
-template <int CG>
+// Epilogue variants are compile-time: each instantiation carries only the
+// store path it uses (a smaller footprint keeps the MMA issue loop's
+// instructions resident).
+constexpr int kEpiBF16 = 1;    // BF16 output (else FP32)
+constexpr int kEpiAcc = 2;     // use_acc: C_in is read and added
+constexpr int kEpiTma = 4;     // C's rows are 16-byte aligned: TMA stores
+
+template <int CG, int EPI>
 __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
     mxgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const __grid_constant__ CUtensorMap tmSFA,
                   const __grid_constant__ CUtensorMap tmSFB, const __grid_constant__ CUtensorMap tmC,
                   const KParams p) {
   using C = Cfg<CG>;
+  constexpr bool kBF16 = (EPI & kEpiBF16) != 0;
+  constexpr bool kAcc = (EPI & kEpiAcc) != 0;
+  constexpr bool kTma = (EPI & kEpiTma) != 0;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -188,7 +198,7 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
     tma_prefetch_desc(&tmB);
     tma_prefetch_desc(&tmSFA);
     tma_prefetch_desc(&tmSFB);
-    if (p.tma_store) tma_prefetch_desc(&tmC);
+    if (kTma) tma_prefetch_desc(&tmC);
   }
   if (warp == 1) {
     tmem_alloc<CG>(smem_u32(tmem_slot), C::TM_COLS);
@@ -204,6 +214,11 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
   griddep_wait();
 
   const WaitCtl wc{p.status, abort_flag, p.timeout_ns};
+  // Barriers completed by TMA byte counts or tcgen05.commit arrivals are
+  // observed with CTA-scope acquire; only acc_empty, which the peer CTA's
+  // epilogue warps release with cluster-scope arrives, is waited on with
+  // cluster scope (a cluster-scope wait on every K step cost ~40% of the
+  // pair's MMA rate).
   constexpr bool CL = (CG == 2);
   const int first_tile = blockIdx.x / CG;
   const int tile_stride = gridDim.x / CG;
@@ -227,7 +242,7 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
 #pragma unroll
         for (int st = 0; st < C::STAGES; ++st) {
           if (ok) {
-            if (!wait_phase<CL>(bar_empty + 8 * st, phase ^ 1u, wc, 0x01 | (st << 8))) {
+            if (!wait_phase<false>(bar_empty + 8 * st, phase ^ 1u, wc, 0x01 | (st << 8))) {
               ok = false;
             } else {
               const uint32_t fb = bar_full + 8 * st;
@@ -244,15 +259,15 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
                 tma_load_2d(sA, &tmA, k0, row0, fb);
                 tma_load_2d(sB, &tmB, col0, k0, fb);
                 tma_load_2d(sB + 16384, &tmB, col0 + 128, k0, fb);
-                tma_load_2d(sSA, &tmSFA, 0, (mblk * p.k_steps + ks) * 32, fb);
-                tma_load_2d(sSB, &tmSFB, 0, (nt * p.k_steps + ks) * 64, fb);
+                tma_load_2d(sSA, &tmSFA, 0, (mblk * p.k_steps + ks) * 4, fb);
+                tma_load_2d(sSB, &tmSFB, 0, (nt * p.k_steps + ks) * 8, fb);
               } else {
                 if (rank == 0) mbar_arrive_expect_tx(fb, C::STAGE_TX);
                 const uint32_t fbl = mapa_shared(fb, 0);  // leader's barrier
                 tma_load_2d_pair(sA, &tmA, k0, row0, fbl);
                 tma_load_2d_pair(sB, &tmB, col0 + 128 * (int)rank, k0, fbl);
-                tma_load_2d_pair(sSA, &tmSFA, 0, (mblk * p.k_steps + ks) * 32, fbl);
-                tma_load_2d_pair(sSB, &tmSFB, 0, (nt * p.k_steps + ks) * 64, fbl);
+                tma_load_2d_pair(sSA, &tmSFA, 0, (mblk * p.k_steps + ks) * 4, fbl);
+                tma_load_2d_pair(sSB, &tmSFB, 0, (nt * p.k_steps + ks) * 8, fbl);
               }
               nst = (st + 1 == C::STAGES) ? 0 : st + 1;
               nph = (st + 1 == C::STAGES) ? (phase ^ 1u) : phase;
@@ -270,7 +285,7 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
       // Drain: every stage's last fill has been consumed (its MMA commit has
       // arrived) before this CTA may finish.
       for (int i = 0; i < C::STAGES; ++i) {
-        if (!wait_phase<CL>(bar_empty + 8 * nst, nph ^ 1u, wc, 0x11 | (nst << 8))) break;
+        if (!wait_phase<false>(bar_empty + 8 * nst, nph ^ 1u, wc, 0x11 | (nst << 8))) break;
         if (++nst == C::STAGES) {
           nst = 0;
           nph ^= 1u;
@@ -279,6 +294,11 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
+    // The tensor pipe does not run ahead of this thread: every instruction
+    // between two MMAs adds to the K step's time.  So the loop is lean, and
+    // the next stage's full barrier is probed (non-blocking) right after
+    // the current stage's first MMA, hiding the probe's latency behind the
+    // other three.
     if (lane == 0 && rank == 0) {
       uint32_t phase = 0, acc_phase = 0;
       int t = first_tile, ks = 0;
@@ -286,53 +306,55 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
       if (ok) {
         ok = wait_phase<CL>(bar_acc_empty, acc_phase ^ 1u, wc, 0x02 | ((t & 0xFFFF) << 16));
         tc_fence_after();
+        if (ok) ok = wait_phase<false>(bar_full, 0, wc, 0x03);
       }
       while (ok) {
 #pragma unroll
         for (int st = 0; st < C::STAGES; ++st) {
           if (ok) {
-            if (!wait_phase<CL>(bar_full + 8 * st, phase, wc, 0x03 | (st << 8))) {
-              ok = false;
-            } else {
-              const uint32_t sA = base + C::OFF_A + st * C::A_BYTES;
-              const uint32_t sB = base + C::OFF_B + st * C::B_BYTES;
-              const uint32_t sSA = base + C::OFF_SFA + st * C::SFA_BYTES;
-              const uint32_t sSB = base + C::OFF_SFB + st * C::SFB_BYTES;
-              const uint32_t tSA = tmem + C::TM_SFA + 4 * st;
-              const uint32_t tSB = tmem + C::TM_SFB + 8 * st;
-              // scale chunks: 32 rows x 16 bytes each, no swizzle, 8-row groups 128 B apart
-              tmem_cp_32x128b_x4<CG>(tSA, smem_desc(sSA, 0, 128, 0));
-              tmem_cp_32x128b_x4<CG>(tSB, smem_desc(sSB, 0, 128, 0));
-              tmem_cp_32x128b_x4<CG>(tSB + 4, smem_desc(sSB + 512, 0, 128, 0));
-              const uint32_t acc0 = ks != 0;
+            // stage st is full
+            const uint32_t sA = base + C::OFF_A + st * C::A_BYTES;
+            const uint32_t sB = base + C::OFF_B + st * C::B_BYTES;
+            const uint32_t sSA = base + C::OFF_SFA + st * C::SFA_BYTES;
+            const uint32_t sSB = base + C::OFF_SFB + st * C::SFB_BYTES;
+            const uint32_t tSA = tmem + C::TM_SFA + 4 * st;
+            const uint32_t tSB = tmem + C::TM_SFB + 8 * st;
+            // scale chunks: 32 rows x 16 bytes each, no swizzle, 8-row groups 128 B apart
+            tmem_cp_32x128b_x4<CG>(tSA, smem_desc(sSA, 0, 128, 0));
+            tmem_cp_32x128b_x4<CG>(tSB, smem_desc(sSB, 0, 128, 0));
+            tmem_cp_32x128b_x4<CG>(tSB + 4, smem_desc(sSB + 512, 0, 128, 0));
+            // A: K-major, 128-byte swizzle, 8-row groups 1024 B apart; 32 B per K=32.
+            // B: N-major, 128-byte swizzle; 128-column chunks 16 KB apart,
+            // 8-row K groups 1024 B apart; 32 rows (4 KB) per K=32.
+            mma_mxf8<CG>(tmem + C::TM_ACC, smem_desc(sA, 0, 1024, 2), smem_desc(sB, 16384, 1024, 2),
+                         idesc_mxf8(128 * CG, 256, 0, 0), tSA, tSB, ks != 0);
+            const int nst = (st + 1 == C::STAGES) ? 0 : st + 1;
+            const uint32_t nph = (st + 1 == C::STAGES) ? (phase ^ 1u) : phase;
+            const uint32_t next_ready = mbar_test_wait(bar_full + 8 * nst, nph);
 #pragma unroll
-              for (int k = 0; k < 4; ++k) {
-                // A: K-major, 128-byte swizzle, 8-row groups 1024 B apart; 32 B per K=32
-                const uint64_t ad = smem_desc(sA + 32 * k, 0, 1024, 2);
-                // B: N-major, 128-byte swizzle; 128-column chunks 16 KB apart,
-                // 8-row K groups 1024 B apart; 32 rows (4 KB) per K=32
-                const uint64_t bd = smem_desc(sB + 4096 * k, 16384, 1024, 2);
-                mma_mxf8<CG>(tmem + C::TM_ACC, ad, bd, idesc_mxf8(128 * CG, 256, k, k), tSA, tSB,
-                             acc0 | (k != 0));
-              }
-              if constexpr (CG == 1) tc_commit(bar_empty + 8 * st);
-              else tc_commit_pair(bar_empty + 8 * st, 0x3);
-              if (++ks == p.k_steps) {
-                ks = 0;
-                if constexpr (CG == 1) tc_commit(bar_acc_full);
-                else tc_commit_pair(bar_acc_full, 0x3);
-                acc_phase ^= 1u;
-                t += tile_stride;
-                if (t >= p.num_tiles) {
-                  ok = false;
-                } else if (!wait_phase<CL>(bar_acc_empty, acc_phase ^ 1u, wc,
-                                           0x02 | ((t & 0xFFFF) << 16))) {
-                  ok = false;
-                } else {
-                  tc_fence_after();
-                }
+            for (int k = 1; k < 4; ++k)
+              mma_mxf8<CG>(tmem + C::TM_ACC, smem_desc(sA + 32 * k, 0, 1024, 2),
+                           smem_desc(sB + 4096 * k, 16384, 1024, 2),
+                           idesc_mxf8(128 * CG, 256, k, k), tSA, tSB, 1u);
+            if constexpr (CG == 1) tc_commit(bar_empty + 8 * st);
+            else tc_commit_pair(bar_empty + 8 * st, 0x3);
+            if (++ks == p.k_steps) {
+              ks = 0;
+              if constexpr (CG == 1) tc_commit(bar_acc_full);
+              else tc_commit_pair(bar_acc_full, 0x3);
+              acc_phase ^= 1u;
+              t += tile_stride;
+              if (t >= p.num_tiles) {
+                ok = false;
+              } else if (!wait_phase<CL>(bar_acc_empty, acc_phase ^ 1u, wc,
+                                         0x02 | ((t & 0xFFFF) << 16))) {
+                ok = false;
+              } else {
+                tc_fence_after();
               }
             }
+            if (ok && !next_ready)
+              ok = wait_phase<false>(bar_full + 8 * nst, nph, wc, 0x03 | (nst << 8));
           }
         }
         if (ok) phase ^= 1u;
@@ -354,15 +376,15 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
     for (int t = first_tile; t < p.num_tiles; t += tile_stride) {
       int mt, nt;
       tile_coords(t, p.m_tiles, p.n_tiles, mt, nt);
-      if (p.use_acc && p.tma_store && lane == 0) {
+      if (kAcc && kTma && lane == 0) {
         // pull this warp's part of C_in into L2 while the tile's MMAs run
         const int r0 = mt * (128 * CG) + 128 * (int)rank + 32 * q;
-        const int cw = p.out_bf16 ? 32 : 16;
+        const int cw = kBF16 ? 32 : 16;
         for (int c0 = nt * 256 + 128 * h; c0 < nt * 256 + 128 * h + 128 && c0 < p.N && r0 < p.M; c0 += cw)
           tma_prefetch_l2_2d(&tmC, c0, r0);
       }
       int ok = 1;
-      if (lane == 0) ok = wait_phase<CL>(bar_acc_full, acc_phase, wc, 0x05 | ((t & 0xFFFF) << 16));
+      if (lane == 0) ok = wait_phase<false>(bar_acc_full, acc_phase, wc, 0x05 | ((t & 0xFFFF) << 16));
       ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
       if (!ok) break;
       tc_fence_after();
@@ -384,9 +406,9 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
       const int row0w = mt * (128 * CG) + 128 * (int)rank + 32 * q;  // this warp's first row
       const int row = row0w + lane;
       const int colb = nt * 256 + 128 * h;
-      if (p.use_acc && row < p.M) {
+      if (kAcc && row < p.M) {
         // C_in: this lane's row, 128 columns (the prefetch below put them in L2)
-        if (!p.out_bf16) {
+        if constexpr (!kBF16) {
           const float *cp = reinterpret_cast<const float *>(p.C) + static_cast<int64_t>(row) * p.N + colb;
 #pragma unroll
           for (int c = 0; c < 128; c += 4) {
@@ -430,7 +452,7 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
         }
       }
 
-      if (p.tma_store) {
+      if constexpr (kTma) {
         // 64-byte-wide column chunks through this warp's staging buffer: lane
         // l writes row l (64-byte swizzle: 16-byte unit u of row r sits at
         // u ^ ((r >> 1) & 3)), then one lane issues the TMA store, which
@@ -442,13 +464,13 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
         if (row0w < p.M) {
 #pragma unroll
           for (int ch = 0; ch < CHUNKS; ++ch) {
-            const int ccols = p.out_bf16 ? 32 : 16;
-            if (p.out_bf16 && ch >= 4) break;
+            const int ccols = kBF16 ? 32 : 16;
+            if (kBF16 && ch >= 4) break;
             const int c0 = colb + ch * ccols;
             if (c0 >= p.N) break;
             if (lane == 0) bulk_wait_read_all();
             __syncwarp();
-            if (!p.out_bf16) {
+            if constexpr (!kBF16) {
 #pragma unroll
               for (int u = 0; u < 4; ++u) {
                 const int c = ch * 16 + 4 * u;
@@ -479,7 +501,7 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
         }
       } else if (row < p.M) {
         // C rows not 16-byte aligned: direct stores
-        if (!p.out_bf16) {
+        if constexpr (!kBF16) {
           float *cp = reinterpret_cast<float *>(p.C) + static_cast<int64_t>(row) * p.N + colb;
 #pragma unroll
           for (int c = 0; c < 128; ++c)
@@ -503,85 +525,6 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
   if constexpr (CG == 2) cluster_sync(); else __syncthreads();
   tc_fence_after();
   if (warp == 1) tmem_dealloc<CG>(tmem, C::TM_COLS);
-}
-
-// ---------------------------------------------------------------- prepasses
-
-// Scale repack: row-major scales S[rows][kb_count] -> 512-byte chunks.  Chunk
-// g = (tile * k_steps + ks) * atoms + a covers rows (tile*atoms + a)*128 + r,
-// r in [0,128), and K-blocks ks*4 + j, j in [0,4); its byte
-// (r % 32) * 16 + (r / 32) * 4 + j holds that scale (127 = 1.0 where the row
-// or K-block is out of range).  This is the 32-row x 16-byte source shape of
-// tcgen05.cp .32x128b.warpx4, which replicates it into the four TMEM lane
-// quarters: TMEM column c+(r/32), lane (r%32) of every quarter, byte j.
-//
-// One launch repacks both operands.  A CTA takes 128 rows x 64 K-blocks of
-// one operand: coalesced byte reads of the rows into shared memory, then
-// coalesced 4-byte writes of the 16 chunks they form.
-struct RepackArgs {
-  const uint8_t *S;   // scales, rows x kb_count
-  uint32_t *out;      // chunks
-  int64_t rows;
-  int kb_count;
-  int k_steps;
-  int atoms;          // 128-row blocks per tile of this operand
-  int row_blocks;     // 128-row blocks to produce (tiles * atoms)
-  int kgroups;        // ceil(k_steps / 16)
-};
-
-constexpr int kRepackThreads = 512;
-
-__global__ void __launch_bounds__(kRepackThreads)
-    repack_scales_kernel(RepackArgs a0, RepackArgs a1, int blocks0) {
-  __shared__ uint32_t tile[128 * 16];  // 128 rows x 64 bytes
-  const bool second = static_cast<int>(blockIdx.x) >= blocks0;
-  const RepackArgs a = second ? a1 : a0;
-  const int b = second ? static_cast<int>(blockIdx.x) - blocks0 : static_cast<int>(blockIdx.x);
-  griddep_launch_dependents();
-  const int rb = b / a.kgroups;          // 128-row block
-  const int kg = b - rb * a.kgroups;     // group of 16 K steps
-  const int64_t row0 = static_cast<int64_t>(rb) * 128;
-  const int kb0 = kg * 64;
-  uint8_t *t8 = reinterpret_cast<uint8_t *>(tile);
-  for (int i = threadIdx.x; i < 128 * 64; i += kRepackThreads) {
-    const int r = i >> 6, c = i & 63;
-    const int64_t row = row0 + r;
-    const int kb = kb0 + c;
-    t8[i] = (row < a.rows && kb < a.kb_count) ? a.S[row * a.kb_count + kb] : static_cast<uint8_t>(127);
-  }
-  __syncthreads();
-  const int tile_idx = rb / a.atoms, at = rb - tile_idx * a.atoms;
-  const int nks = min(16, a.k_steps - kg * 16);
-  for (int i = threadIdx.x; i < nks * 128; i += kRepackThreads) {
-    const int ksl = i >> 7, w = i & 127;
-    const int r = (w & 3) * 32 + (w >> 2);
-    const int ks = kg * 16 + ksl;
-    const int64_t g = (static_cast<int64_t>(tile_idx) * a.k_steps + ks) * a.atoms + at;
-    a.out[g * 128 + w] = tile[r * 16 + ksl];
-  }
-}
-
-// Copy B [K][N] into [K][Npad] (Npad a multiple of 16) so that its rows meet
-// the 16-byte stride rule of tensor-map loads; the pad columns are zero.
-__global__ void pad_rows_kernel(const uint8_t *__restrict__ B, int64_t rows, int64_t N,
-                                int64_t Npad, uint8_t *__restrict__ out) {
-  const int64_t per_row = Npad / 16;
-  const int64_t total = rows * per_row;
-  griddep_launch_dependents();
-  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
-       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t r = i / per_row;
-    const int64_t c0 = (i - r * per_row) * 16;
-    const uint8_t *src = B + r * N;
-    uint32_t w[4] = {0, 0, 0, 0};
-#pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const int64_t c = c0 + j;
-      const uint32_t b = c < N ? src[c] : 0u;
-      w[j >> 2] |= b << (8 * (j & 3));
-    }
-    *reinterpret_cast<uint4 *>(out + r * Npad + c0) = make_uint4(w[0], w[1], w[2], w[3]);
-  }
 }
 
 }  // namespace mxg

@@ -1,0 +1,105 @@
+// prepass.cuh -- the HBM-bound prepasses that run before the GEMM kernel:
+// the scale repack (row-major E8M0 bytes -> the tcgen05.cp chunk layout) and
+// the B row re-pitch for N % 16 != 0.
+#pragma once
+#include <cstdint>
+
+#include "ptx.cuh"
+
+namespace mxg {
+
+// ---------------------------------------------------------------- prepasses
+
+// Scale repack: row-major scales S[rows][kb_count] -> 512-byte chunks.  Chunk
+// g = (tile * k_steps + ks) * atoms + a covers rows (tile*atoms + a)*128 + r,
+// r in [0,128), and K-blocks ks*4 + j, j in [0,4); its byte
+// (r % 32) * 16 + (r / 32) * 4 + j holds that scale (127 = 1.0 where the row
+// or K-block is out of range).  This is the 32-row x 16-byte source shape of
+// tcgen05.cp .32x128b.warpx4, which replicates it into the four TMEM lane
+// quarters: TMEM column c+(r/32), lane (r%32) of every quarter, byte j.
+//
+// One launch repacks both operands.  A CTA takes 128 rows x 64 K-blocks of
+// one operand: one 16-byte read per thread (all issued before any is used, so
+// the CTA pays DRAM latency once), then coalesced 4-byte writes of the 16
+// chunks they form.
+struct RepackArgs {
+  const uint8_t *S;   // scales, rows x kb_count
+  uint32_t *out;      // chunks
+  int64_t rows;
+  int kb_count;
+  int k_steps;
+  int atoms;          // 128-row blocks per tile of this operand
+  int row_blocks;     // 128-row blocks to produce (tiles * atoms)
+  int kgroups;        // ceil(k_steps / 16)
+};
+
+constexpr int kRepackThreads = 512;
+
+__global__ void __launch_bounds__(kRepackThreads)
+    repack_scales_kernel(RepackArgs a0, RepackArgs a1, int blocks0) {
+  __shared__ __align__(16) uint32_t tile[128 * 16];  // 128 rows x 64 bytes
+  const bool second = static_cast<int>(blockIdx.x) >= blocks0;
+  const RepackArgs a = second ? a1 : a0;
+  const int b = second ? static_cast<int>(blockIdx.x) - blocks0 : static_cast<int>(blockIdx.x);
+  griddep_launch_dependents();
+  const int rb = b / a.kgroups;          // 128-row block
+  const int kg = b - rb * a.kgroups;     // group of 16 K steps
+  const int64_t row0 = static_cast<int64_t>(rb) * 128;
+  const int kb0 = kg * 64;
+  uint8_t *t8 = reinterpret_cast<uint8_t *>(tile);
+  // each thread brings in 16 consecutive bytes of one row (128 rows x 64 bytes)
+  const int r = threadIdx.x >> 2, c0 = (threadIdx.x & 3) * 16;
+  const int64_t row = row0 + r;
+  const int kb = kb0 + c0;
+  uint4 v = make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+  if (row < a.rows) {
+    const uint8_t *src = a.S + row * a.kb_count + kb;
+    if (kb + 16 <= a.kb_count && (reinterpret_cast<uintptr_t>(src) & 15) == 0) {
+      v = *reinterpret_cast<const uint4 *>(src);
+    } else {
+      uint32_t w[4] = {0, 0, 0, 0};
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const uint32_t byte = kb + j < a.kb_count ? src[j] : 127u;
+        w[j >> 2] |= byte << (8 * (j & 3));
+      }
+      v = make_uint4(w[0], w[1], w[2], w[3]);
+    }
+  }
+  *reinterpret_cast<uint4 *>(t8 + r * 64 + c0) = v;
+  __syncthreads();
+  const int tile_idx = rb / a.atoms, at = rb - tile_idx * a.atoms;
+  const int nks = min(16, a.k_steps - kg * 16);
+  for (int i = threadIdx.x; i < nks * 128; i += kRepackThreads) {
+    const int ksl = i >> 7, w = i & 127;
+    const int r = (w & 3) * 32 + (w >> 2);
+    const int ks = kg * 16 + ksl;
+    const int64_t g = (static_cast<int64_t>(tile_idx) * a.k_steps + ks) * a.atoms + at;
+    a.out[g * 128 + w] = tile[r * 16 + ksl];
+  }
+}
+
+// Copy B [K][N] into [K][Npad] (Npad a multiple of 16) so that its rows meet
+// the 16-byte stride rule of tensor-map loads; the pad columns are zero.
+__global__ void pad_rows_kernel(const uint8_t *__restrict__ B, int64_t rows, int64_t N,
+                                int64_t Npad, uint8_t *__restrict__ out) {
+  const int64_t per_row = Npad / 16;
+  const int64_t total = rows * per_row;
+  griddep_launch_dependents();
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    const int64_t r = i / per_row;
+    const int64_t c0 = (i - r * per_row) * 16;
+    const uint8_t *src = B + r * N;
+    uint32_t w[4] = {0, 0, 0, 0};
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const int64_t c = c0 + j;
+      const uint32_t b = c < N ? src[c] : 0u;
+      w[j >> 2] |= b << (8 * (j & 3));
+    }
+    *reinterpret_cast<uint4 *>(out + r * Npad + c0) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+}  // namespace mxg

@@ -66,8 +66,9 @@ typedef enum {
 
 /* Options for mxgemm_set_option. */
 typedef enum {
-  /* Tile mode: 0 = automatic, 1 = one CTA per 128x256 tile, 2 = CTA pair
-   * (cta_group::2) per 256x256 tile.  Default 0. */
+  /* Tile mode: 0 = automatic (CTA pair when M > 128 and K >= 6144, else one
+   * CTA), 1 = one CTA per 128x256 tile, 2 = CTA pair (cta_group::2) per
+   * 256x256 tile.  Default 0. */
   MXGEMM_OPT_MODE = 1,
   /* Device-side wait limit in nanoseconds (default 2e9).  A wait that runs
    * out sets MXGEMM_ERR_TIMEOUT and the kernel drains and returns. */
