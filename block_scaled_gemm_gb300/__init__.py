@@ -23,7 +23,7 @@ from . import _build
 
 __all__ = [
     "OUT_F32", "OUT_BF16", "OPT_MODE", "OPT_WAIT_TIMEOUT_NS", "OPT_TEST_STALL_PRODUCER",
-    "OPT_SCHEDULER", "MxgemmError", "library", "library_path", "mxgemm_create", "mxgemm_run",
+    "OPT_SCHEDULER", "OPT_STREAM_K", "MxgemmError", "library", "library_path", "mxgemm_create", "mxgemm_run",
     "mxgemm_destroy", "mxgemm_set_option", "mxgemm_get_device_status", "mxgemm_status_string",
     "mxgemm_set_profile_events", "mxgemm_get_launch_count", "mxgemm_run_noalloc",
     "EXPORTED_SYMBOLS", "Gemm",
@@ -36,6 +36,7 @@ OPT_MODE = 1
 OPT_WAIT_TIMEOUT_NS = 2
 OPT_TEST_STALL_PRODUCER = 3
 OPT_SCHEDULER = 4
+OPT_STREAM_K = 5
 
 OK = 0
 ERR_INVALID_VALUE = 1

@@ -38,7 +38,7 @@ struct Plan {
   int64_t M = 0, N = 0, K = 0;
   const void *A = nullptr, *As = nullptr, *B = nullptr, *Bs = nullptr;
   void *C = nullptr;
-  int use_acc = 0, out_dtype = 0, mode = 0, stall = 0, sched = 0;
+  int use_acc = 0, out_dtype = 0, mode = 0, stall = 0, sched = 0, sk = 0;
   long long timeout_ns = 0;
   uint8_t *ws = nullptr;
   // value
@@ -49,13 +49,16 @@ struct Plan {
   KParams kp;
   mxg::RepackArgs ra, rb;
   int blocks_a = 0, blocks_b = 0;
+  int units = 0;     // persistent CTAs (pairs) of the GEMM grid
+  int *flags = nullptr;
+  int nflags = 0;
 
   bool matches(int64_t M_, int64_t N_, int64_t K_, const void *A_, const void *As_, const void *B_,
-               const void *Bs_, void *C_, int ua, int od, int md, int sl, int sc, long long to,
-               uint8_t *w) const {
+               const void *Bs_, void *C_, int ua, int od, int md, int sl, int sc, int sk_,
+               long long to, uint8_t *w) const {
     return valid && M == M_ && N == N_ && K == K_ && A == A_ && As == As_ && B == B_ &&
            Bs == Bs_ && C == C_ && use_acc == ua && out_dtype == od && mode == md &&
-           stall == sl && sched == sc && timeout_ns == to && ws == w;
+           stall == sl && sched == sc && sk == sk_ && timeout_ns == to && ws == w;
   }
 };
 
@@ -73,6 +76,7 @@ struct mxgemm_ctx {
   int mode = 0;
   int stall_producer = 0;
   int scheduler = 0;
+  int stream_k = 1;
   bool attr_set[3][8] = {};
   cudaEvent_t prof_before = nullptr;
   cudaEvent_t prof_after = nullptr;
@@ -146,7 +150,7 @@ int ensure_workspace(mxgemm_ctx *h, size_t bytes, cudaStream_t stream) {
 template <int CG, int EPI>
 int launch_gemm_epi(mxgemm_ctx *h, const CUtensorMap &tA, const CUtensorMap &tB,
                     const CUtensorMap &tSA, const CUtensorMap &tSB, const CUtensorMap &tC,
-                    const KParams &kp, cudaStream_t stream) {
+                    const KParams &kp, int units, cudaStream_t stream) {
   using C = Cfg<CG>;
   auto kern = mxg::mxgemm_kernel<CG, EPI>;
   if (!h->attr_set[CG][EPI]) {
@@ -157,8 +161,7 @@ int launch_gemm_epi(mxgemm_ctx *h, const CUtensorMap &tA, const CUtensorMap &tB,
     }
     h->attr_set[CG][EPI] = true;
   }
-  const int units = h->sm_count / CG;
-  const int clusters = kp.num_tiles < units ? kp.num_tiles : units;
+  const int clusters = units;
   cudaLaunchConfig_t cfg;
   std::memset(&cfg, 0, sizeof(cfg));
   cfg.gridDim = dim3(static_cast<unsigned>(clusters * CG), 1, 1);
@@ -201,18 +204,18 @@ int launch_gemm_epi(mxgemm_ctx *h, const CUtensorMap &tA, const CUtensorMap &tB,
 template <int CG>
 int launch_gemm(mxgemm_ctx *h, const CUtensorMap &tA, const CUtensorMap &tB,
                 const CUtensorMap &tSA, const CUtensorMap &tSB, const CUtensorMap &tC,
-                const KParams &kp, cudaStream_t stream) {
+                const KParams &kp, int units, cudaStream_t stream) {
   const int epi = (kp.out_bf16 ? mxg::kEpiBF16 : 0) | (kp.use_acc ? mxg::kEpiAcc : 0) |
                   (kp.tma_store ? mxg::kEpiTma : 0);
   switch (epi) {
-    case 0: return launch_gemm_epi<CG, 0>(h, tA, tB, tSA, tSB, tC, kp, stream);
-    case 1: return launch_gemm_epi<CG, 1>(h, tA, tB, tSA, tSB, tC, kp, stream);
-    case 2: return launch_gemm_epi<CG, 2>(h, tA, tB, tSA, tSB, tC, kp, stream);
-    case 3: return launch_gemm_epi<CG, 3>(h, tA, tB, tSA, tSB, tC, kp, stream);
-    case 4: return launch_gemm_epi<CG, 4>(h, tA, tB, tSA, tSB, tC, kp, stream);
-    case 5: return launch_gemm_epi<CG, 5>(h, tA, tB, tSA, tSB, tC, kp, stream);
-    case 6: return launch_gemm_epi<CG, 6>(h, tA, tB, tSA, tSB, tC, kp, stream);
-    default: return launch_gemm_epi<CG, 7>(h, tA, tB, tSA, tSB, tC, kp, stream);
+    case 0: return launch_gemm_epi<CG, 0>(h, tA, tB, tSA, tSB, tC, kp, units, stream);
+    case 1: return launch_gemm_epi<CG, 1>(h, tA, tB, tSA, tSB, tC, kp, units, stream);
+    case 2: return launch_gemm_epi<CG, 2>(h, tA, tB, tSA, tSB, tC, kp, units, stream);
+    case 3: return launch_gemm_epi<CG, 3>(h, tA, tB, tSA, tSB, tC, kp, units, stream);
+    case 4: return launch_gemm_epi<CG, 4>(h, tA, tB, tSA, tSB, tC, kp, units, stream);
+    case 5: return launch_gemm_epi<CG, 5>(h, tA, tB, tSA, tSB, tC, kp, units, stream);
+    case 6: return launch_gemm_epi<CG, 6>(h, tA, tB, tSA, tSB, tC, kp, units, stream);
+    default: return launch_gemm_epi<CG, 7>(h, tA, tB, tSA, tSB, tC, kp, units, stream);
   }
 }
 
@@ -223,13 +226,65 @@ int launch_blocks(int64_t work, int per_block) {
   return static_cast<int>(b);
 }
 
+// How the GEMM grid covers the tiles: whole tiles in full waves, and a
+// stream-K tail (the leftover tiles' K steps split evenly over the CTAs)
+// when the tiles do not fill the last wave.
+struct Split {
+  int units;           // persistent CTAs (pairs)
+  int dp_tiles;        // tiles computed whole
+  int sk_ctas;         // CTAs sharing the tail
+  long long sk_units;  // K steps in the tail
+};
+
+Split plan_split(int64_t T, int64_t S, int P, bool allow_stream_k) {
+  Split r;
+  r.units = static_cast<int>(T < P ? T : P);
+  r.dp_tiles = static_cast<int>(T);
+  r.sk_ctas = 0;
+  r.sk_units = 0;
+  // Measured on GB300: the owners' gather of FP32 partials is slow enough
+  // that the split pays off only with long K (64+ steps) after 1 to 8 full
+  // waves, and not when the last wave is nearly full; in particular not when
+  // every tile would be split (fewer tiles than CTAs).
+  if (!allow_stream_k || T == 0 || S < 64) return r;
+  const int64_t W = T / P, R = T % P;
+  if (W < 1 || W > 8 || R == 0 || R * 100 >= static_cast<int64_t>(P) * 85) return r;
+  const int64_t tail = R * S;
+  int64_t ctas = tail / 4;  // at least 4 K steps per CTA
+  if (ctas > P) ctas = P;
+  if (ctas <= R) return r;  // no CTA would get less than a whole tile
+  r.units = P;
+  r.dp_tiles = static_cast<int>(W * P);
+  r.sk_ctas = static_cast<int>(ctas);
+  r.sk_units = tail;
+  return r;
+}
+
+// Workspace layout of a run: repacked scales, re-pitched B, stream-K
+// partials and flags.
+struct Sizes {
+  size_t off_sfb, off_b, off_part, off_flags, total;
+};
+
+Sizes plan_sizes(int64_t a_chunks, int64_t b_chunks, bool pad_b, int64_t K, int64_t npad,
+                 const Split &sp, int CG) {
+  Sizes z;
+  z.off_sfb = round_up(static_cast<size_t>(a_chunks) * 512, 1024);
+  z.off_b = round_up(z.off_sfb + static_cast<size_t>(b_chunks) * 512, 1024);
+  z.off_part = round_up(z.off_b + (pad_b ? static_cast<size_t>(K) * npad : 0), 1024);
+  z.off_flags = z.off_part + static_cast<size_t>(sp.sk_ctas) * CG * 128 * 256 * sizeof(float);
+  z.total = round_up(z.off_flags + static_cast<size_t>(sp.sk_ctas) * CG * sizeof(int) + 16, 1024);
+  return z;
+}
+
 // Validate-once work of a run: prepass arguments, tensor maps and kernel
 // parameters, stored in `pl` under the run's key.
 int build_plan(mxgemm_ctx *h, Plan *pl, int64_t M, int64_t N, int64_t K, const void *A,
                const void *A_scale, const void *B, const void *B_scale, void *C, int use_acc,
                int out_dtype, int CG, int64_t m_tiles, int64_t n_tiles, int64_t k_steps,
                int64_t num_tiles, int64_t a_chunks, int64_t b_chunks, bool pad_b, int64_t npad,
-               size_t off_sfb, size_t off_b) {
+               const Split &sp, const Sizes &z) {
+  const size_t off_sfb = z.off_sfb, off_b = z.off_b;
   const size_t esz = out_dtype == MXGEMM_OUT_F32 ? 4 : 2;
   const int64_t kb = K / 32;
   uint8_t *sfa = h->ws.ptr;
@@ -281,13 +336,22 @@ int build_plan(mxgemm_ctx *h, Plan *pl, int64_t M, int64_t N, int64_t K, const v
   kp.timeout_ns = static_cast<unsigned long long>(h->timeout_ns);
   kp.stall_producer = h->stall_producer;
   kp.use_clc = h->scheduler;
+  kp.dp_tiles = sp.dp_tiles;
+  kp.sk_ctas = sp.sk_ctas;
+  kp.sk_units = sp.sk_units;
+  kp.partials = reinterpret_cast<float *>(h->ws.ptr + z.off_part);
+  kp.flags = reinterpret_cast<int *>(h->ws.ptr + z.off_flags);
+  pl->units = sp.units;
+  pl->flags = kp.flags;
+  pl->nflags = sp.sk_ctas * CG;
   pl->CG = CG;
   pl->pad_b = pad_b;
   pl->npad = npad;
   pl->M = M; pl->N = N; pl->K = K;
   pl->A = A; pl->As = A_scale; pl->B = B; pl->Bs = B_scale; pl->C = C;
   pl->use_acc = use_acc; pl->out_dtype = out_dtype; pl->mode = h->mode;
-  pl->stall = h->stall_producer; pl->sched = h->scheduler; pl->timeout_ns = h->timeout_ns;
+  pl->stall = h->stall_producer; pl->sched = h->scheduler; pl->sk = h->stream_k;
+  pl->timeout_ns = h->timeout_ns;
   pl->ws = h->ws.ptr;
   pl->valid = true;
   return MXGEMM_OK;
@@ -375,6 +439,10 @@ int mxgemm_set_option(mxgemm_handle_t h, int option, int64_t value) {
       if (value < 0 || value > 1) return MXGEMM_ERR_INVALID_VALUE;
       h->scheduler = static_cast<int>(value);
       return MXGEMM_OK;
+    case MXGEMM_OPT_STREAM_K:
+      if (value < 0 || value > 1) return MXGEMM_ERR_INVALID_VALUE;
+      h->stream_k = static_cast<int>(value);
+      return MXGEMM_OK;
     default:
       return MXGEMM_ERR_INVALID_VALUE;
   }
@@ -423,14 +491,15 @@ int mxgemm_run(mxgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A
   const int64_t b_chunks = n_tiles * k_steps * 2;   // 2 per 256 columns
   const bool pad_b = (N % 16) != 0;
   const int64_t npad = round_up(static_cast<size_t>(N), 16);
-  const size_t off_sfb = round_up(static_cast<size_t>(a_chunks) * 512, 1024);
-  const size_t off_b = round_up(off_sfb + static_cast<size_t>(b_chunks) * 512, 1024);
-  const size_t ws_bytes = off_b + (pad_b ? static_cast<size_t>(K) * npad : 0);
+  const Split sp = plan_split(num_tiles, k_steps, h->sm_count / CG, h->stream_k != 0);
+  const Sizes z = plan_sizes(a_chunks, b_chunks, pad_b, K, npad, sp, CG);
+  const size_t off_b = z.off_b;
+  const size_t ws_bytes = z.total;
 
   Plan *plan = nullptr;
   for (Plan &pl : h->plans)
     if (pl.matches(M, N, K, A, A_scale, B, B_scale, C, use_acc, out_dtype, h->mode,
-                   h->stall_producer, h->scheduler, h->timeout_ns, h->ws.ptr) &&
+                   h->stall_producer, h->scheduler, h->stream_k, h->timeout_ns, h->ws.ptr) &&
         h->ws.bytes >= ws_bytes) {
       plan = &pl;
       break;
@@ -445,7 +514,7 @@ int mxgemm_run(mxgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A
     h->next_plan = (h->next_plan + 1) % kPlanCache;
     plan->valid = false;
     st = build_plan(h, plan, M, N, K, A, A_scale, B, B_scale, C, use_acc, out_dtype, CG, m_tiles,
-                    n_tiles, k_steps, num_tiles, a_chunks, b_chunks, pad_b, npad, off_sfb, off_b);
+                    n_tiles, k_steps, num_tiles, a_chunks, b_chunks, pad_b, npad, sp, z);
     if (st != MXGEMM_OK) return st;
   }
 
@@ -456,13 +525,13 @@ int mxgemm_run(mxgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A
     ++h->launches;
   }
   mxg::repack_scales_kernel<<<plan->blocks_a + plan->blocks_b, mxg::kRepackThreads, 0, stream>>>(
-      plan->ra, plan->rb, plan->blocks_a);
+      plan->ra, plan->rb, plan->blocks_a, plan->flags, plan->nflags);
   h->launches += 1;
   if (cudaGetLastError() != cudaSuccess) return MXGEMM_ERR_CUDA;
   return plan->CG == 2 ? launch_gemm<2>(h, plan->tA, plan->tB, plan->tSA, plan->tSB, plan->tC,
-                                        plan->kp, stream)
+                                        plan->kp, plan->units, stream)
                        : launch_gemm<1>(h, plan->tA, plan->tB, plan->tSA, plan->tSB, plan->tC,
-                                        plan->kp, stream);
+                                        plan->kp, plan->units, stream);
 }
 
 int mxgemm_get_device_status(mxgemm_handle_t h, mxgemm_stream_t stream_, int *status_out,
@@ -630,9 +699,11 @@ extern "C" int mxgemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A
   const int64_t b_chunks = n_tiles * k_steps * 2;
   const bool pad_b = (N % 16) != 0;
   const int64_t npad = round_up(static_cast<size_t>(N), 16);
-  const size_t off_sfb = round_up(static_cast<size_t>(a_chunks) * 512, 1024);
-  const size_t off_b = round_up(off_sfb + static_cast<size_t>(b_chunks) * 512, 1024);
-  const size_t ws_bytes = off_b + (pad_b ? static_cast<size_t>(K) * npad : 0);
+  // no stream-K split here: the scratch holds only the repacked scales and B
+  const Split sp = plan_split(num_tiles, k_steps, nd->sm_count / CG, false);
+  const Sizes z = plan_sizes(a_chunks, b_chunks, pad_b, K, npad, sp, CG);
+  const size_t off_b = z.off_b;
+  const size_t ws_bytes = z.total;
   if (ws_bytes > kNoAllocScratchBytes) return MXGEMM_ERR_TOO_LARGE;
   if (!on_device(C, dev) || !on_device(A, dev) || !on_device(B, dev) ||
       !on_device(A_scale, dev) || !on_device(B_scale, dev))
@@ -654,7 +725,7 @@ extern "C" int mxgemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A
   }
   Plan plan;
   st = build_plan(&ctx, &plan, M, N, K, A, A_scale, B, B_scale, C, use_acc, out_dtype, CG, m_tiles,
-                  n_tiles, k_steps, num_tiles, a_chunks, b_chunks, pad_b, npad, off_sfb, off_b);
+                  n_tiles, k_steps, num_tiles, a_chunks, b_chunks, pad_b, npad, sp, z);
   if (st != MXGEMM_OK) return st;
   // the status word must start each call at zero
   if (cudaMemsetAsync(nd->status, 0, 2 * sizeof(int), stream) != cudaSuccess) {
@@ -665,9 +736,10 @@ extern "C" int mxgemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A
     mxg::pad_rows_kernel<<<launch_blocks(K * (npad / 16), 256), 256, 0, stream>>>(
         static_cast<const uint8_t *>(B), K, N, npad, nd->scratch + off_b);
   mxg::repack_scales_kernel<<<plan.blocks_a + plan.blocks_b, mxg::kRepackThreads, 0, stream>>>(
-      plan.ra, plan.rb, plan.blocks_a);
+      plan.ra, plan.rb, plan.blocks_a, plan.flags, plan.nflags);
   if (cudaGetLastError() != cudaSuccess) return MXGEMM_ERR_CUDA;
-  st = launch_gemm<1>(&ctx, plan.tA, plan.tB, plan.tSA, plan.tSB, plan.tC, plan.kp, stream);
+  st = launch_gemm<1>(&ctx, plan.tA, plan.tB, plan.tSA, plan.tSB, plan.tC, plan.kp, plan.units,
+                      stream);
   {
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
     for (int i = 0; i < 3; ++i)

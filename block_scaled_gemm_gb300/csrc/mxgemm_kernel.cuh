@@ -91,6 +91,12 @@ struct KParams {
   unsigned long long timeout_ns;
   int stall_producer;
   int use_clc;
+  // stream-K tail (see WorkIter)
+  int dp_tiles;        // tiles [0, dp_tiles) are computed whole, one CTA (pair) each
+  int sk_ctas;         // CTAs (pairs) sharing the K steps of tiles [dp_tiles, num_tiles)
+  long long sk_units;  // (num_tiles - dp_tiles) * k_steps
+  float *partials;     // per CTA: 128 x 256 FP32 partial accumulator
+  int *flags;          // per CTA: epilogue warps that have written its partial
 };
 
 // Instruction descriptor of tcgen05.mma.kind::mxf8f6f4.block_scale:
@@ -119,6 +125,71 @@ __device__ __forceinline__ void tile_coords(int t, int m_tiles, int n_tiles, int
   mt = first + r % gm;
   nt = r / gm;
 }
+
+// Work of one CTA (or CTA pair) u of P.  When the tiles do not divide into
+// whole waves, the tiles after the last full wave (the "tail") are shared
+// stream-K style: their K steps, laid end to end, are cut into sk_ctas equal
+// contiguous ranges, one per CTA.  A range is shorter than one tile, so it
+// touches at most two tiles: the start of one (a partial this CTA writes to
+// its own slot) and the end of another (which this CTA finishes: it adds the
+// other contributors' partials and stores C).  Each CTA does its tail work
+// first, partial before finish, and then its whole tiles dp_tiles-ward
+// (u, u+P, ...): every partial is written before anyone waits for it, and an
+// owner's wait for partials overlaps the MMAs of its first whole tile.
+constexpr int kFull = 0;     // whole K range: store C
+constexpr int kPartial = 1;  // first part of a tile's K range: write a partial
+constexpr int kOwner = 2;    // last part: add the earlier parts' partials, store C
+
+struct WorkItem {
+  int tile;
+  int kb, ke;         // K steps [kb, ke)
+  int kind;
+  int first_contrib;  // kOwner: CTAs first_contrib .. u-1 hold this tile's partials
+};
+
+struct WorkIter {
+  int u, P, dp_tiles, k_steps, sk_ctas;
+  long long sk_units;
+  int i = 0;         // next whole tile: u + i * P
+  int tail_pos = 0;  // next tail segment (0: later tile, 1: earlier tile, 2: done)
+
+  __device__ WorkIter(const KParams &p, int u_, int P_)
+      : u(u_), P(P_), dp_tiles(p.dp_tiles), k_steps(p.k_steps), sk_ctas(p.sk_ctas),
+        sk_units(p.sk_units) {
+    if (sk_units == 0 || u >= sk_ctas) tail_pos = 2;
+  }
+
+  __device__ bool next(WorkItem &w) {
+    while (tail_pos < 2) {
+      const long long S = k_steps;
+      const long long beg = static_cast<long long>(u) * sk_units / sk_ctas;
+      const long long end = static_cast<long long>(u + 1) * sk_units / sk_ctas;
+      const long long j0 = beg / S, j1 = (end - 1) / S;
+      const int pos = tail_pos++;
+      if (beg >= end || (pos == 1 && j0 == j1)) continue;
+      const long long j = pos == 0 ? j1 : j0;
+      const long long sb = beg > j * S ? beg : j * S;
+      const long long se = end < (j + 1) * S ? end : (j + 1) * S;
+      w.tile = dp_tiles + static_cast<int>(j);
+      w.kb = static_cast<int>(sb - j * S);
+      w.ke = static_cast<int>(se - j * S);
+      const bool first = w.kb == 0, last = w.ke == k_steps;
+      w.kind = last ? (first ? kFull : kOwner) : kPartial;
+      // the CTA whose range holds the tile's first K step
+      w.first_contrib = static_cast<int>(((j * S + 1) * sk_ctas - 1) / sk_units);
+      return true;
+    }
+    const int t = u + i * P;
+    if (t >= dp_tiles) return false;
+    ++i;
+    w.tile = t;
+    w.kb = 0;
+    w.ke = k_steps;
+    w.kind = kFull;
+    w.first_contrib = u;
+    return true;
+  }
+};
 
 struct WaitCtl {
   int *status;
@@ -154,6 +225,27 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const 
 constexpr int kEpiBF16 = 1;    // BF16 output (else FP32)
 constexpr int kEpiAcc = 2;     // use_acc: C_in is read and added
 constexpr int kEpiTma = 4;     // C's rows are 16-byte aligned: TMA stores
+
+// Bounded wait until *flag (written by other CTAs with release atomics)
+// reaches `target`.
+__device__ __forceinline__ bool wait_flag(const int *flag, int target, const WaitCtl &w,
+                                          int detail) {
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0;; ++it) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+    if (v >= target) return true;
+    if ((it & 15u) == 15u) {
+      if (*w.abort_flag) return false;
+      if (globaltimer_ns() - t0 > w.timeout_ns) {
+        if (atomicCAS(w.status, 0, kStatusTimeout) == 0) atomicExch(w.status + 1, detail);
+        *w.abort_flag = 1;
+        return false;
+      }
+    }
+    __nanosleep(64);
+  }
+}
 
 template <int CG, int EPI>
 __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
@@ -220,8 +312,8 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
   // cluster scope (a cluster-scope wait on every K step cost ~40% of the
   // pair's MMA rate).
   constexpr bool CL = (CG == 2);
-  const int first_tile = blockIdx.x / CG;
-  const int tile_stride = gridDim.x / CG;
+  const int unit = blockIdx.x / CG;    // this CTA's (pair's) index in the persistent grid
+  const int units = gridDim.x / CG;
 
   // The producer and MMA loops are unrolled over the ring stages: with the
   // stage index a compile-time constant every shared-memory address, TMEM
@@ -234,10 +326,11 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
       uint32_t phase = 0;
       int nst = 0;           // next stage to fill ...
       uint32_t nph = 0;      // ... and the ring phase it belongs to
-      int t = first_tile, ks = 0;
-      bool ok = !p.stall_producer && t < p.num_tiles;
-      int mt = 0, nt = 0;
-      if (ok) tile_coords(t, p.m_tiles, p.n_tiles, mt, nt);
+      WorkIter wi(p, unit, units);
+      WorkItem w;
+      bool ok = !p.stall_producer && wi.next(w);
+      int ks = w.kb, mt = 0, nt = 0;
+      if (ok) tile_coords(w.tile, p.m_tiles, p.n_tiles, mt, nt);
       while (ok) {
 #pragma unroll
         for (int st = 0; st < C::STAGES; ++st) {
@@ -271,11 +364,13 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
               }
               nst = (st + 1 == C::STAGES) ? 0 : st + 1;
               nph = (st + 1 == C::STAGES) ? (phase ^ 1u) : phase;
-              if (++ks == p.k_steps) {
-                ks = 0;
-                t += tile_stride;
-                if (t >= p.num_tiles) ok = false;
-                else tile_coords(t, p.m_tiles, p.n_tiles, mt, nt);
+              if (++ks == w.ke) {
+                if (wi.next(w)) {
+                  ks = w.kb;
+                  tile_coords(w.tile, p.m_tiles, p.n_tiles, mt, nt);
+                } else {
+                  ok = false;
+                }
               }
             }
           }
@@ -294,77 +389,92 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    // The tensor pipe does not run ahead of this thread: every instruction
-    // between two MMAs adds to the K step's time.  So the loop is lean, and
-    // the next stage's full barrier is probed (non-blocking) right after
-    // the current stage's first MMA, hiding the probe's latency behind the
-    // other three.
-    if (lane == 0 && rank == 0) {
+    // The tensor pipe does not run ahead of the issuing thread: every
+    // instruction between two MMAs adds to the K step's time.  The whole warp
+    // runs the loop in lock-step (warp-uniform control flow) and one elected
+    // lane issues; the next stage's full barrier is probed right after the
+    // current stage's first MMA, hiding the probe's latency behind the other
+    // three.
+    if (rank == 0) {
+      const bool leader = elect_one() != 0;
       uint32_t phase = 0, acc_phase = 0;
-      int t = first_tile, ks = 0;
-      bool ok = t < p.num_tiles;
+      WorkIter wi(p, unit, units);
+      WorkItem w;
+      bool ok = wi.next(w);
+      int ks = w.kb;
       if (ok) {
-        ok = wait_phase<CL>(bar_acc_empty, acc_phase ^ 1u, wc, 0x02 | ((t & 0xFFFF) << 16));
+        ok = __all_sync(0xFFFFFFFFu, wait_phase<CL>(bar_acc_empty, acc_phase ^ 1u, wc, 0x02));
         tc_fence_after();
-        if (ok) ok = wait_phase<false>(bar_full, 0, wc, 0x03);
+        if (ok) ok = __all_sync(0xFFFFFFFFu, wait_phase<false>(bar_full, 0, wc, 0x03));
       }
       while (ok) {
 #pragma unroll
         for (int st = 0; st < C::STAGES; ++st) {
           if (ok) {
             // stage st is full
-            const uint32_t sA = base + C::OFF_A + st * C::A_BYTES;
-            const uint32_t sB = base + C::OFF_B + st * C::B_BYTES;
-            const uint32_t sSA = base + C::OFF_SFA + st * C::SFA_BYTES;
-            const uint32_t sSB = base + C::OFF_SFB + st * C::SFB_BYTES;
-            const uint32_t tSA = tmem + C::TM_SFA + 4 * st;
-            const uint32_t tSB = tmem + C::TM_SFB + 8 * st;
-            // scale chunks: 32 rows x 16 bytes each, no swizzle, 8-row groups 128 B apart
-            tmem_cp_32x128b_x4<CG>(tSA, smem_desc(sSA, 0, 128, 0));
-            tmem_cp_32x128b_x4<CG>(tSB, smem_desc(sSB, 0, 128, 0));
-            tmem_cp_32x128b_x4<CG>(tSB + 4, smem_desc(sSB + 512, 0, 128, 0));
-            // A: K-major, 128-byte swizzle, 8-row groups 1024 B apart; 32 B per K=32.
-            // B: N-major, 128-byte swizzle; 128-column chunks 16 KB apart,
-            // 8-row K groups 1024 B apart; 32 rows (4 KB) per K=32.
-            mma_mxf8<CG>(tmem + C::TM_ACC, smem_desc(sA, 0, 1024, 2), smem_desc(sB, 16384, 1024, 2),
-                         idesc_mxf8(128 * CG, 256, 0, 0), tSA, tSB, ks != 0);
             const int nst = (st + 1 == C::STAGES) ? 0 : st + 1;
             const uint32_t nph = (st + 1 == C::STAGES) ? (phase ^ 1u) : phase;
-            const uint32_t next_ready = mbar_test_wait(bar_full + 8 * nst, nph);
+            uint32_t next_ready = 0;
+            if (leader) {
+              const uint32_t sA = base + C::OFF_A + st * C::A_BYTES;
+              const uint32_t sB = base + C::OFF_B + st * C::B_BYTES;
+              const uint32_t sSA = base + C::OFF_SFA + st * C::SFA_BYTES;
+              const uint32_t sSB = base + C::OFF_SFB + st * C::SFB_BYTES;
+              const uint32_t tSA = tmem + C::TM_SFA + 4 * st;
+              const uint32_t tSB = tmem + C::TM_SFB + 8 * st;
+              // scale chunks: 32 rows x 16 bytes each, no swizzle, 8-row groups 128 B apart
+              tmem_cp_32x128b_x4<CG>(tSA, smem_desc(sSA, 0, 128, 0));
+              tmem_cp_32x128b_x4<CG>(tSB, smem_desc(sSB, 0, 128, 0));
+              tmem_cp_32x128b_x4<CG>(tSB + 4, smem_desc(sSB + 512, 0, 128, 0));
+              // A: K-major, 128-byte swizzle, 8-row groups 1024 B apart; 32 B per K=32.
+              // B: N-major, 128-byte swizzle; 128-column chunks 16 KB apart,
+              // 8-row K groups 1024 B apart; 32 rows (4 KB) per K=32.
+              mma_mxf8<CG>(tmem + C::TM_ACC, smem_desc(sA, 0, 1024, 2), smem_desc(sB, 16384, 1024, 2),
+                           idesc_mxf8(128 * CG, 256, 0, 0), tSA, tSB, ks != w.kb);
+              next_ready = mbar_test_wait(bar_full + 8 * nst, nph);
 #pragma unroll
-            for (int k = 1; k < 4; ++k)
-              mma_mxf8<CG>(tmem + C::TM_ACC, smem_desc(sA + 32 * k, 0, 1024, 2),
-                           smem_desc(sB + 4096 * k, 16384, 1024, 2),
-                           idesc_mxf8(128 * CG, 256, k, k), tSA, tSB, 1u);
-            if constexpr (CG == 1) tc_commit(bar_empty + 8 * st);
-            else tc_commit_pair(bar_empty + 8 * st, 0x3);
-            if (++ks == p.k_steps) {
-              ks = 0;
-              if constexpr (CG == 1) tc_commit(bar_acc_full);
-              else tc_commit_pair(bar_acc_full, 0x3);
+              for (int k = 1; k < 4; ++k)
+                mma_mxf8<CG>(tmem + C::TM_ACC, smem_desc(sA + 32 * k, 0, 1024, 2),
+                             smem_desc(sB + 4096 * k, 16384, 1024, 2),
+                             idesc_mxf8(128 * CG, 256, k, k), tSA, tSB, 1u);
+              if constexpr (CG == 1) tc_commit(bar_empty + 8 * st);
+              else tc_commit_pair(bar_empty + 8 * st, 0x3);
+            }
+            __syncwarp();
+            next_ready = __shfl_sync(0xFFFFFFFFu, next_ready, __ffs(__ballot_sync(0xFFFFFFFFu, leader)) - 1);
+            if (++ks == w.ke) {
+              if (leader) {
+                if constexpr (CG == 1) tc_commit(bar_acc_full);
+                else tc_commit_pair(bar_acc_full, 0x3);
+              }
+              __syncwarp();
               acc_phase ^= 1u;
-              t += tile_stride;
-              if (t >= p.num_tiles) {
-                ok = false;
-              } else if (!wait_phase<CL>(bar_acc_empty, acc_phase ^ 1u, wc,
-                                         0x02 | ((t & 0xFFFF) << 16))) {
+              if (!wi.next(w)) {
                 ok = false;
               } else {
-                tc_fence_after();
+                ks = w.kb;
+                ok = __all_sync(0xFFFFFFFFu, wait_phase<CL>(bar_acc_empty, acc_phase ^ 1u, wc,
+                                                            0x02 | ((w.tile & 0xFFFF) << 16)));
+                if (ok) tc_fence_after();
               }
             }
             if (ok && !next_ready)
-              ok = wait_phase<false>(bar_full + 8 * nst, nph, wc, 0x03 | (nst << 8));
+              ok = __all_sync(0xFFFFFFFFu,
+                              wait_phase<false>(bar_full + 8 * nst, nph, wc, 0x03 | (nst << 8)));
           }
         }
         if (ok) phase ^= 1u;
       }
       // all issued tcgen05 work has finished before TMEM can be released
-      if constexpr (CG == 1) tc_commit(bar_final);
-      else tc_commit_pair(bar_final, 0x1);
+      if (leader) {
+        if constexpr (CG == 1) tc_commit(bar_final);
+        else tc_commit_pair(bar_final, 0x1);
+      }
+      __syncwarp();
       WaitCtl wf = wc;
       wf.abort_flag = reinterpret_cast<volatile int *>(sm + C::OFF_MISC + 8);  // never raised
-      *wf.abort_flag = 0;
+      if (lane == 0) *wf.abort_flag = 0;
+      __syncwarp();
       wait_phase<false>(bar_final, 0, wf, 0x04);
     }
   } else {
@@ -373,10 +483,13 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
     const int q = warp & 3;   // TMEM lane quarter this warp may access
     const int h = ew >> 2;    // which 128-column half
     uint32_t acc_phase = 0;
-    for (int t = first_tile; t < p.num_tiles; t += tile_stride) {
+    WorkIter wi(p, unit, units);
+    WorkItem w;
+    while (wi.next(w)) {
+      const int t = w.tile;
       int mt, nt;
       tile_coords(t, p.m_tiles, p.n_tiles, mt, nt);
-      if (kAcc && kTma && lane == 0) {
+      if (kAcc && kTma && w.kind != kPartial && lane == 0) {
         // pull this warp's part of C_in into L2 while the tile's MMAs run
         const int r0 = mt * (128 * CG) + 128 * (int)rank + 32 * q;
         const int cw = kBF16 ? 32 : 16;
@@ -402,6 +515,50 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
         else mbar_arrive_cluster(bar_acc_empty, 0);
       }
       acc_phase ^= 1u;
+
+      if (w.kind == kPartial) {
+        // first part of a split tile: the FP32 partial to this CTA's slot,
+        // then count this warp in the slot's flag.  The slot is laid out by
+        // (warp, 4-column group, lane) -- the reader uses the same warp/lane
+        // to row mapping -- so every warp access covers 512 contiguous bytes.
+        float4 *slot = reinterpret_cast<float4 *>(p.partials) +
+                       static_cast<int64_t>(unit * CG + (int)rank) * (128 * 256 / 4) + ew * (32 * 32) + lane;
+#pragma unroll
+        for (int c = 0; c < 128; c += 4)
+          __stcg(slot + (c / 4) * 32,
+                 make_float4(__uint_as_float(v[c >> 5][(c & 31) + 0]), __uint_as_float(v[c >> 5][(c & 31) + 1]),
+                             __uint_as_float(v[c >> 5][(c & 31) + 2]), __uint_as_float(v[c >> 5][(c & 31) + 3])));
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) atomicAdd(p.flags + unit * CG + (int)rank, 1);
+        continue;
+      }
+      if (w.kind == kOwner) {
+        // last part: add the partials of the CTAs that computed the earlier parts
+        bool got = true;
+        for (int c = w.first_contrib; c < unit && got; ++c) {
+          const int *flag = p.flags + c * CG + (int)rank;
+          int ready = 1;
+          if (lane == 0) ready = wait_flag(flag, C::EPI_WARPS, wc, 0x06 | ((t & 0xFFFF) << 16));
+          ready = __shfl_sync(0xFFFFFFFFu, ready, 0);
+          if (!ready) {
+            got = false;
+            break;
+          }
+          __threadfence();
+          const float4 *slot = reinterpret_cast<const float4 *>(p.partials) +
+                               static_cast<int64_t>(c * CG + (int)rank) * (128 * 256 / 4) + ew * (32 * 32) + lane;
+#pragma unroll
+          for (int c4 = 0; c4 < 128; c4 += 4) {
+            const float4 o = __ldcg(slot + (c4 / 4) * 32);
+            v[c4 >> 5][(c4 & 31) + 0] = __float_as_uint(__uint_as_float(v[c4 >> 5][(c4 & 31) + 0]) + o.x);
+            v[c4 >> 5][(c4 & 31) + 1] = __float_as_uint(__uint_as_float(v[c4 >> 5][(c4 & 31) + 1]) + o.y);
+            v[c4 >> 5][(c4 & 31) + 2] = __float_as_uint(__uint_as_float(v[c4 >> 5][(c4 & 31) + 2]) + o.z);
+            v[c4 >> 5][(c4 & 31) + 3] = __float_as_uint(__uint_as_float(v[c4 >> 5][(c4 & 31) + 3]) + o.w);
+          }
+        }
+        if (!got) break;
+      }
 
       const int row0w = mt * (128 * CG) + 128 * (int)rank + 32 * q;  // this warp's first row
       const int row = row0w + lane;

@@ -36,7 +36,10 @@ struct RepackArgs {
 constexpr int kRepackThreads = 512;
 
 __global__ void __launch_bounds__(kRepackThreads)
-    repack_scales_kernel(RepackArgs a0, RepackArgs a1, int blocks0) {
+    repack_scales_kernel(RepackArgs a0, RepackArgs a1, int blocks0, int *flags, int nflags) {
+  // the GEMM's stream-K flags start every launch at zero
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < nflags; i += kRepackThreads) flags[i] = 0;
   __shared__ __align__(16) uint32_t tile[128 * 16];  // 128 rows x 64 bytes
   const bool second = static_cast<int>(blockIdx.x) >= blocks0;
   const RepackArgs a = second ? a1 : a0;

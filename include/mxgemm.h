@@ -80,7 +80,12 @@ typedef enum {
   /* Persistent tile scheduler: 0 = static striding over a grid of one CTA
    * (pair) per SM, 1 = cluster launch control (grid of all tiles; running
    * CTAs cancel not-yet-launched ones and take their tiles).  Default 0. */
-  MXGEMM_OPT_SCHEDULER = 4
+  MXGEMM_OPT_SCHEDULER = 4,
+  /* Stream-K tail: 1 (default) lets the persistent grid split the K steps
+   * of the tiles left over after the last full wave evenly over all CTAs,
+   * one CTA per tile adding the others' FP32 partials (kept in the handle's
+   * workspace) before it stores C; 0 computes every tile whole. */
+  MXGEMM_OPT_STREAM_K = 5
 } mxgemm_option_t;
 
 /* Create a handle bound to CUDA device `device`.  Fails with

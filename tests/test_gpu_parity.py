@@ -222,3 +222,29 @@ def test_timeout_reports_and_device_stays_usable():
             gu.check_full(g, p)
     finally:
         mx.mxgemm_destroy(g)
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("out_dtype,use_acc", [("f32", False), ("bf16", False), ("f32", True), ("bf16", True)])
+def test_stream_k_tail_matches_whole_tiles(h, mode, out_dtype, use_acc):
+    # 256 x 22016 x 8192: 172 tiles of 128x256 (86 of 256x256) with 64 K
+    # steps, one full wave on 152 CTAs (76 pairs), then a tail of 20 (10)
+    # tiles -- the last 10 tile columns -- whose K ranges are split over all
+    # CTAs and finished by the CTA holding each tile's last K steps.  Checked
+    # on 16 whole rows against the oracle, with the tail on and off.
+    _mode(h, mode)
+    p = mi.random_problem(256, 256 * 86, 8192, seed=41 + mode, kind="normal", out_dtype=out_dtype)
+    cin = mi.c_init(p.M, p.N, 41, out_dtype) if use_acc else None
+    rows = np.array([0, 1, 31, 64, 127, 128, 129, 160, 191, 200, 223, 250, 253, 254, 255, 100])
+    ref, bound = oracle.rows(p.A, p.As, p.B, p.Bs, rows=rows,
+                             c_in=None if cin is None else cin.to(torch.float64).numpy()[rows])
+    outs = {}
+    try:
+        for sk in (1, 0):
+            mx.mxgemm_set_option(h, mx.OPT_STREAM_K, sk)
+            C = gu.run_gpu(h, p, c_init=cin, use_acc=use_acc)
+            outs[sk] = gu.to_numpy_out(C, out_dtype)
+            res = oracle.accept(outs[sk][rows], ref, bound, out_dtype)
+            assert res["ok"], f"stream_k={sk}: {res}"
+    finally:
+        mx.mxgemm_set_option(h, mx.OPT_STREAM_K, 1)
