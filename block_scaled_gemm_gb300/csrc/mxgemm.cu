@@ -479,9 +479,9 @@ int mxgemm_run(mxgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A
   // workspace size depends only on the shape and mode
   int CG = 1;
   if (h->mode == 2) CG = 2;
-  // automatic: the CTA pair halves the B traffic and TMA requests per SM;
-  // measured faster once K is long enough to amortise its per-tile cost
-  else if (h->mode == 0 && M > 128 && K >= 6144) CG = 2;
+  // automatic: the CTA pair halves the B traffic and TMA requests per SM
+  // and measured faster on every workload with more than one 128-row block
+  else if (h->mode == 0 && M > 128) CG = 2;
   const int64_t m_tiles = cdiv(M, 128 * CG);
   const int64_t n_tiles = cdiv(N, 256);
   const int64_t k_steps = cdiv(K, 128);

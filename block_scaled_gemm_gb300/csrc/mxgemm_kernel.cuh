@@ -322,7 +322,9 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
   // (a rolled loop with a runtime stage index cost about 30% of MMA rate).
   if (warp == 0) {
     // ------------------------------------------------------------ producer
-    if (lane == 0) {
+    // the whole warp runs the loop in lock-step; one elected lane issues
+    {
+      const bool leader = elect_one() != 0;
       uint32_t phase = 0;
       int nst = 0;           // next stage to fill ...
       uint32_t nph = 0;      // ... and the ring phase it belongs to
@@ -335,9 +337,10 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
 #pragma unroll
         for (int st = 0; st < C::STAGES; ++st) {
           if (ok) {
-            if (!wait_phase<false>(bar_empty + 8 * st, phase ^ 1u, wc, 0x01 | (st << 8))) {
+            if (!__all_sync(0xFFFFFFFFu,
+                            wait_phase<false>(bar_empty + 8 * st, phase ^ 1u, wc, 0x01 | (st << 8)))) {
               ok = false;
-            } else {
+            } else if (leader) {
               const uint32_t fb = bar_full + 8 * st;
               const uint32_t sA = base + C::OFF_A + st * C::A_BYTES;
               const uint32_t sB = base + C::OFF_B + st * C::B_BYTES;
@@ -362,6 +365,9 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
                 tma_load_2d_pair(sSA, &tmSFA, 0, (mblk * p.k_steps + ks) * 4, fbl);
                 tma_load_2d_pair(sSB, &tmSFB, 0, (nt * p.k_steps + ks) * 8, fbl);
               }
+            }
+            if (ok) {
+              __syncwarp();
               nst = (st + 1 == C::STAGES) ? 0 : st + 1;
               nph = (st + 1 == C::STAGES) ? (phase ^ 1u) : phase;
               if (++ks == w.ke) {
@@ -380,7 +386,8 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
       // Drain: every stage's last fill has been consumed (its MMA commit has
       // arrived) before this CTA may finish.
       for (int i = 0; i < C::STAGES; ++i) {
-        if (!wait_phase<false>(bar_empty + 8 * nst, nph ^ 1u, wc, 0x11 | (nst << 8))) break;
+        if (!__all_sync(0xFFFFFFFFu, wait_phase<false>(bar_empty + 8 * nst, nph ^ 1u, wc, 0x11 | (nst << 8))))
+          break;
         if (++nst == C::STAGES) {
           nst = 0;
           nph ^= 1u;
@@ -496,10 +503,10 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
         for (int c0 = nt * 256 + 128 * h; c0 < nt * 256 + 128 * h + 128 && c0 < p.N && r0 < p.M; c0 += cw)
           tma_prefetch_l2_2d(&tmC, c0, r0);
       }
-      int ok = 1;
-      if (lane == 0) ok = wait_phase<false>(bar_acc_full, acc_phase, wc, 0x05 | ((t & 0xFFFF) << 16));
-      ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-      if (!ok) break;
+      // all lanes wait (warp-uniform control flow)
+      if (!__all_sync(0xFFFFFFFFu,
+                      wait_phase<false>(bar_acc_full, acc_phase, wc, 0x05 | ((t & 0xFFFF) << 16))))
+        break;
       tc_fence_after();
       uint32_t v[4][32];
       const uint32_t ta = tmem + (static_cast<uint32_t>(32 * q) << 16) + C::TM_ACC + 128 * h;
@@ -538,9 +545,8 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
         bool got = true;
         for (int c = w.first_contrib; c < unit && got; ++c) {
           const int *flag = p.flags + c * CG + (int)rank;
-          int ready = 1;
-          if (lane == 0) ready = wait_flag(flag, C::EPI_WARPS, wc, 0x06 | ((t & 0xFFFF) << 16));
-          ready = __shfl_sync(0xFFFFFFFFu, ready, 0);
+          const bool ready =
+              __all_sync(0xFFFFFFFFu, wait_flag(flag, C::EPI_WARPS, wc, 0x06 | ((t & 0xFFFF) << 16)));
           if (!ready) {
             got = false;
             break;

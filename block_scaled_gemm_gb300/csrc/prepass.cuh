@@ -84,22 +84,34 @@ __global__ void __launch_bounds__(kRepackThreads)
 
 // Copy B [K][N] into [K][Npad] (Npad a multiple of 16) so that its rows meet
 // the 16-byte stride rule of tensor-map loads; the pad columns are zero.
+// Each thread writes 16 bytes; it reads them with the widest loads the
+// source row's alignment allows (8, 4 or 1 byte).
 __global__ void pad_rows_kernel(const uint8_t *__restrict__ B, int64_t rows, int64_t N,
                                 int64_t Npad, uint8_t *__restrict__ out) {
   const int64_t per_row = Npad / 16;
   const int64_t total = rows * per_row;
   griddep_launch_dependents();
+  const int align = (N % 8 == 0 && (reinterpret_cast<uintptr_t>(B) & 7) == 0) ? 8
+                    : (N % 4 == 0 && (reinterpret_cast<uintptr_t>(B) & 3) == 0) ? 4 : 1;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t r = i / per_row;
     const int64_t c0 = (i - r * per_row) * 16;
-    const uint8_t *src = B + r * N;
+    const uint8_t *src = B + r * N + c0;
     uint32_t w[4] = {0, 0, 0, 0};
+    if (c0 + 16 <= N && align == 8) {
+      const uint2 a = reinterpret_cast<const uint2 *>(src)[0];
+      const uint2 b = reinterpret_cast<const uint2 *>(src)[1];
+      w[0] = a.x; w[1] = a.y; w[2] = b.x; w[3] = b.y;
+    } else if (c0 + 16 <= N && align == 4) {
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
-      const int64_t c = c0 + j;
-      const uint32_t b = c < N ? src[c] : 0u;
-      w[j >> 2] |= b << (8 * (j & 3));
+      for (int j = 0; j < 4; ++j) w[j] = reinterpret_cast<const uint32_t *>(src)[j];
+    } else {
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const uint32_t b = c0 + j < N ? src[j] : 0u;
+        w[j >> 2] |= b << (8 * (j & 3));
+      }
     }
     *reinterpret_cast<uint4 *>(out + r * Npad + c0) = make_uint4(w[0], w[1], w[2], w[3]);
   }

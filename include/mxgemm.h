@@ -66,9 +66,9 @@ typedef enum {
 
 /* Options for mxgemm_set_option. */
 typedef enum {
-  /* Tile mode: 0 = automatic (CTA pair when M > 128 and K >= 6144, else one
-   * CTA), 1 = one CTA per 128x256 tile, 2 = CTA pair (cta_group::2) per
-   * 256x256 tile.  Default 0. */
+  /* Tile mode: 0 = automatic (CTA pair when M > 128, else one CTA), 1 = one
+   * CTA per 128x256 tile, 2 = CTA pair (cta_group::2) per 256x256 tile.
+   * Default 0. */
   MXGEMM_OPT_MODE = 1,
   /* Device-side wait limit in nanoseconds (default 2e9).  A wait that runs
    * out sets MXGEMM_ERR_TIMEOUT and the kernel drains and returns. */
@@ -155,7 +155,8 @@ int mxgemm_destroy(mxgemm_handle_t h);
  * The first call on a device does a one-time set-up for that device (device
  * check and lookup of the array's device address); make that first call
  * before starting any stream capture.  Arguments, layouts and use_acc are as
- * for mxgemm_run; tile mode is automatic.  A device-side wait that runs out
+ * for mxgemm_run; it always uses single-CTA 128x256 tiles computed whole.  A
+ * device-side wait that runs out
  * is recorded in an internal status word that this entry point cannot report:
  * C is then incomplete. */
 int mxgemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A,

@@ -50,9 +50,10 @@ def test_noalloc_matches_regular_entry_point_twice():
     outs = [_noalloc(p) for p in problems]
     torch.cuda.synchronize()
     h = mx.mxgemm_create(0)
-    # whole tiles, as the no-allocation path computes them, so that the two
-    # results can also be compared bit for bit
+    # whole single-CTA tiles, as the no-allocation path computes them, so
+    # that the two results can also be compared bit for bit
     mx.mxgemm_set_option(h, mx.OPT_STREAM_K, 0)
+    mx.mxgemm_set_option(h, mx.OPT_MODE, 1)
     try:
         for p, c_na in zip(problems, outs):
             c_reg = _regular(h, p)
