@@ -45,7 +45,7 @@ struct Plan {
   int CG = 1;
   bool pad_b = false;
   int64_t npad = 0;
-  CUtensorMap tA, tB, tSA, tSB, tC;
+  CUtensorMap tA, tB, tB64, tSA, tSB, tC;
   KParams kp;
   mxg::RepackArgs ra, rb;
   int blocks_a = 0, blocks_b = 0;
@@ -149,7 +149,7 @@ int ensure_workspace(mxgemm_ctx *h, size_t bytes, cudaStream_t stream) {
 
 template <int CG, int EPI>
 int launch_gemm_epi(mxgemm_ctx *h, const CUtensorMap &tA, const CUtensorMap &tB,
-                    const CUtensorMap &tSA, const CUtensorMap &tSB, const CUtensorMap &tC,
+                    const CUtensorMap &tB64, const CUtensorMap &tSA, const CUtensorMap &tSB, const CUtensorMap &tC,
                     const KParams &kp, int units, cudaStream_t stream) {
   using C = Cfg<CG>;
   auto kern = mxg::mxgemm_kernel<CG, EPI>;
@@ -186,7 +186,7 @@ int launch_gemm_epi(mxgemm_ctx *h, const CUtensorMap &tA, const CUtensorMap &tB,
     cudaGetLastError();
     return MXGEMM_ERR_CUDA;
   }
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tA, tB, tSA, tSB, tC, kp);
+  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tA, tB, tB64, tSA, tSB, tC, kp);
   if (e != cudaSuccess) {
     cudaGetLastError();
     return MXGEMM_ERR_CUDA;
@@ -203,19 +203,19 @@ int launch_gemm_epi(mxgemm_ctx *h, const CUtensorMap &tA, const CUtensorMap &tB,
 // TMA or direct stores).
 template <int CG>
 int launch_gemm(mxgemm_ctx *h, const CUtensorMap &tA, const CUtensorMap &tB,
-                const CUtensorMap &tSA, const CUtensorMap &tSB, const CUtensorMap &tC,
+                const CUtensorMap &tB64, const CUtensorMap &tSA, const CUtensorMap &tSB, const CUtensorMap &tC,
                 const KParams &kp, int units, cudaStream_t stream) {
   const int epi = (kp.out_bf16 ? mxg::kEpiBF16 : 0) | (kp.use_acc ? mxg::kEpiAcc : 0) |
                   (kp.tma_store ? mxg::kEpiTma : 0);
   switch (epi) {
-    case 0: return launch_gemm_epi<CG, 0>(h, tA, tB, tSA, tSB, tC, kp, units, stream);
-    case 1: return launch_gemm_epi<CG, 1>(h, tA, tB, tSA, tSB, tC, kp, units, stream);
-    case 2: return launch_gemm_epi<CG, 2>(h, tA, tB, tSA, tSB, tC, kp, units, stream);
-    case 3: return launch_gemm_epi<CG, 3>(h, tA, tB, tSA, tSB, tC, kp, units, stream);
-    case 4: return launch_gemm_epi<CG, 4>(h, tA, tB, tSA, tSB, tC, kp, units, stream);
-    case 5: return launch_gemm_epi<CG, 5>(h, tA, tB, tSA, tSB, tC, kp, units, stream);
-    case 6: return launch_gemm_epi<CG, 6>(h, tA, tB, tSA, tSB, tC, kp, units, stream);
-    default: return launch_gemm_epi<CG, 7>(h, tA, tB, tSA, tSB, tC, kp, units, stream);
+    case 0: return launch_gemm_epi<CG, 0>(h, tA, tB, tB64, tSA, tSB, tC, kp, units, stream);
+    case 1: return launch_gemm_epi<CG, 1>(h, tA, tB, tB64, tSA, tSB, tC, kp, units, stream);
+    case 2: return launch_gemm_epi<CG, 2>(h, tA, tB, tB64, tSA, tSB, tC, kp, units, stream);
+    case 3: return launch_gemm_epi<CG, 3>(h, tA, tB, tB64, tSA, tSB, tC, kp, units, stream);
+    case 4: return launch_gemm_epi<CG, 4>(h, tA, tB, tB64, tSA, tSB, tC, kp, units, stream);
+    case 5: return launch_gemm_epi<CG, 5>(h, tA, tB, tB64, tSA, tSB, tC, kp, units, stream);
+    case 6: return launch_gemm_epi<CG, 6>(h, tA, tB, tB64, tSA, tSB, tC, kp, units, stream);
+    default: return launch_gemm_epi<CG, 7>(h, tA, tB, tB64, tSA, tSB, tC, kp, units, stream);
   }
 }
 
@@ -226,37 +226,51 @@ int launch_blocks(int64_t work, int per_block) {
   return static_cast<int>(b);
 }
 
-// How the GEMM grid covers the tiles: whole tiles in full waves, and a
-// stream-K tail (the leftover tiles' K steps split evenly over the CTAs)
-// when the tiles do not fill the last wave.
+// How the GEMM grid covers the tiles: whole tiles in full waves, and for
+// the tiles that do not fill the last wave either a stream-K tail (their K
+// steps split evenly over the CTAs) or half-width tiles (each leftover tile
+// computed as two 128-column halves).
 struct Split {
   int units;           // persistent CTAs (pairs)
   int dp_tiles;        // tiles computed whole
   int sk_ctas;         // CTAs sharing the tail
   long long sk_units;  // K steps in the tail
+  int half_tiles;      // half-width items after the whole tiles (2 per leftover tile)
 };
 
-Split plan_split(int64_t T, int64_t S, int P, bool allow_stream_k) {
+Split plan_split(int64_t T, int64_t S, int P, bool allow_tail) {
   Split r;
   r.units = static_cast<int>(T < P ? T : P);
   r.dp_tiles = static_cast<int>(T);
   r.sk_ctas = 0;
   r.sk_units = 0;
+  r.half_tiles = 0;
+  if (!allow_tail || T == 0) return r;
+  const int64_t W = T / P, R = T % P;
+  if (R == 0) return r;
   // Measured on GB300: the owners' gather of FP32 partials is slow enough
-  // that the split pays off only with long K (64+ steps) after 1 to 8 full
+  // that stream-K pays off only with long K (64+ steps) after 1 to 8 full
   // waves, and not when the last wave is nearly full; in particular not when
   // every tile would be split (fewer tiles than CTAs).
-  if (!allow_stream_k || T == 0 || S < 64) return r;
-  const int64_t W = T / P, R = T % P;
-  if (W < 1 || W > 8 || R == 0 || R * 100 >= static_cast<int64_t>(P) * 85) return r;
-  const int64_t tail = R * S;
-  int64_t ctas = tail / 4;  // at least 4 K steps per CTA
-  if (ctas > P) ctas = P;
-  if (ctas <= R) return r;  // no CTA would get less than a whole tile
-  r.units = P;
-  r.dp_tiles = static_cast<int>(W * P);
-  r.sk_ctas = static_cast<int>(ctas);
-  r.sk_units = tail;
+  if (S >= 64 && W >= 1 && W <= 8 && R * 100 < static_cast<int64_t>(P) * 85) {
+    const int64_t tail = R * S;
+    int64_t ctas = tail / 4;  // at least 4 K steps per CTA
+    if (ctas > P) ctas = P;
+    if (ctas > R) {  // else no CTA would get less than a whole tile
+      r.units = P;
+      r.dp_tiles = static_cast<int>(W * P);
+      r.sk_ctas = static_cast<int>(ctas);
+      r.sk_units = tail;
+      return r;
+    }
+  }
+  // Otherwise, when the leftover tiles fill at most half a wave, halve
+  // their width: twice as many CTAs (pairs) finish them in half the time.
+  if (2 * R <= P) {
+    r.dp_tiles = static_cast<int>(W * P);
+    r.half_tiles = static_cast<int>(2 * R);
+    r.units = static_cast<int>(W >= 1 ? P : 2 * R);
+  }
   return r;
 }
 
@@ -302,6 +316,8 @@ int build_plan(mxgemm_ctx *h, Plan *pl, int64_t M, int64_t N, int64_t K, const v
   const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
   if (encode_2d(h, &pl->tA, u8, A, K, M, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
       encode_2d(h, &pl->tB, u8, bsrc, N, K, bpitch, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+      // half-width tiles of CTA pairs: 64 columns per CTA
+      encode_2d(h, &pl->tB64, u8, bsrc, N, K, bpitch, 64, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
       // scale chunks are contiguous 512-byte blocks; fetched as rows of 128
       // bytes (4 rows per chunk) so each chunk is a handful of TMA requests
       encode_2d(h, &pl->tSA, u8, sfa, 128, a_chunks * 4, 128, 128, 4, CU_TENSOR_MAP_SWIZZLE_NONE) ||
@@ -341,6 +357,7 @@ int build_plan(mxgemm_ctx *h, Plan *pl, int64_t M, int64_t N, int64_t K, const v
   kp.sk_units = sp.sk_units;
   kp.partials = reinterpret_cast<float *>(h->ws.ptr + z.off_part);
   kp.flags = reinterpret_cast<int *>(h->ws.ptr + z.off_flags);
+  kp.half_tiles = sp.half_tiles;
   pl->units = sp.units;
   pl->flags = kp.flags;
   pl->nflags = sp.sk_ctas * CG;
@@ -528,9 +545,9 @@ int mxgemm_run(mxgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A
       plan->ra, plan->rb, plan->blocks_a, plan->flags, plan->nflags);
   h->launches += 1;
   if (cudaGetLastError() != cudaSuccess) return MXGEMM_ERR_CUDA;
-  return plan->CG == 2 ? launch_gemm<2>(h, plan->tA, plan->tB, plan->tSA, plan->tSB, plan->tC,
+  return plan->CG == 2 ? launch_gemm<2>(h, plan->tA, plan->tB, plan->tB64, plan->tSA, plan->tSB, plan->tC,
                                         plan->kp, plan->units, stream)
-                       : launch_gemm<1>(h, plan->tA, plan->tB, plan->tSA, plan->tSB, plan->tC,
+                       : launch_gemm<1>(h, plan->tA, plan->tB, plan->tB64, plan->tSA, plan->tSB, plan->tC,
                                         plan->kp, plan->units, stream);
 }
 
@@ -738,7 +755,7 @@ extern "C" int mxgemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A
   mxg::repack_scales_kernel<<<plan.blocks_a + plan.blocks_b, mxg::kRepackThreads, 0, stream>>>(
       plan.ra, plan.rb, plan.blocks_a, plan.flags, plan.nflags);
   if (cudaGetLastError() != cudaSuccess) return MXGEMM_ERR_CUDA;
-  st = launch_gemm<1>(&ctx, plan.tA, plan.tB, plan.tSA, plan.tSB, plan.tC, plan.kp, plan.units,
+  st = launch_gemm<1>(&ctx, plan.tA, plan.tB, plan.tB64, plan.tSA, plan.tSB, plan.tC, plan.kp, plan.units,
                       stream);
   {
     std::lock_guard<std::mutex> lock(g_noalloc_mu);

@@ -54,6 +54,8 @@ struct Cfg {
   static constexpr int SFA_BYTES = 512;   // 128 rows x 4 K-blocks
   static constexpr int SFB_BYTES = 1024;  // 256 columns x 4 K-blocks
   static constexpr uint32_t STAGE_TX = (A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES) * CG;
+  // half-width (128-column) tile: each CTA loads half of its B columns
+  static constexpr uint32_t STAGE_TX_HALF = STAGE_TX - (B_BYTES / 2) * CG;
   static constexpr int OFF_A = 0;
   static constexpr int OFF_B = OFF_A + STAGES * A_BYTES;
   static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
@@ -97,6 +99,9 @@ struct KParams {
   long long sk_units;  // (num_tiles - dp_tiles) * k_steps
   float *partials;     // per CTA: 128 x 256 FP32 partial accumulator
   int *flags;          // per CTA: epilogue warps that have written its partial
+  // half-width tail (see WorkIter): items [dp_tiles, dp_tiles + half_tiles)
+  // of the whole-tile walk are 128-column halves of tiles dp_tiles, ...
+  int half_tiles;
 };
 
 // Instruction descriptor of tcgen05.mma.kind::mxf8f6f4.block_scale:
@@ -136,6 +141,9 @@ __device__ __forceinline__ void tile_coords(int t, int m_tiles, int n_tiles, int
 // first, partial before finish, and then its whole tiles dp_tiles-ward
 // (u, u+P, ...): every partial is written before anyone waits for it, and an
 // owner's wait for partials overlaps the MMAs of its first whole tile.
+// Alternatively, when the leftover tiles fill at most half a wave, each of
+// them is computed as two 128-column halves by two CTAs (pairs): the last
+// wave then takes half as long and needs no partial sums.
 constexpr int kFull = 0;     // whole K range: store C
 constexpr int kPartial = 1;  // first part of a tile's K range: write a partial
 constexpr int kOwner = 2;    // last part: add the earlier parts' partials, store C
@@ -145,17 +153,18 @@ struct WorkItem {
   int kb, ke;         // K steps [kb, ke)
   int kind;
   int first_contrib;  // kOwner: CTAs first_contrib .. u-1 hold this tile's partials
+  int half;           // -1: all 256 columns; 0 / 1: only that 128-column half
 };
 
 struct WorkIter {
-  int u, P, dp_tiles, k_steps, sk_ctas;
+  int u, P, dp_tiles, k_steps, sk_ctas, half_tiles;
   long long sk_units;
   int i = 0;         // next whole tile: u + i * P
   int tail_pos = 0;  // next tail segment (0: later tile, 1: earlier tile, 2: done)
 
   __device__ WorkIter(const KParams &p, int u_, int P_)
       : u(u_), P(P_), dp_tiles(p.dp_tiles), k_steps(p.k_steps), sk_ctas(p.sk_ctas),
-        sk_units(p.sk_units) {
+        half_tiles(p.half_tiles), sk_units(p.sk_units) {
     if (sk_units == 0 || u >= sk_ctas) tail_pos = 2;
   }
 
@@ -177,16 +186,23 @@ struct WorkIter {
       w.kind = last ? (first ? kFull : kOwner) : kPartial;
       // the CTA whose range holds the tile's first K step
       w.first_contrib = static_cast<int>(((j * S + 1) * sk_ctas - 1) / sk_units);
+      w.half = -1;
       return true;
     }
     const int t = u + i * P;
-    if (t >= dp_tiles) return false;
+    if (t >= dp_tiles + half_tiles) return false;
     ++i;
-    w.tile = t;
     w.kb = 0;
     w.ke = k_steps;
     w.kind = kFull;
     w.first_contrib = u;
+    if (t < dp_tiles) {
+      w.tile = t;
+      w.half = -1;
+    } else {
+      w.tile = dp_tiles + ((t - dp_tiles) >> 1);
+      w.half = (t - dp_tiles) & 1;
+    }
     return true;
   }
 };
@@ -250,6 +266,7 @@ __device__ __forceinline__ bool wait_flag(const int *flag, int target, const Wai
 template <int CG, int EPI>
 __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
     mxgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                  const __grid_constant__ CUtensorMap tmB64,
                   const __grid_constant__ CUtensorMap tmSFA,
                   const __grid_constant__ CUtensorMap tmSFB, const __grid_constant__ CUtensorMap tmC,
                   const KParams p) {
@@ -288,6 +305,7 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
+    if (CG == 2 && p.half_tiles > 0) tma_prefetch_desc(&tmB64);
     tma_prefetch_desc(&tmSFA);
     tma_prefetch_desc(&tmSFB);
     if (kTma) tma_prefetch_desc(&tmC);
@@ -333,6 +351,13 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
       bool ok = !p.stall_producer && wi.next(w);
       int ks = w.kb, mt = 0, nt = 0;
       if (ok) tile_coords(w.tile, p.m_tiles, p.n_tiles, mt, nt);
+      // whole tiles in the unrolled loop below; half-width tiles (only ever
+      // at the end of the walk) in the rolled loop after it
+      bool go_half = false;
+      if (ok && w.half >= 0) {
+        go_half = true;
+        ok = false;
+      }
       while (ok) {
 #pragma unroll
         for (int st = 0; st < C::STAGES; ++st) {
@@ -374,6 +399,10 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
                 if (wi.next(w)) {
                   ks = w.kb;
                   tile_coords(w.tile, p.m_tiles, p.n_tiles, mt, nt);
+                  if (w.half >= 0) {
+                    go_half = true;
+                    ok = false;
+                  }
                 } else {
                   ok = false;
                 }
@@ -382,6 +411,47 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
           }
         }
         if (ok) phase ^= 1u;
+      }
+      // half-width tiles: rolled loop, runtime stage index (nst, nph)
+      while (go_half) {
+        if (!__all_sync(0xFFFFFFFFu, wait_phase<false>(bar_empty + 8 * nst, nph ^ 1u, wc, 0x01 | (nst << 8))))
+          break;
+        if (leader) {
+          const uint32_t fb = bar_full + 8 * nst;
+          const uint32_t sA = base + C::OFF_A + nst * C::A_BYTES;
+          const uint32_t sB = base + C::OFF_B + nst * C::B_BYTES;
+          const uint32_t sSA = base + C::OFF_SFA + nst * C::SFA_BYTES;
+          const uint32_t sSB = base + C::OFF_SFB + nst * C::SFB_BYTES;
+          const int row0 = mt * (128 * CG) + 128 * (int)rank;
+          const int mblk = mt * CG + (int)rank;
+          const int col0 = nt * 256 + 128 * w.half;
+          const int k0 = ks * 128;
+          if constexpr (CG == 1) {
+            mbar_arrive_expect_tx(fb, C::STAGE_TX_HALF);
+            tma_load_2d(sA, &tmA, k0, row0, fb);
+            tma_load_2d(sB, &tmB, col0, k0, fb);
+            tma_load_2d(sSA, &tmSFA, 0, (mblk * p.k_steps + ks) * 4, fb);
+            tma_load_2d(sSB, &tmSFB, 0, (nt * p.k_steps + ks) * 8, fb);
+          } else {
+            if (rank == 0) mbar_arrive_expect_tx(fb, C::STAGE_TX_HALF);
+            const uint32_t fbl = mapa_shared(fb, 0);
+            tma_load_2d_pair(sA, &tmA, k0, row0, fbl);
+            // 64 columns per CTA, 64-byte swizzle
+            tma_load_2d_pair(sB, &tmB64, col0 + 64 * (int)rank, k0, fbl);
+            tma_load_2d_pair(sSA, &tmSFA, 0, (mblk * p.k_steps + ks) * 4, fbl);
+            tma_load_2d_pair(sSB, &tmSFB, 0, (nt * p.k_steps + ks) * 8, fbl);
+          }
+        }
+        __syncwarp();
+        if (++nst == C::STAGES) {
+          nst = 0;
+          nph ^= 1u;
+        }
+        if (++ks == w.ke) {
+          if (!wi.next(w)) break;
+          ks = w.kb;
+          tile_coords(w.tile, p.m_tiles, p.n_tiles, mt, nt);
+        }
       }
       // Drain: every stage's last fill has been consumed (its MMA commit has
       // arrived) before this CTA may finish.
@@ -409,6 +479,15 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
       WorkItem w;
       bool ok = wi.next(w);
       int ks = w.kb;
+      // whole tiles in the unrolled loop; half-width tiles (only ever at the
+      // end of the walk) in the rolled loop after it, from stage hst
+      bool go_half = false;
+      int hst = 0;
+      uint32_t hph = 0;
+      if (ok && w.half >= 0) {
+        go_half = true;
+        ok = false;
+      }
       if (ok) {
         ok = __all_sync(0xFFFFFFFFu, wait_phase<CL>(bar_acc_empty, acc_phase ^ 1u, wc, 0x02));
         tc_fence_after();
@@ -458,6 +537,11 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
               acc_phase ^= 1u;
               if (!wi.next(w)) {
                 ok = false;
+              } else if (w.half >= 0) {
+                go_half = true;
+                hst = nst;
+                hph = nph;
+                ok = false;
               } else {
                 ks = w.kb;
                 ok = __all_sync(0xFFFFFFFFu, wait_phase<CL>(bar_acc_empty, acc_phase ^ 1u, wc,
@@ -471,6 +555,60 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
           }
         }
         if (ok) phase ^= 1u;
+      }
+      // Half-width tiles: N = 128 MMAs; B scales are the matching 128-row
+      // half of the 256-column chunk.  Pairs hold 64 B columns per CTA
+      // (64-byte swizzle, 8-row K groups 512 B apart).
+      if (go_half) {
+        int s = hst;
+        uint32_t ph = hph;
+        const uint64_t bdesc = CG == 2 ? smem_desc(0, 8192, 512, 4) : smem_desc(0, 16384, 1024, 2);
+        const uint32_t bstep = CG == 2 ? 2048 : 4096;
+        bool run = true;
+        while (run) {
+          run = __all_sync(0xFFFFFFFFu, wait_phase<CL>(bar_acc_empty, acc_phase ^ 1u, wc,
+                                                       0x02 | ((w.tile & 0xFFFF) << 16)));
+          if (!run) break;
+          tc_fence_after();
+          const uint32_t sfb_off = 4u * static_cast<uint32_t>(w.half);
+          for (int k0 = w.kb; k0 < w.ke; ++k0) {
+            if (!__all_sync(0xFFFFFFFFu, wait_phase<false>(bar_full + 8 * s, ph, wc, 0x03 | (s << 8)))) {
+              run = false;
+              break;
+            }
+            if (leader) {
+              const uint32_t sA = base + C::OFF_A + s * C::A_BYTES;
+              const uint32_t sB = base + C::OFF_B + s * C::B_BYTES;
+              const uint32_t sSA = base + C::OFF_SFA + s * C::SFA_BYTES;
+              const uint32_t sSB = base + C::OFF_SFB + s * C::SFB_BYTES;
+              const uint32_t tSA = tmem + C::TM_SFA + 4 * s;
+              const uint32_t tSB = tmem + C::TM_SFB + 8 * s;
+              tmem_cp_32x128b_x4<CG>(tSA, smem_desc(sSA, 0, 128, 0));
+              tmem_cp_32x128b_x4<CG>(tSB, smem_desc(sSB, 0, 128, 0));
+              tmem_cp_32x128b_x4<CG>(tSB + 4, smem_desc(sSB + 512, 0, 128, 0));
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                mma_mxf8<CG>(tmem + C::TM_ACC, smem_desc(sA + 32 * k, 0, 1024, 2),
+                             bdesc | ((sB + bstep * k) >> 4), idesc_mxf8(128 * CG, 128, k, k), tSA,
+                             tSB + sfb_off, (k0 != w.kb || k != 0) ? 1u : 0u);
+              if constexpr (CG == 1) tc_commit(bar_empty + 8 * s);
+              else tc_commit_pair(bar_empty + 8 * s, 0x3);
+            }
+            __syncwarp();
+            if (++s == C::STAGES) {
+              s = 0;
+              ph ^= 1u;
+            }
+          }
+          if (!run) break;
+          if (leader) {
+            if constexpr (CG == 1) tc_commit(bar_acc_full);
+            else tc_commit_pair(bar_acc_full, 0x3);
+          }
+          __syncwarp();
+          acc_phase ^= 1u;
+          run = wi.next(w);
+        }
       }
       // all issued tcgen05 work has finished before TMEM can be released
       if (leader) {
@@ -488,7 +626,7 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
     // ------------------------------------------------------------ epilogue
     const int ew = warp - 2;  // 0..7
     const int q = warp & 3;   // TMEM lane quarter this warp may access
-    const int h = ew >> 2;    // which 128-column half
+    const int h = ew >> 2;    // which half of the tile's columns
     uint32_t acc_phase = 0;
     WorkIter wi(p, unit, units);
     WorkItem w;
@@ -496,11 +634,16 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
       const int t = w.tile;
       int mt, nt;
       tile_coords(t, p.m_tiles, p.n_tiles, mt, nt);
+      // this warp's columns: 128 of a whole tile, 64 of a half-width tile
+      const bool whole = w.half < 0;
+      const int ncols = whole ? 128 : 64;
+      const int tcol = whole ? 128 * h : 64 * h;  // first accumulator column
+      const int colb = nt * 256 + (whole ? 128 * h : 128 * w.half + 64 * h);
       if (kAcc && kTma && w.kind != kPartial && lane == 0) {
         // pull this warp's part of C_in into L2 while the tile's MMAs run
         const int r0 = mt * (128 * CG) + 128 * (int)rank + 32 * q;
         const int cw = kBF16 ? 32 : 16;
-        for (int c0 = nt * 256 + 128 * h; c0 < nt * 256 + 128 * h + 128 && c0 < p.N && r0 < p.M; c0 += cw)
+        for (int c0 = colb; c0 < colb + ncols && c0 < p.N && r0 < p.M; c0 += cw)
           tma_prefetch_l2_2d(&tmC, c0, r0);
       }
       // all lanes wait (warp-uniform control flow)
@@ -509,11 +652,13 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
         break;
       tc_fence_after();
       uint32_t v[4][32];
-      const uint32_t ta = tmem + (static_cast<uint32_t>(32 * q) << 16) + C::TM_ACC + 128 * h;
+      const uint32_t ta = tmem + (static_cast<uint32_t>(32 * q) << 16) + C::TM_ACC + tcol;
       tmem_ld_32x32b_x32(ta + 0, v[0]);
       tmem_ld_32x32b_x32(ta + 32, v[1]);
-      tmem_ld_32x32b_x32(ta + 64, v[2]);
-      tmem_ld_32x32b_x32(ta + 96, v[3]);
+      if (whole) {
+        tmem_ld_32x32b_x32(ta + 64, v[2]);
+        tmem_ld_32x32b_x32(ta + 96, v[3]);
+      }
       tmem_ld_wait();
       tc_fence_before();
       __syncwarp();
@@ -568,13 +713,13 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
 
       const int row0w = mt * (128 * CG) + 128 * (int)rank + 32 * q;  // this warp's first row
       const int row = row0w + lane;
-      const int colb = nt * 256 + 128 * h;
       if (kAcc && row < p.M) {
-        // C_in: this lane's row, 128 columns (the prefetch below put them in L2)
+        // C_in: this lane's row, ncols columns (the prefetch above put them in L2)
         if constexpr (!kBF16) {
           const float *cp = reinterpret_cast<const float *>(p.C) + static_cast<int64_t>(row) * p.N + colb;
 #pragma unroll
           for (int c = 0; c < 128; c += 4) {
+            if (c >= ncols) break;
             if (p.vec_ok && colb + c + 4 <= p.N) {
               const float4 o = *reinterpret_cast<const float4 *>(cp + c);
               v[c >> 5][(c & 31) + 0] = __float_as_uint(__uint_as_float(v[c >> 5][(c & 31) + 0]) + o.x);
@@ -594,6 +739,7 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
               reinterpret_cast<const __nv_bfloat16 *>(p.C) + static_cast<int64_t>(row) * p.N + colb;
 #pragma unroll
           for (int c = 0; c < 128; c += 8) {
+            if (c >= ncols) break;
             if (p.vec_ok && colb + c + 8 <= p.N) {
               const uint4 o = *reinterpret_cast<const uint4 *>(cp + c);
               const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
@@ -629,6 +775,7 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
           for (int ch = 0; ch < CHUNKS; ++ch) {
             const int ccols = kBF16 ? 32 : 16;
             if (kBF16 && ch >= 4) break;
+            if (ch * ccols >= ncols) break;
             const int c0 = colb + ch * ccols;
             if (c0 >= p.N) break;
             if (lane == 0) bulk_wait_read_all();
@@ -668,13 +815,13 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
           float *cp = reinterpret_cast<float *>(p.C) + static_cast<int64_t>(row) * p.N + colb;
 #pragma unroll
           for (int c = 0; c < 128; ++c)
-            if (colb + c < p.N) cp[c] = __uint_as_float(v[c >> 5][c & 31]);
+            if (c < ncols && colb + c < p.N) cp[c] = __uint_as_float(v[c >> 5][c & 31]);
         } else {
           __nv_bfloat16 *cp =
               reinterpret_cast<__nv_bfloat16 *>(p.C) + static_cast<int64_t>(row) * p.N + colb;
 #pragma unroll
           for (int c = 0; c < 128; ++c)
-            if (colb + c < p.N) cp[c] = __float2bfloat16_rn(__uint_as_float(v[c >> 5][c & 31]));
+            if (c < ncols && colb + c < p.N) cp[c] = __float2bfloat16_rn(__uint_as_float(v[c >> 5][c & 31]));
         }
       }
     }

@@ -248,3 +248,31 @@ def test_stream_k_tail_matches_whole_tiles(h, mode, out_dtype, use_acc):
             assert res["ok"], f"stream_k={sk}: {res}"
     finally:
         mx.mxgemm_set_option(h, mx.OPT_STREAM_K, 1)
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("out_dtype,use_acc", [("f32", False), ("bf16", False), ("f32", True), ("bf16", True)])
+def test_half_width_tail(h, mode, out_dtype, use_acc):
+    # 2560 x 3976 x 512: 160 tiles of 256x256 (320 of 128x256), two full
+    # waves on 76 pairs (152 CTAs), then 8 (16) leftover tiles -- rows
+    # 2048..2559, tile columns 12..15 -- each computed as two 128-column
+    # halves, the last half holding only 8 columns.  Whole rows in and
+    # outside that region are checked against the oracle.
+    _mode(h, mode)
+    p = mi.random_problem(2560, 3976, 512, seed=51 + mode, kind="normal", out_dtype=out_dtype)
+    cin = mi.c_init(p.M, p.N, 51, out_dtype) if use_acc else None
+    rows = np.array([0, 5, 2047, 2048, 2100, 2175, 2176, 2300, 2303, 2304, 2431, 2432, 2559])
+    ref, bound = oracle.rows(p.A, p.As, p.B, p.Bs, rows=rows,
+                             c_in=None if cin is None else cin.to(torch.float64).numpy()[rows])
+    C = gu.run_gpu(h, p, c_init=cin, use_acc=use_acc)
+    res = oracle.accept(gu.to_numpy_out(C, out_dtype)[rows], ref, bound, out_dtype)
+    assert res["ok"], res
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+def test_half_width_only(h, mode):
+    # 2000 x 1000 x 256: fewer tiles than half the CTAs (pairs), so every
+    # tile is computed as two 128-column halves; full check.
+    _mode(h, mode)
+    p = mi.random_problem(2000, 1000, 256, seed=61 + mode, kind="normal", out_dtype="f32")
+    gu.check_full(h, p)
