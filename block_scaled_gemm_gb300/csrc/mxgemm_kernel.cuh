@@ -338,6 +338,9 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
   // column and barrier of a step is a constant offset from a base, which
   // keeps the single issuing thread fast enough to hold the tensor pipe busy
   // (a rolled loop with a runtime stage index cost about 30% of MMA rate).
+  // Code size matters as much: these loops run from the instruction cache,
+  // and measured 5-20% slower whenever rarely taken code (another loop, a
+  // tile-switch path per stage) grew around them.
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     // the whole warp runs the loop in lock-step; one elected lane issues
@@ -358,59 +361,110 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
         go_half = true;
         ok = false;
       }
-      while (ok) {
+      // one whole-tile K step into stage st (elected lane)
+      auto load_whole = [&](int st) {
+        const uint32_t fb = bar_full + 8 * st;
+        const uint32_t sA = base + C::OFF_A + st * C::A_BYTES;
+        const uint32_t sB = base + C::OFF_B + st * C::B_BYTES;
+        const uint32_t sSA = base + C::OFF_SFA + st * C::SFA_BYTES;
+        const uint32_t sSB = base + C::OFF_SFB + st * C::SFB_BYTES;
+        const int row0 = mt * (128 * CG) + 128 * (int)rank;  // this CTA's A rows
+        const int mblk = mt * CG + (int)rank;                  // its 128-row block
+        const int col0 = nt * 256;
+        const int k0 = ks * 128;
+        if constexpr (CG == 1) {
+          mbar_arrive_expect_tx(fb, C::STAGE_TX);
+          tma_load_2d(sA, &tmA, k0, row0, fb);
+          tma_load_2d(sB, &tmB, col0, k0, fb);
+          tma_load_2d(sB + 16384, &tmB, col0 + 128, k0, fb);
+          tma_load_2d(sSA, &tmSFA, 0, (mblk * p.k_steps + ks) * 4, fb);
+          tma_load_2d(sSB, &tmSFB, 0, (nt * p.k_steps + ks) * 8, fb);
+        } else {
+          if (rank == 0) mbar_arrive_expect_tx(fb, C::STAGE_TX);
+          const uint32_t fbl = mapa_shared(fb, 0);  // leader's barrier
+          tma_load_2d_pair(sA, &tmA, k0, row0, fbl);
+          tma_load_2d_pair(sB, &tmB, col0 + 128 * (int)rank, k0, fbl);
+          tma_load_2d_pair(sSA, &tmSFA, 0, (mblk * p.k_steps + ks) * 4, fbl);
+          tma_load_2d_pair(sSB, &tmSFB, 0, (nt * p.k_steps + ks) * 8, fbl);
+        }
+      };
+      if constexpr (CG == 2) {
+        // Pairs: the unrolled loop holds only the per-step work; a stage
+        // that is not free yet, or a tile boundary, is handled after it
+        // (measured faster for pairs; slower for single CTAs, whose 4-stage
+        // ring is refilled late by the extra exit and re-entry).
+        int skip = 0;  // stages of the current ring round already filled
+        while (ok) {
+          bool tile_end = false, must_wait = false;
 #pragma unroll
-        for (int st = 0; st < C::STAGES; ++st) {
-          if (ok) {
-            if (!__all_sync(0xFFFFFFFFu,
-                            wait_phase<false>(bar_empty + 8 * st, phase ^ 1u, wc, 0x01 | (st << 8)))) {
-              ok = false;
-            } else if (leader) {
-              const uint32_t fb = bar_full + 8 * st;
-              const uint32_t sA = base + C::OFF_A + st * C::A_BYTES;
-              const uint32_t sB = base + C::OFF_B + st * C::B_BYTES;
-              const uint32_t sSA = base + C::OFF_SFA + st * C::SFA_BYTES;
-              const uint32_t sSB = base + C::OFF_SFB + st * C::SFB_BYTES;
-              const int row0 = mt * (128 * CG) + 128 * (int)rank;  // this CTA's A rows
-              const int mblk = mt * CG + (int)rank;                  // its 128-row block
-              const int col0 = nt * 256;
-              const int k0 = ks * 128;
-              if constexpr (CG == 1) {
-                mbar_arrive_expect_tx(fb, C::STAGE_TX);
-                tma_load_2d(sA, &tmA, k0, row0, fb);
-                tma_load_2d(sB, &tmB, col0, k0, fb);
-                tma_load_2d(sB + 16384, &tmB, col0 + 128, k0, fb);
-                tma_load_2d(sSA, &tmSFA, 0, (mblk * p.k_steps + ks) * 4, fb);
-                tma_load_2d(sSB, &tmSFB, 0, (nt * p.k_steps + ks) * 8, fb);
-              } else {
-                if (rank == 0) mbar_arrive_expect_tx(fb, C::STAGE_TX);
-                const uint32_t fbl = mapa_shared(fb, 0);  // leader's barrier
-                tma_load_2d_pair(sA, &tmA, k0, row0, fbl);
-                tma_load_2d_pair(sB, &tmB, col0 + 128 * (int)rank, k0, fbl);
-                tma_load_2d_pair(sSA, &tmSFA, 0, (mblk * p.k_steps + ks) * 4, fbl);
-                tma_load_2d_pair(sSB, &tmSFB, 0, (nt * p.k_steps + ks) * 8, fbl);
-              }
+          for (int st = 0; st < C::STAGES; ++st) {
+            if (skip > 0) {
+              --skip;
+              continue;
             }
+            if (!__all_sync(0xFFFFFFFFu, mbar_test_wait(bar_empty + 8 * st, phase ^ 1u))) {
+              must_wait = true;
+              break;
+            }
+            if (leader) load_whole(st);
+            __syncwarp();
+            nst = (st + 1 == C::STAGES) ? 0 : st + 1;
+            nph = (st + 1 == C::STAGES) ? (phase ^ 1u) : phase;
+            if (++ks == w.ke) {
+              tile_end = true;
+              break;
+            }
+          }
+          if (!must_wait && !tile_end) {  // a whole ring round
+            phase ^= 1u;
+            continue;
+          }
+          // resume at stage nst of the ring round of phase nph
+          phase = nph;
+          skip = nst;
+          if (tile_end) {
+            if (!wi.next(w)) break;
+            ks = w.kb;
+            tile_coords(w.tile, p.m_tiles, p.n_tiles, mt, nt);
+            if (w.half >= 0) {
+              go_half = true;
+              break;
+            }
+          } else {
+            ok = __all_sync(0xFFFFFFFFu,
+                            wait_phase<false>(bar_empty + 8 * nst, nph ^ 1u, wc, 0x01 | (nst << 8)));
+          }
+        }
+      } else {
+        while (ok) {
+#pragma unroll
+          for (int st = 0; st < C::STAGES; ++st) {
             if (ok) {
-              __syncwarp();
-              nst = (st + 1 == C::STAGES) ? 0 : st + 1;
-              nph = (st + 1 == C::STAGES) ? (phase ^ 1u) : phase;
-              if (++ks == w.ke) {
-                if (wi.next(w)) {
-                  ks = w.kb;
-                  tile_coords(w.tile, p.m_tiles, p.n_tiles, mt, nt);
-                  if (w.half >= 0) {
-                    go_half = true;
+              if (!__all_sync(0xFFFFFFFFu,
+                              wait_phase<false>(bar_empty + 8 * st, phase ^ 1u, wc, 0x01 | (st << 8)))) {
+                ok = false;
+              } else {
+                if (leader) load_whole(st);
+                __syncwarp();
+                nst = (st + 1 == C::STAGES) ? 0 : st + 1;
+                nph = (st + 1 == C::STAGES) ? (phase ^ 1u) : phase;
+                if (++ks == w.ke) {
+                  if (wi.next(w)) {
+                    ks = w.kb;
+                    tile_coords(w.tile, p.m_tiles, p.n_tiles, mt, nt);
+                    if (w.half >= 0) {
+                      go_half = true;
+                      ok = false;
+                    }
+                  } else {
                     ok = false;
                   }
-                } else {
-                  ok = false;
                 }
               }
             }
           }
+          if (ok) phase ^= 1u;
         }
-        if (ok) phase ^= 1u;
       }
       // half-width tiles: rolled loop, runtime stage index (nst, nph)
       while (go_half) {
@@ -493,68 +547,130 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
         tc_fence_after();
         if (ok) ok = __all_sync(0xFFFFFFFFu, wait_phase<false>(bar_full, 0, wc, 0x03));
       }
-      while (ok) {
+      // one whole-tile K step from stage st (elected lane); returns whether
+      // stage nst (phase nph) is already full, probed after the first MMA
+      auto mma_whole = [&](int st, int nst, uint32_t nph) -> uint32_t {
+        const uint32_t sA = base + C::OFF_A + st * C::A_BYTES;
+        const uint32_t sB = base + C::OFF_B + st * C::B_BYTES;
+        const uint32_t sSA = base + C::OFF_SFA + st * C::SFA_BYTES;
+        const uint32_t sSB = base + C::OFF_SFB + st * C::SFB_BYTES;
+        const uint32_t tSA = tmem + C::TM_SFA + 4 * st;
+        const uint32_t tSB = tmem + C::TM_SFB + 8 * st;
+        // scale chunks: 32 rows x 16 bytes each, no swizzle, 8-row groups 128 B apart
+        tmem_cp_32x128b_x4<CG>(tSA, smem_desc(sSA, 0, 128, 0));
+        tmem_cp_32x128b_x4<CG>(tSB, smem_desc(sSB, 0, 128, 0));
+        tmem_cp_32x128b_x4<CG>(tSB + 4, smem_desc(sSB + 512, 0, 128, 0));
+        // A: K-major, 128-byte swizzle, 8-row groups 1024 B apart; 32 B per K=32.
+        // B: N-major, 128-byte swizzle; 128-column chunks 16 KB apart,
+        // 8-row K groups 1024 B apart; 32 rows (4 KB) per K=32.
+        mma_mxf8<CG>(tmem + C::TM_ACC, smem_desc(sA, 0, 1024, 2), smem_desc(sB, 16384, 1024, 2),
+                     idesc_mxf8(128 * CG, 256, 0, 0), tSA, tSB, ks != w.kb);
+        const uint32_t ready = mbar_test_wait(bar_full + 8 * nst, nph);
 #pragma unroll
-        for (int st = 0; st < C::STAGES; ++st) {
-          if (ok) {
+        for (int k = 1; k < 4; ++k)
+          mma_mxf8<CG>(tmem + C::TM_ACC, smem_desc(sA + 32 * k, 0, 1024, 2),
+                       smem_desc(sB + 4096 * k, 16384, 1024, 2), idesc_mxf8(128 * CG, 256, k, k), tSA,
+                       tSB, 1u);
+        if constexpr (CG == 1) tc_commit(bar_empty + 8 * st);
+        else tc_commit_pair(bar_empty + 8 * st, 0x3);
+        return ready;
+      };
+      if constexpr (CG == 2) {
+        // Pairs: the unrolled loop holds only the per-step work.  A tile
+        // boundary, or a next stage that is not full yet, leaves it for the
+        // code after it (one copy instead of one per stage), which re-enters
+        // the loop at that stage.
+        int skip = 0;  // stages of the current ring round already done
+        while (ok) {
+          int exit_st = -1;  // next stage, when the loop was left early
+          bool tile_end = false;
+#pragma unroll
+          for (int st = 0; st < C::STAGES; ++st) {
+            if (skip > 0) {
+              --skip;
+              continue;
+            }
             // stage st is full
             const int nst = (st + 1 == C::STAGES) ? 0 : st + 1;
             const uint32_t nph = (st + 1 == C::STAGES) ? (phase ^ 1u) : phase;
             uint32_t next_ready = 0;
-            if (leader) {
-              const uint32_t sA = base + C::OFF_A + st * C::A_BYTES;
-              const uint32_t sB = base + C::OFF_B + st * C::B_BYTES;
-              const uint32_t sSA = base + C::OFF_SFA + st * C::SFA_BYTES;
-              const uint32_t sSB = base + C::OFF_SFB + st * C::SFB_BYTES;
-              const uint32_t tSA = tmem + C::TM_SFA + 4 * st;
-              const uint32_t tSB = tmem + C::TM_SFB + 8 * st;
-              // scale chunks: 32 rows x 16 bytes each, no swizzle, 8-row groups 128 B apart
-              tmem_cp_32x128b_x4<CG>(tSA, smem_desc(sSA, 0, 128, 0));
-              tmem_cp_32x128b_x4<CG>(tSB, smem_desc(sSB, 0, 128, 0));
-              tmem_cp_32x128b_x4<CG>(tSB + 4, smem_desc(sSB + 512, 0, 128, 0));
-              // A: K-major, 128-byte swizzle, 8-row groups 1024 B apart; 32 B per K=32.
-              // B: N-major, 128-byte swizzle; 128-column chunks 16 KB apart,
-              // 8-row K groups 1024 B apart; 32 rows (4 KB) per K=32.
-              mma_mxf8<CG>(tmem + C::TM_ACC, smem_desc(sA, 0, 1024, 2), smem_desc(sB, 16384, 1024, 2),
-                           idesc_mxf8(128 * CG, 256, 0, 0), tSA, tSB, ks != w.kb);
-              next_ready = mbar_test_wait(bar_full + 8 * nst, nph);
-#pragma unroll
-              for (int k = 1; k < 4; ++k)
-                mma_mxf8<CG>(tmem + C::TM_ACC, smem_desc(sA + 32 * k, 0, 1024, 2),
-                             smem_desc(sB + 4096 * k, 16384, 1024, 2),
-                             idesc_mxf8(128 * CG, 256, k, k), tSA, tSB, 1u);
-              if constexpr (CG == 1) tc_commit(bar_empty + 8 * st);
-              else tc_commit_pair(bar_empty + 8 * st, 0x3);
-            }
+            if (leader) next_ready = mma_whole(st, nst, nph);
             __syncwarp();
             next_ready = __shfl_sync(0xFFFFFFFFu, next_ready, __ffs(__ballot_sync(0xFFFFFFFFu, leader)) - 1);
             if (++ks == w.ke) {
-              if (leader) {
-                if constexpr (CG == 1) tc_commit(bar_acc_full);
-                else tc_commit_pair(bar_acc_full, 0x3);
-              }
-              __syncwarp();
-              acc_phase ^= 1u;
-              if (!wi.next(w)) {
-                ok = false;
-              } else if (w.half >= 0) {
-                go_half = true;
-                hst = nst;
-                hph = nph;
-                ok = false;
-              } else {
-                ks = w.kb;
-                ok = __all_sync(0xFFFFFFFFu, wait_phase<CL>(bar_acc_empty, acc_phase ^ 1u, wc,
-                                                            0x02 | ((w.tile & 0xFFFF) << 16)));
-                if (ok) tc_fence_after();
-              }
+              tile_end = true;
+              exit_st = nst;
+              break;
             }
-            if (ok && !next_ready)
-              ok = __all_sync(0xFFFFFFFFu,
-                              wait_phase<false>(bar_full + 8 * nst, nph, wc, 0x03 | (nst << 8)));
+            if (!next_ready) {
+              exit_st = nst;
+              break;
+            }
           }
+          if (exit_st < 0) {  // a whole ring round
+            phase ^= 1u;
+            continue;
+          }
+          if (exit_st == 0) phase ^= 1u;  // the round ended with its last stage
+          skip = exit_st;
+          if (tile_end) {
+            if (leader) tc_commit_pair(bar_acc_full, 0x3);
+            __syncwarp();
+            acc_phase ^= 1u;
+            if (!wi.next(w)) break;
+            if (w.half >= 0) {
+              go_half = true;
+              hst = exit_st;
+              hph = phase;
+              break;
+            }
+            ks = w.kb;
+            ok = __all_sync(0xFFFFFFFFu, wait_phase<CL>(bar_acc_empty, acc_phase ^ 1u, wc,
+                                                        0x02 | ((w.tile & 0xFFFF) << 16)));
+            if (!ok) break;
+            tc_fence_after();
+          }
+          ok = __all_sync(0xFFFFFFFFu,
+                          wait_phase<false>(bar_full + 8 * exit_st, phase, wc, 0x03 | (exit_st << 8)));
         }
-        if (ok) phase ^= 1u;
+      } else {
+        while (ok) {
+#pragma unroll
+          for (int st = 0; st < C::STAGES; ++st) {
+            if (ok) {
+              // stage st is full
+              const int nst = (st + 1 == C::STAGES) ? 0 : st + 1;
+              const uint32_t nph = (st + 1 == C::STAGES) ? (phase ^ 1u) : phase;
+              uint32_t next_ready = 0;
+              if (leader) next_ready = mma_whole(st, nst, nph);
+              __syncwarp();
+              next_ready =
+                  __shfl_sync(0xFFFFFFFFu, next_ready, __ffs(__ballot_sync(0xFFFFFFFFu, leader)) - 1);
+              if (++ks == w.ke) {
+                if (leader) tc_commit(bar_acc_full);
+                __syncwarp();
+                acc_phase ^= 1u;
+                if (!wi.next(w)) {
+                  ok = false;
+                } else if (w.half >= 0) {
+                  go_half = true;
+                  hst = nst;
+                  hph = nph;
+                  ok = false;
+                } else {
+                  ks = w.kb;
+                  ok = __all_sync(0xFFFFFFFFu, wait_phase<CL>(bar_acc_empty, acc_phase ^ 1u, wc,
+                                                              0x02 | ((w.tile & 0xFFFF) << 16)));
+                  if (ok) tc_fence_after();
+                }
+              }
+              if (ok && !next_ready)
+                ok = __all_sync(0xFFFFFFFFu,
+                                wait_phase<false>(bar_full + 8 * nst, nph, wc, 0x03 | (nst << 8)));
+            }
+          }
+          if (ok) phase ^= 1u;
+        }
       }
       // Half-width tiles: N = 128 MMAs; B scales are the matching 128-row
       // half of the 256-column chunk.  Pairs hold 64 B columns per CTA
