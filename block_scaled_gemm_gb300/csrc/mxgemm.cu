@@ -238,7 +238,7 @@ struct Split {
   int half_tiles;      // half-width items after the whole tiles (2 per leftover tile)
 };
 
-Split plan_split(int64_t T, int64_t S, int P, bool allow_tail) {
+Split plan_split(int64_t T, int64_t S, int P, bool allow_tail, bool allow_stream_k) {
   Split r;
   r.units = static_cast<int>(T < P ? T : P);
   r.dp_tiles = static_cast<int>(T);
@@ -252,7 +252,7 @@ Split plan_split(int64_t T, int64_t S, int P, bool allow_tail) {
   // that stream-K pays off only with long K (64+ steps) after 1 to 8 full
   // waves, and not when the last wave is nearly full; in particular not when
   // every tile would be split (fewer tiles than CTAs).
-  if (S >= 64 && W >= 1 && W <= 8 && R * 100 < static_cast<int64_t>(P) * 85) {
+  if (allow_stream_k && S >= 64 && W >= 1 && W <= 8 && R * 100 < static_cast<int64_t>(P) * 85) {
     const int64_t tail = R * S;
     int64_t ctas = tail / 4;  // at least 4 K steps per CTA
     if (ctas > P) ctas = P;
@@ -508,7 +508,12 @@ int mxgemm_run(mxgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A
   const int64_t b_chunks = n_tiles * k_steps * 2;   // 2 per 256 columns
   const bool pad_b = (N % 16) != 0;
   const int64_t npad = round_up(static_cast<size_t>(N), 16);
-  const Split sp = plan_split(num_tiles, k_steps, h->sm_count / CG, h->stream_k != 0);
+  // Cluster launch control: one cluster per work item (whole tiles, then
+  // half-width items), handed out by the hardware; no stream-K, whose
+  // partial-sum slots belong to fixed CTAs.
+  const bool clc = h->scheduler == 1;
+  Split sp = plan_split(num_tiles, k_steps, h->sm_count / CG, h->stream_k != 0, !clc);
+  if (clc) sp.units = sp.dp_tiles + sp.half_tiles;
   const Sizes z = plan_sizes(a_chunks, b_chunks, pad_b, K, npad, sp, CG);
   const size_t off_b = z.off_b;
   const size_t ws_bytes = z.total;
@@ -717,7 +722,7 @@ extern "C" int mxgemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A
   const bool pad_b = (N % 16) != 0;
   const int64_t npad = round_up(static_cast<size_t>(N), 16);
   // no stream-K split here: the scratch holds only the repacked scales and B
-  const Split sp = plan_split(num_tiles, k_steps, nd->sm_count / CG, false);
+  const Split sp = plan_split(num_tiles, k_steps, nd->sm_count / CG, false, false);
   const Sizes z = plan_sizes(a_chunks, b_chunks, pad_b, K, npad, sp, CG);
   const size_t off_b = z.off_b;
   const size_t ws_bytes = z.total;

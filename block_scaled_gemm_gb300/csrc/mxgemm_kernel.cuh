@@ -61,8 +61,11 @@ struct Cfg {
   static constexpr int OFF_SFA = OFF_B + STAGES * B_BYTES;
   static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
   static constexpr int OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;
-  static constexpr int NUM_BARS = 2 * STAGES + 3;  // full[], empty[], acc_full, acc_empty, final
-  static constexpr int OFF_MISC = OFF_BAR + NUM_BARS * 8;
+  static constexpr int CLC_SLOTS = 4;  // cluster-launch-control response ring
+  // full[], empty[], acc_full, acc_empty, final, clc_full[], clc_empty[]
+  static constexpr int NUM_BARS = 2 * STAGES + 3 + 2 * CLC_SLOTS;
+  static constexpr int OFF_CLC = (OFF_BAR + NUM_BARS * 8 + 15) / 16 * 16;  // 16-byte responses
+  static constexpr int OFF_MISC = OFF_CLC + 16 * CLC_SLOTS;
   // epilogue staging: one 32-row x 64-byte buffer per epilogue warp
   static constexpr int EPI_BUF = 2048;
   static constexpr int OFF_EPI = (OFF_MISC + 16 + 1023) / 1024 * 1024;
@@ -76,6 +79,7 @@ struct Cfg {
   static_assert(TM_SFB + 8 * STAGES <= (int)TM_COLS, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(OFF_B % 1024 == 0 && A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "align");
+  static_assert(OFF_BAR % 8 == 0 && OFF_CLC % 16 == 0, "barrier and response alignment");
 };
 
 struct KParams {
@@ -156,6 +160,22 @@ struct WorkItem {
   int half;           // -1: all 256 columns; 0 / 1: only that 128-column half
 };
 
+// Item t of the whole-tile walk: t < dp_tiles is tile t; the items after
+// them are the 128-column halves of tiles dp_tiles, dp_tiles + 1, ...
+__device__ __forceinline__ void item_to_work(int t, int dp_tiles, int k_steps, WorkItem &w) {
+  w.kb = 0;
+  w.ke = k_steps;
+  w.kind = kFull;
+  w.first_contrib = 0;
+  if (t < dp_tiles) {
+    w.tile = t;
+    w.half = -1;
+  } else {
+    w.tile = dp_tiles + ((t - dp_tiles) >> 1);
+    w.half = (t - dp_tiles) & 1;
+  }
+}
+
 struct WorkIter {
   int u, P, dp_tiles, k_steps, sk_ctas, half_tiles;
   long long sk_units;
@@ -192,17 +212,7 @@ struct WorkIter {
     const int t = u + i * P;
     if (t >= dp_tiles + half_tiles) return false;
     ++i;
-    w.kb = 0;
-    w.ke = k_steps;
-    w.kind = kFull;
-    w.first_contrib = u;
-    if (t < dp_tiles) {
-      w.tile = t;
-      w.half = -1;
-    } else {
-      w.tile = dp_tiles + ((t - dp_tiles) >> 1);
-      w.half = (t - dp_tiles) & 1;
-    }
+    item_to_work(t, dp_tiles, k_steps, w);
     return true;
   }
 };
@@ -263,6 +273,101 @@ __device__ __forceinline__ bool wait_flag(const int *flag, int target, const Wai
   }
 }
 
+// ---------------------------------------------------------------------------
+// Work source under cluster launch control ("TLX API Quick Reference",
+// section "CLC (Cluster Launch Control)").  The grid has one cluster per
+// work item.  A resident cluster first takes its own item, then asks the
+// hardware to cancel a cluster that has not launched yet and takes that
+// cluster's item instead, until none is left to cancel.  The leader CTA's
+// producer warp issues each request one item ahead, in the multicast form:
+// the 16-byte response and its byte count land in every CTA of the cluster.
+// Every role of every CTA reads the responses in order from a ring of
+// CLC_SLOTS slots; the leader reuses a slot only after all readers released
+// it (producer, MMA issuer and 8 epilogue warps in the leader, producer and
+// 8 epilogue warps in the peer).  At most one request is outstanding, so none
+// is issued after the one that found no cluster left.
+struct ClcRing {
+  uint32_t resp;       // response slot 0 (16 bytes per slot)
+  uint32_t full;       // per-slot barrier: the response has landed in this CTA
+  uint32_t empty;      // per-slot barrier of the leader CTA: readers done
+  int slot = 0;        // next slot to read, and its ring phase
+  uint32_t phase = 0;
+  int rslot = 0;       // next slot to request into (leader's producer)
+  uint32_t rphase = 0;
+  bool first = true;   // the cluster's own item has not been taken yet
+};
+
+// Whole-warp call.  Returns the next item, -1 when no work is left, -2 on a
+// timed-out wait (status recorded).
+template <int CG, int SLOTS>
+__device__ __noinline__ int clc_fetch(ClcRing &r, bool requester, uint32_t rank, const WaitCtl &wc) {
+  const int lane = threadIdx.x & 31;
+  int t;
+  if (r.first) {
+    r.first = false;
+    t = static_cast<int>(blockIdx.x) / CG;
+  } else {
+    if (!__all_sync(0xFFFFFFFFu, wait_phase<false>(r.full + 8 * r.slot, r.phase, wc, 0x07 | (r.slot << 8))))
+      return -2;
+    const int x = clc_decode_x(r.resp + 16 * r.slot);
+    __syncwarp();
+    if (lane == 0) {
+      if constexpr (CG == 1) mbar_arrive(r.empty + 8 * r.slot);
+      else mbar_arrive_cluster(r.empty + 8 * r.slot, 0);
+    }
+    if (++r.slot == SLOTS) {
+      r.slot = 0;
+      r.phase ^= 1u;
+    }
+    if (x < 0) return -1;
+    t = x / CG;
+  }
+  if (requester) {
+    // the item after this one; each CTA expects the 16 response bytes on
+    // its own barrier, the leader issues the request once the slot is free
+    if (lane == 0) mbar_arrive_expect_tx(r.full + 8 * r.rslot, 16);
+    if (rank == 0) {
+      if (!__all_sync(0xFFFFFFFFu,
+                      wait_phase<false>(r.empty + 8 * r.rslot, r.rphase ^ 1u, wc, 0x08 | (r.rslot << 8))))
+        return -2;
+      if (lane == 0) {
+        if constexpr (CG == 1) clc_try_cancel(r.resp + 16 * r.rslot, r.full + 8 * r.rslot);
+        else clc_try_cancel_all(r.resp + 16 * r.rslot, r.full + 8 * r.rslot);
+      }
+      __syncwarp();
+    }
+    if (++r.rslot == SLOTS) {
+      r.rslot = 0;
+      r.rphase ^= 1u;
+    }
+  }
+  return t;
+}
+
+// The work source of one role: the static walk, or cluster launch control
+// (whose ring position lives in the caller's ClcRing; the static walk's
+// state stays in registers).
+template <int CG, int SLOTS>
+struct Sched {
+  WorkIter wi;
+  ClcRing *clc;
+  const WaitCtl *wc;
+  int dp_tiles, k_steps;
+  bool use_clc, requester;
+  uint32_t rank;
+  __device__ Sched(const KParams &p, int u, int P, ClcRing *r, bool req, uint32_t rk,
+                   const WaitCtl *w)
+      : wi(p, u, P), clc(r), wc(w), dp_tiles(p.dp_tiles), k_steps(p.k_steps),
+        use_clc(p.use_clc != 0), requester(req), rank(rk) {}
+  __device__ bool next(WorkItem &w) {
+    if (!use_clc) return wi.next(w);
+    const int t = clc_fetch<CG, SLOTS>(*clc, requester, rank, *wc);
+    if (t < 0) return false;
+    item_to_work(t, dp_tiles, k_steps, w);
+    return true;
+  }
+};
+
 template <int CG, int EPI>
 __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
     mxgemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -288,6 +393,8 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
   const uint32_t bar_acc_full = bar_empty + 8 * C::STAGES;
   const uint32_t bar_acc_empty = bar_acc_full + 8;
   const uint32_t bar_final = bar_acc_empty + 8;
+  const uint32_t bar_clc_full = bar_final + 8;
+  const uint32_t bar_clc_empty = bar_clc_full + 8 * C::CLC_SLOTS;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + C::OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + C::OFF_MISC + 4);
 
@@ -299,6 +406,11 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
     mbar_init(bar_acc_full, 1);
     mbar_init(bar_acc_empty, C::EPI_WARPS * CG);
     mbar_init(bar_final, 1);
+    for (int s = 0; s < C::CLC_SLOTS; ++s) {
+      mbar_init(bar_clc_full + 8 * s, 1);
+      // readers of a response: producer + 8 epilogue warps per CTA, and the MMA issuer
+      mbar_init(bar_clc_empty + 8 * s, (1 + C::EPI_WARPS) * CG + 1);
+    }
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -332,6 +444,10 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
   constexpr bool CL = (CG == 2);
   const int unit = blockIdx.x / CG;    // this CTA's (pair's) index in the persistent grid
   const int units = gridDim.x / CG;
+  ClcRing clc_ring;
+  clc_ring.resp = base + C::OFF_CLC;
+  clc_ring.full = bar_clc_full;
+  clc_ring.empty = bar_clc_empty;
 
   // The producer and MMA loops are unrolled over the ring stages: with the
   // stage index a compile-time constant every shared-memory address, TMEM
@@ -349,7 +465,8 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
       uint32_t phase = 0;
       int nst = 0;           // next stage to fill ...
       uint32_t nph = 0;      // ... and the ring phase it belongs to
-      WorkIter wi(p, unit, units);
+      ClcRing ring = clc_ring;
+      Sched<CG, C::CLC_SLOTS> wi(p, unit, units, &ring, true, rank, &wc);
       WorkItem w;
       bool ok = !p.stall_producer && wi.next(w);
       int ks = w.kb, mt = 0, nt = 0;
@@ -529,7 +646,8 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
     if (rank == 0) {
       const bool leader = elect_one() != 0;
       uint32_t phase = 0, acc_phase = 0;
-      WorkIter wi(p, unit, units);
+      ClcRing ring = clc_ring;
+      Sched<CG, C::CLC_SLOTS> wi(p, unit, units, &ring, false, rank, &wc);
       WorkItem w;
       bool ok = wi.next(w);
       int ks = w.kb;
@@ -744,7 +862,8 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
     const int q = warp & 3;   // TMEM lane quarter this warp may access
     const int h = ew >> 2;    // which half of the tile's columns
     uint32_t acc_phase = 0;
-    WorkIter wi(p, unit, units);
+    ClcRing ring = clc_ring;
+    Sched<CG, C::CLC_SLOTS> wi(p, unit, units, &ring, false, rank, &wc);
     WorkItem w;
     while (wi.next(w)) {
       const int t = w.tile;

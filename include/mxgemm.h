@@ -77,14 +77,19 @@ typedef enum {
    * of the next launches issues no loads, so the consumer waits run out and
    * the kernel reports MXGEMM_ERR_TIMEOUT.  Default 0. */
   MXGEMM_OPT_TEST_STALL_PRODUCER = 3,
-  /* Persistent tile scheduler: 0 = static striding over a grid of one CTA
-   * (pair) per SM, 1 = cluster launch control (grid of all tiles; running
-   * CTAs cancel not-yet-launched ones and take their tiles).  Default 0. */
+  /* Tile scheduler: 0 = static striding over a persistent grid of one CTA
+   * (pair) per SM; 1 = cluster launch control ("TLX API Quick Reference",
+   * section "CLC (Cluster Launch Control)"): the grid has one cluster per
+   * work item, and running clusters cancel clusters that have not launched
+   * yet and take their items (no stream-K tail under this scheduler).
+   * Default 0. */
   MXGEMM_OPT_SCHEDULER = 4,
-  /* Stream-K tail: 1 (default) lets the persistent grid split the K steps
-   * of the tiles left over after the last full wave evenly over all CTAs,
-   * one CTA per tile adding the others' FP32 partials (kept in the handle's
-   * workspace) before it stores C; 0 computes every tile whole. */
+  /* Balancing of the tiles left over after the last full wave.  1
+   * (default): with long K (64+ steps of 128) their K steps are split
+   * evenly over all CTAs (stream-K), one CTA per tile adding the others'
+   * FP32 partials (kept in the handle's workspace) before it stores C;
+   * otherwise, when they fill at most half a wave, each is computed as two
+   * 128-column halves.  0: every tile is computed whole. */
   MXGEMM_OPT_STREAM_K = 5
 } mxgemm_option_t;
 

@@ -276,3 +276,53 @@ def test_half_width_only(h, mode):
     _mode(h, mode)
     p = mi.random_problem(2000, 1000, 256, seed=61 + mode, kind="normal", out_dtype="f32")
     gu.check_full(h, p)
+
+
+CLC_CASES = [
+    # (M, N, K, out_dtype, use_acc): fewer clusters than fit (no cancel succeeds),
+    # many more (most items taken by cancelling), a half-width tail, ragged edges
+    (256, 256, 4096, "f32", False),
+    (4096, 4096, 1024, "f32", False),
+    (2560, 3976, 512, "bf16", False),
+    (1000, 1000, 1024, "f32", True),
+]
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("case", CLC_CASES, ids=lambda c: "x".join(map(str, c[:3])) + f"-{c[3]}-acc{int(c[4])}")
+def test_clc_scheduler(h, mode, case):
+    # Cluster launch control: one cluster per work item, the running ones
+    # cancel launches and take their items.  Checked against the oracle on
+    # whole rows spread over the tiles, and bit for bit against the static
+    # schedule (each tile is computed by one CTA or pair either way).
+    M, N, K, out_dtype, use_acc = case
+    _mode(h, mode)
+    p = mi.random_problem(M, N, K, seed=71 + mode + M, kind="normal", out_dtype=out_dtype)
+    cin = mi.c_init(M, N, 71, out_dtype) if use_acc else None
+    rows = np.unique(np.linspace(0, M - 1, 24).astype(int))
+    ref, bound = oracle.rows(p.A, p.As, p.B, p.Bs, rows=rows,
+                             c_in=None if cin is None else cin.to(torch.float64).numpy()[rows])
+    outs = {}
+    try:
+        for sched in (1, 0):
+            mx.mxgemm_set_option(h, mx.OPT_SCHEDULER, sched)
+            C = gu.run_gpu(h, p, c_init=cin, use_acc=use_acc)
+            outs[sched] = gu.to_numpy_out(C, out_dtype)
+            res = oracle.accept(outs[sched][rows], ref, bound, out_dtype)
+            assert res["ok"], f"scheduler={sched}: {res}"
+    finally:
+        mx.mxgemm_set_option(h, mx.OPT_SCHEDULER, 0)
+    assert np.array_equal(outs[0].view(np.uint32) if out_dtype == "f32" else outs[0],
+                          outs[1].view(np.uint32) if out_dtype == "f32" else outs[1])
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+def test_clc_scheduler_full_check(h, mode):
+    # every element of a problem whose items are mostly taken by cancelling
+    _mode(h, mode)
+    p = mi.random_problem(1536, 2304, 256, seed=81 + mode, kind="normal", out_dtype="f32")
+    try:
+        mx.mxgemm_set_option(h, mx.OPT_SCHEDULER, 1)
+        gu.check_full(h, p)
+    finally:
+        mx.mxgemm_set_option(h, mx.OPT_SCHEDULER, 0)
