@@ -25,7 +25,7 @@ __all__ = [
     "OUT_F32", "OUT_BF16", "OPT_MODE", "OPT_WAIT_TIMEOUT_NS", "OPT_TEST_STALL_PRODUCER",
     "OPT_SCHEDULER", "OPT_STREAM_K", "MxgemmError", "library", "library_path", "mxgemm_create", "mxgemm_run",
     "mxgemm_destroy", "mxgemm_set_option", "mxgemm_get_device_status", "mxgemm_status_string",
-    "mxgemm_set_profile_events", "mxgemm_get_launch_count", "mxgemm_run_noalloc",
+    "mxgemm_set_profile_events", "mxgemm_get_launch_count", "mxgemm_run_noalloc", "mxgemm_run_host",
     "EXPORTED_SYMBOLS", "Gemm",
 ]
 
@@ -50,7 +50,7 @@ ERR_TOO_LARGE = 7
 EXPORTED_SYMBOLS = (
     "mxgemm_create", "mxgemm_run", "mxgemm_destroy", "mxgemm_set_option",
     "mxgemm_get_device_status", "mxgemm_status_string", "mxgemm_set_profile_events",
-    "mxgemm_get_launch_count", "mxgemm_run_noalloc",
+    "mxgemm_get_launch_count", "mxgemm_run_noalloc", "mxgemm_run_host",
 )
 
 _lib = None
@@ -91,6 +91,8 @@ def library():
         lib.mxgemm_set_profile_events.restype = i32
         lib.mxgemm_get_launch_count.argtypes = [vp, ctypes.POINTER(i64)]
         lib.mxgemm_get_launch_count.restype = i32
+        lib.mxgemm_run_host.argtypes = [vp, i64, i64, i64, vp, vp, vp, vp, vp, i32, i32, vp]
+        lib.mxgemm_run_host.restype = i32
         lib.mxgemm_run_noalloc.argtypes = [i64, i64, i64, vp, vp, vp, vp, vp, i32, i32, vp]
         lib.mxgemm_run_noalloc.restype = i32
         lib.mxgemm_status_string.argtypes = [i32]
@@ -137,6 +139,19 @@ def mxgemm_run(h, M, N, K, A, A_scale, B, B_scale, C, use_acc=0, out_dtype=OUT_F
                               _stream(stream))
     if check:
         _check(st, "mxgemm_run")
+    return st
+
+
+def mxgemm_run_host(h, M, N, K, A, A_scale, B, B_scale, C, use_acc=0, out_dtype=OUT_F32,
+                    stream=None, check: bool = True) -> int:
+    """C (+)= A.B with every operand and C in host memory (CPU tensors,
+    contiguous; pinned ones let the copies overlap the GEMM).  C is complete
+    once `stream` is synchronized (see include/mxgemm.h)."""
+    st = library().mxgemm_run_host(h, int(M), int(N), int(K), _ptr(A), _ptr(A_scale), _ptr(B),
+                                   _ptr(B_scale), _ptr(C), int(bool(use_acc)), int(out_dtype),
+                                   _stream(stream))
+    if check:
+        _check(st, "mxgemm_run_host")
     return st
 
 

@@ -64,6 +64,18 @@ struct Plan {
 
 constexpr int kPlanCache = 8;
 
+// Copy streams, events and device staging of mxgemm_run_host.
+struct HostPipe {
+  bool ready = false;
+  cudaStream_t h2d = nullptr, d2h = nullptr;
+  cudaEvent_t start = nullptr;      // the caller's stream reached the call
+  cudaEvent_t b_ready = nullptr;    // B and its scales are on the device
+  cudaEvent_t in_ready[2] = {};     // slot s holds its slab's inputs
+  cudaEvent_t gemm_done[2] = {};    // slot s's GEMM has finished
+  cudaEvent_t out_done[2] = {};     // slot s's C rows are back on the host
+  Workspace stage;
+};
+
 }  // namespace
 
 struct mxgemm_ctx {
@@ -83,6 +95,7 @@ struct mxgemm_ctx {
   int64_t launches = 0;
   Plan plans[kPlanCache];
   int next_plan = 0;
+  HostPipe hp;
 };
 
 namespace {
@@ -591,12 +604,187 @@ int mxgemm_destroy(mxgemm_handle_t h) {
     cudaDeviceSynchronize();
     if (h->ws.ptr) cudaFree(h->ws.ptr);
     if (h->d_status) cudaFree(h->d_status);
+    HostPipe &hp = h->hp;
+    if (hp.stage.ptr) cudaFree(hp.stage.ptr);
+    for (cudaEvent_t e : {hp.start, hp.b_ready, hp.in_ready[0], hp.in_ready[1], hp.gemm_done[0],
+                          hp.gemm_done[1], hp.out_done[0], hp.out_done[1]})
+      if (e) cudaEventDestroy(e);
+    if (hp.h2d) cudaStreamDestroy(hp.h2d);
+    if (hp.d2h) cudaStreamDestroy(hp.d2h);
   }
   delete h;
   return MXGEMM_OK;
 }
 
 }  // extern "C"
+
+// ===========================================================================
+// mxgemm_run_host: operands and result in host memory.
+//
+// B and its scales go to the device first; then the rows of A (and of C)
+// move in slabs through two device slots, so that a slab's GEMM overlaps the
+// next slab's copy in and the previous slab's copy out.  The GEMM of a slab
+// is an ordinary mxgemm_run on the slot's buffers.
+// ===========================================================================
+
+namespace {
+
+int host_pipe_init(mxgemm_ctx *h) {
+  HostPipe &hp = h->hp;
+  if (hp.ready) return MXGEMM_OK;
+  if (cudaStreamCreateWithFlags(&hp.h2d, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaStreamCreateWithFlags(&hp.d2h, cudaStreamNonBlocking) != cudaSuccess) {
+    cudaGetLastError();
+    return MXGEMM_ERR_CUDA;
+  }
+  cudaEvent_t *evs[] = {&hp.start,        &hp.b_ready,      &hp.in_ready[0], &hp.in_ready[1],
+                        &hp.gemm_done[0], &hp.gemm_done[1], &hp.out_done[0], &hp.out_done[1]};
+  for (cudaEvent_t *e : evs)
+    if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) {
+      cudaGetLastError();
+      return MXGEMM_ERR_CUDA;
+    }
+  hp.ready = true;
+  return MXGEMM_OK;
+}
+
+int ensure_stage(mxgemm_ctx *h, size_t bytes, cudaStream_t stream) {
+  Workspace &w = h->hp.stage;
+  if (w.bytes >= bytes) return MXGEMM_OK;
+  if (w.ptr) {
+    // every earlier use is ordered before this point of `stream`
+    cudaFreeAsync(w.ptr, stream);
+    w.ptr = nullptr;
+    w.bytes = 0;
+  }
+  void *p = nullptr;
+  const size_t want = round_up(bytes, size_t(2) << 20);
+  if (cudaMallocAsync(&p, want, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return MXGEMM_ERR_OUT_OF_MEMORY;
+  }
+  w.ptr = static_cast<uint8_t *>(p);
+  w.bytes = want;
+  return MXGEMM_OK;
+}
+
+// one asynchronous copy; false when it could not be enqueued
+bool copy_async(void *dst, const void *src, size_t bytes, cudaMemcpyKind kind, cudaStream_t s) {
+  if (bytes == 0) return true;
+  if (cudaMemcpyAsync(dst, src, bytes, kind, s) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return true;
+}
+
+bool wait_event(cudaStream_t s, cudaEvent_t e) {
+  if (cudaStreamWaitEvent(s, e, 0) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return true;
+}
+
+bool record_event(cudaEvent_t e, cudaStream_t s) {
+  if (cudaEventRecord(e, s) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return true;
+}
+
+}  // namespace
+
+extern "C" int mxgemm_run_host(mxgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A,
+                               const void *A_scale, const void *B, const void *B_scale, void *C,
+                               int use_acc, int out_dtype, mxgemm_stream_t stream_) {
+  if (!h) return MXGEMM_ERR_INVALID_VALUE;
+  const int64_t lim = int64_t(1) << 31;
+  if (M < 0 || N < 0 || K < 0 || M >= lim || N >= lim || K >= lim) return MXGEMM_ERR_INVALID_VALUE;
+  if (K % 32 != 0) return MXGEMM_ERR_INVALID_VALUE;
+  if (out_dtype != MXGEMM_OUT_F32 && out_dtype != MXGEMM_OUT_BF16) return MXGEMM_ERR_INVALID_VALUE;
+  if (use_acc != 0 && use_acc != 1) return MXGEMM_ERR_INVALID_VALUE;
+  if (M == 0 || N == 0) return MXGEMM_OK;
+  if (!C) return MXGEMM_ERR_INVALID_VALUE;
+  const size_t esz = out_dtype == MXGEMM_OUT_F32 ? 4 : 2;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  DeviceGuard g(h->device);
+  if (K == 0) {
+    if (use_acc) return MXGEMM_OK;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) {
+      cudaGetLastError();
+      return MXGEMM_ERR_CUDA;
+    }
+    std::memset(C, 0, static_cast<size_t>(M) * N * esz);
+    return MXGEMM_OK;
+  }
+  if (!A || !B || !A_scale || !B_scale) return MXGEMM_ERR_INVALID_VALUE;
+
+  int st = host_pipe_init(h);
+  if (st != MXGEMM_OK) return st;
+  HostPipe &hp = h->hp;
+  const int64_t kb = K / 32;
+  // slab rows: about 8 slabs, whole 256-row pair tiles, at least 256 rows
+  int64_t ms = round_up(static_cast<size_t>(cdiv(M, 8)), 256);
+  if (ms < 256) ms = 256;
+  if (ms > M) ms = M;
+  const int64_t nslab = cdiv(M, ms);
+  const size_t b_bytes = static_cast<size_t>(K) * N, bs_bytes = static_cast<size_t>(N) * kb;
+  const size_t a_bytes = static_cast<size_t>(ms) * K, as_bytes = static_cast<size_t>(ms) * kb;
+  const size_t c_bytes = static_cast<size_t>(ms) * N * esz;
+  const size_t off_bs = round_up(b_bytes, 256);
+  const size_t off_slot = round_up(off_bs + bs_bytes, 256);
+  const size_t off_as = round_up(a_bytes, 256);
+  const size_t off_c = round_up(off_as + as_bytes, 256);
+  const size_t slot_bytes = round_up(off_c + c_bytes, 256);
+  st = ensure_stage(h, off_slot + 2 * slot_bytes, stream);
+  if (st != MXGEMM_OK) return st;
+  uint8_t *base = hp.stage.ptr;
+  const uint8_t *hA = static_cast<const uint8_t *>(A), *hAs = static_cast<const uint8_t *>(A_scale);
+  uint8_t *hC = static_cast<uint8_t *>(C);
+
+  // the copy streams start where the caller's stream is
+  if (!record_event(hp.start, stream) || !wait_event(hp.h2d, hp.start) || !wait_event(hp.d2h, hp.start))
+    return MXGEMM_ERR_CUDA;
+  if (!copy_async(base, B, b_bytes, cudaMemcpyHostToDevice, hp.h2d) ||
+      !copy_async(base + off_bs, B_scale, bs_bytes, cudaMemcpyHostToDevice, hp.h2d) ||
+      !record_event(hp.b_ready, hp.h2d))
+    return MXGEMM_ERR_CUDA;
+  for (int64_t j = 0; j < nslab; ++j) {
+    const int s = static_cast<int>(j & 1);
+    const int64_t m0 = j * ms, mj = (M - m0 < ms) ? M - m0 : ms;
+    uint8_t *dA = base + off_slot + s * slot_bytes;
+    uint8_t *dAs = dA + off_as;
+    uint8_t *dC = dA + off_c;
+    const size_t crow = static_cast<size_t>(N) * esz;
+    // inputs of slab j into slot s, once slab j-2's GEMM (and, when C is
+    // read, its copy out) no longer needs the slot
+    if (j >= 2 && (!wait_event(hp.h2d, hp.gemm_done[s]) || (use_acc && !wait_event(hp.h2d, hp.out_done[s]))))
+      return MXGEMM_ERR_CUDA;
+    if (!copy_async(dA, hA + m0 * K, static_cast<size_t>(mj) * K, cudaMemcpyHostToDevice, hp.h2d) ||
+        !copy_async(dAs, hAs + m0 * kb, static_cast<size_t>(mj) * kb, cudaMemcpyHostToDevice, hp.h2d) ||
+        (use_acc && !copy_async(dC, hC + m0 * crow, mj * crow, cudaMemcpyHostToDevice, hp.h2d)) ||
+        !record_event(hp.in_ready[s], hp.h2d))
+      return MXGEMM_ERR_CUDA;
+    // the GEMM of slab j on the caller's stream
+    if (!wait_event(stream, hp.in_ready[s]) || (j == 0 && !wait_event(stream, hp.b_ready)) ||
+        (j >= 2 && !wait_event(stream, hp.out_done[s])))
+      return MXGEMM_ERR_CUDA;
+    st = mxgemm_run(h, mj, N, K, dA, dAs, base, base + off_bs, dC, use_acc, out_dtype, stream);
+    if (st != MXGEMM_OK) return st;
+    if (!record_event(hp.gemm_done[s], stream)) return MXGEMM_ERR_CUDA;
+    // its C rows back to the host
+    if (!wait_event(hp.d2h, hp.gemm_done[s]) ||
+        !copy_async(hC + m0 * crow, dC, mj * crow, cudaMemcpyDeviceToHost, hp.d2h) ||
+        !record_event(hp.out_done[s], hp.d2h))
+      return MXGEMM_ERR_CUDA;
+  }
+  // the caller's stream completes once every slab is back
+  if (!wait_event(stream, hp.out_done[0]) || (nslab > 1 && !wait_event(stream, hp.out_done[1])))
+    return MXGEMM_ERR_CUDA;
+  return MXGEMM_OK;
+}
 
 // ===========================================================================
 // mxgemm_run_noalloc: the same product without any device allocation.
