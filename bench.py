@@ -47,6 +47,7 @@ UNIT = "TFLOP/s"
 WORKLOAD = "square_4096"
 FP8_OVER_BF16 = 2.0  # nominal dense MXFP8 / BF16 tensor rate (4.5 / 2.25 PFLOP/s)
 FALLBACK_BF16_BURST = 1900.0  # TFLOP/s, used only when MEASURED_PEAKS.json is absent
+FALLBACK_HBM_GBS = 6800.0     # GB/s, used only when MEASURED_PEAKS.json is absent
 KERNEL_SOURCES = ["block_scaled_gemm_gb300/csrc/mxgemm_kernel.cuh",
                   "block_scaled_gemm_gb300/csrc/ptx.cuh"]
 PROFILE_SUMMARY = ROOT / "profiles" / "mxgemm_kernel_square_4096.md"
@@ -219,6 +220,16 @@ def measured_peak():
     except (OSError, KeyError, ValueError):
         return FALLBACK_BF16_BURST * FP8_OVER_BF16, \
             f"fallback bf16 {FALLBACK_BF16_BURST} TFLOP/s x {FP8_OVER_BF16} (of fallback)"
+
+
+def measured_hbm():
+    """HBM copy bandwidth in GB/s; (value, source text)."""
+    try:
+        d = json.loads((ROOT / "MEASURED_PEAKS.json").read_text())
+        v = float(d["hbm_gbs"])
+        return v, f"measured copy {v} GB/s (of measured)"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, f"fallback {FALLBACK_HBM_GBS} GB/s (of fallback)"
 
 
 def kernel_source_hash() -> str:
@@ -451,6 +462,21 @@ def run_mx(args, world, rank, local):
                "sample": f"first {rows} of {M} output rows (all {N} columns, K={K}), {dt:.1f} s"}
 
     if rank == 0:
+        # Tensor-bound when the arithmetic intensity is above the ridge
+        # (peak FLOP/s / HBM bytes/s), else HBM-bound: achieved = algorithmic
+        # bytes per launch / kernel time.
+        alg_bytes = M * K + K * N + (M + N) * K // 32 + M * N * (4 if prob.out_dtype == "f32" else 2)
+        hbm, hbm_src = measured_hbm()
+        if 2.0 * M * N * K / alg_bytes >= peak * 1e12 / (hbm * 1e9):
+            roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
+                        "frac": achieved / peak, "peak_source": peak_src}
+        else:
+            gbs = alg_bytes / (kern_avg_ms * 1e-3) / 1e9
+            roofline = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
+                        "frac": gbs / hbm, "peak_source": hbm_src}
+        roofline.update({"traffic": profiled_traffic() if args.workload == WORKLOAD else None,
+                         "algorithmic_bytes": alg_bytes, "kernel": "mxgemm_kernel",
+                         "kernel_avg_us": kern_avg_ms * 1e3})
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": step_ms_max / args.steps,
@@ -464,10 +490,7 @@ def run_mx(args, world, rank, local):
                               if flush is not None else "not flushed"),
                        "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
                        "tile_mode": args.mode if args.mode is not None else "auto"},
-            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
-                         "frac": achieved / peak, "traffic": profiled_traffic(),
-                         "kernel": "mxgemm_kernel", "kernel_avg_us": kern_avg_ms * 1e3,
-                         "peak_source": peak_src},
+            "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "steps": e2e_steps},
@@ -488,9 +511,8 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=300)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["mx", "reference"], default="mx")
-    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(
-        ["square_256", "square_4096", "mlp_up_8192x28672x8192", "longk_2048_65536",
-         "ragged_5000x7000x8192"]))
+    import mx_inputs
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(mx_inputs.WORKLOADS))
     ap.add_argument("--mode", type=int, default=None, help="tile mode: 1 = 1-CTA, 2 = CTA pair")
     ap.add_argument("--no-flush", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle baseline and spot parity")

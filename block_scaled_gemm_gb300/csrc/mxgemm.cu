@@ -251,7 +251,7 @@ struct Split {
   int half_tiles;      // half-width items after the whole tiles (2 per leftover tile)
 };
 
-Split plan_split(int64_t T, int64_t S, int P, bool allow_tail, bool allow_stream_k) {
+Split plan_split(int64_t T, int64_t S, int P, bool allow_tail, bool allow_stream_k, int64_t M) {
   Split r;
   r.units = static_cast<int>(T < P ? T : P);
   r.dp_tiles = static_cast<int>(T);
@@ -261,6 +261,28 @@ Split plan_split(int64_t T, int64_t S, int P, bool allow_tail, bool allow_stream
   if (!allow_tail || T == 0) return r;
   const int64_t W = T / P, R = T % P;
   if (R == 0) return r;
+  // Skinny problems (M <= 128: one row of tiles) with fewer tiles than
+  // CTAs: split every tile's K steps into s equal parts, s the largest
+  // divisor of S with T * s <= P and at least 4 K steps per part, so that
+  // every CTA computes one part of one tile (no CTA straddles two tiles and
+  // finishes late).  The partial sums hold only the valid rows, so their
+  // traffic stays small next to B's, and most SMs stream B instead of one
+  // per tile.  Not below 16 rows: at M = 1 the split measured slower than
+  // whole tiles (34.8 -> 41.0 us at N = K = 8192; its owners finished
+  // 4-18 us after the median CTA), at M = 16..128 faster (35.9 -> 30.8 us
+  // at M = 16).
+  if (allow_stream_k && W == 0 && M >= 16 && M <= 128 && S >= 8) {
+    int64_t parts = 1;
+    for (int64_t d = 2; d <= S / 4; ++d)
+      if (S % d == 0 && T * d <= P) parts = d;
+    if (parts > 1) {
+      r.units = static_cast<int>(T * parts);
+      r.dp_tiles = 0;
+      r.sk_ctas = static_cast<int>(T * parts);
+      r.sk_units = T * S;
+      return r;
+    }
+  }
   // Measured on GB300: the owners' gather of FP32 partials is slow enough
   // that stream-K pays off only with long K (64+ steps) after 1 to 8 full
   // waves, and not when the last wave is nearly full; in particular not when
@@ -525,7 +547,7 @@ int mxgemm_run(mxgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A
   // half-width items), handed out by the hardware; no stream-K, whose
   // partial-sum slots belong to fixed CTAs.
   const bool clc = h->scheduler == 1;
-  Split sp = plan_split(num_tiles, k_steps, h->sm_count / CG, h->stream_k != 0, !clc);
+  Split sp = plan_split(num_tiles, k_steps, h->sm_count / CG, h->stream_k != 0, !clc, M);
   if (clc) sp.units = sp.dp_tiles + sp.half_tiles;
   const Sizes z = plan_sizes(a_chunks, b_chunks, pad_b, K, npad, sp, CG);
   const size_t off_b = z.off_b;
@@ -910,7 +932,7 @@ extern "C" int mxgemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A
   const bool pad_b = (N % 16) != 0;
   const int64_t npad = round_up(static_cast<size_t>(N), 16);
   // no stream-K split here: the scratch holds only the repacked scales and B
-  const Split sp = plan_split(num_tiles, k_steps, nd->sm_count / CG, false, false);
+  const Split sp = plan_split(num_tiles, k_steps, nd->sm_count / CG, false, false, M);
   const Sizes z = plan_sizes(a_chunks, b_chunks, pad_b, K, npad, sp, CG);
   const size_t off_b = z.off_b;
   const size_t ws_bytes = z.total;

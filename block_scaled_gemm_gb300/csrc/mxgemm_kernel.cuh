@@ -903,18 +903,23 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
       }
       acc_phase ^= 1u;
 
+      // the accumulator row this lane holds
+      const bool row_ok = mt * (128 * CG) + 128 * (int)rank + 32 * q + lane < p.M;
       if (w.kind == kPartial) {
         // first part of a split tile: the FP32 partial to this CTA's slot,
         // then count this warp in the slot's flag.  The slot is laid out by
         // (warp, 4-column group, lane) -- the reader uses the same warp/lane
         // to row mapping -- so every warp access covers 512 contiguous bytes.
+        // Rows beyond M are neither written nor read.
         float4 *slot = reinterpret_cast<float4 *>(p.partials) +
                        static_cast<int64_t>(unit * CG + (int)rank) * (128 * 256 / 4) + ew * (32 * 32) + lane;
+        if (row_ok) {
 #pragma unroll
-        for (int c = 0; c < 128; c += 4)
-          __stcg(slot + (c / 4) * 32,
-                 make_float4(__uint_as_float(v[c >> 5][(c & 31) + 0]), __uint_as_float(v[c >> 5][(c & 31) + 1]),
-                             __uint_as_float(v[c >> 5][(c & 31) + 2]), __uint_as_float(v[c >> 5][(c & 31) + 3])));
+          for (int c = 0; c < 128; c += 4)
+            __stcg(slot + (c / 4) * 32,
+                   make_float4(__uint_as_float(v[c >> 5][(c & 31) + 0]), __uint_as_float(v[c >> 5][(c & 31) + 1]),
+                               __uint_as_float(v[c >> 5][(c & 31) + 2]), __uint_as_float(v[c >> 5][(c & 31) + 3])));
+        }
         __threadfence();
         __syncwarp();
         if (lane == 0) atomicAdd(p.flags + unit * CG + (int)rank, 1);
@@ -936,6 +941,7 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
                                static_cast<int64_t>(c * CG + (int)rank) * (128 * 256 / 4) + ew * (32 * 32) + lane;
 #pragma unroll
           for (int c4 = 0; c4 < 128; c4 += 4) {
+            if (!row_ok) break;
             const float4 o = __ldcg(slot + (c4 / 4) * 32);
             v[c4 >> 5][(c4 & 31) + 0] = __float_as_uint(__uint_as_float(v[c4 >> 5][(c4 & 31) + 0]) + o.x);
             v[c4 >> 5][(c4 & 31) + 1] = __float_as_uint(__uint_as_float(v[c4 >> 5][(c4 & 31) + 1]) + o.y);

@@ -230,10 +230,26 @@ def c_init(M: int, N: int, seed: int, out_dtype: str) -> torch.Tensor:
     return c.to(torch.bfloat16) if out_dtype == "bf16" else c
 
 
+def skinny(M: int, seed: int = 0, N: int = 8192, K: int = 8192) -> Problem:
+    """Decode-like: a few rows of A against a large B.  N(0,1) entries
+    block-quantized (A per row, B per column), scale bytes as quantized,
+    FP32 out."""
+    g = _gen(seed)
+    A, As = quantize_rows(torch.randn((M, K), generator=g))
+    bt = torch.randn((N, K), generator=g)
+    B, Bs = _quant_B_from_cols(bt)
+    del bt
+    return Problem(f"skinny_{M}x{N}x{K}", M, N, K, A, As, B, Bs, "f32", False)
+
+
 WORKLOADS = {
     "square_256": square_256,
     "square_4096": square_4096,
     "mlp_up_8192x28672x8192": mlp_up,
     "longk_2048_65536": longk,
     "ragged_5000x7000x8192": ragged,
+    "skinny_1x8192x8192": lambda seed=0: skinny(1, seed),
+    "skinny_16x8192x8192": lambda seed=0: skinny(16, seed),
+    "skinny_64x8192x8192": lambda seed=0: skinny(64, seed),
+    "skinny_128x8192x8192": lambda seed=0: skinny(128, seed),
 }

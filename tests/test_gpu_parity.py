@@ -326,3 +326,24 @@ def test_clc_scheduler_full_check(h, mode):
         gu.check_full(h, p)
     finally:
         mx.mxgemm_set_option(h, mx.OPT_SCHEDULER, 0)
+
+
+@pytest.mark.parametrize("M", [1, 16, 100, 128])
+@pytest.mark.parametrize("out_dtype,use_acc", [("f32", False), ("bf16", True)])
+def test_skinny_split_k(h, M, out_dtype, use_acc):
+    # At most 128 rows and fewer tiles than CTAs: every tile's K steps are
+    # split over all CTAs, with partial sums of the valid rows only.  Full
+    # check against the oracle, and against whole tiles (tail balancing off).
+    _mode(h, 0)
+    p = mi.random_problem(M, 2304, 2048, seed=101 + M, kind="normal", out_dtype=out_dtype)
+    cin = mi.c_init(M, p.N, 101, out_dtype) if use_acc else None
+    ref, bound = oracle.rows(p.A, p.As, p.B, p.Bs,
+                             c_in=None if cin is None else cin.to(torch.float64).numpy())
+    try:
+        for sk in (1, 0):
+            mx.mxgemm_set_option(h, mx.OPT_STREAM_K, sk)
+            C = gu.run_gpu(h, p, c_init=cin, use_acc=use_acc)
+            res = oracle.accept(gu.to_numpy_out(C, out_dtype), ref, bound, out_dtype)
+            assert res["ok"], f"stream_k={sk}: {res}"
+    finally:
+        mx.mxgemm_set_option(h, mx.OPT_STREAM_K, 1)
