@@ -64,12 +64,15 @@ def _load():
         lib.mxo_e4m3.restype = ctypes.c_double
         lib.mxo_e8m0.argtypes = [ctypes.c_uint8]
         lib.mxo_e8m0.restype = ctypes.c_double
-        lib.mxo_rows.argtypes = [i64, i64, i64, u8p, u8p, u8p, u8p, i64, i64p,
-                                 f64p, f64p, ctypes.c_int]
-        lib.mxo_rows.restype = ctypes.c_int
-        lib.mxo_points.argtypes = [i64, i64, i64, u8p, u8p, u8p, u8p, i64,
-                                   i64p, i64p, f64p, f64p, ctypes.c_int]
-        lib.mxo_points.restype = ctypes.c_int
+        ci = ctypes.c_int
+        lib.mxo_decode.argtypes = [ci, ctypes.c_uint8]
+        lib.mxo_decode.restype = ctypes.c_double
+        lib.mxo_rows_fmt.argtypes = [i64, i64, i64, u8p, u8p, u8p, u8p, i64, i64p,
+                                     f64p, f64p, ci, ci, ci]
+        lib.mxo_rows_fmt.restype = ci
+        lib.mxo_points_fmt.argtypes = [i64, i64, i64, u8p, u8p, u8p, u8p, i64,
+                                       i64p, i64p, f64p, f64p, ci, ci, ci]
+        lib.mxo_points_fmt.restype = ci
         lib.mxo_round_f32.argtypes = [ctypes.c_double]
         lib.mxo_round_f32.restype = ctypes.c_float
         lib.mxo_round_bf16.argtypes = [ctypes.c_double]
@@ -101,6 +104,16 @@ def e4m3(code: int) -> float:
     return _load().mxo_e4m3(int(code) & 0xFF)
 
 
+# element format ids (OCP MX v1.0 element formats; one code per byte, the
+# sub-byte formats in the low bits)
+FORMATS = {"e4m3": 0, "e5m2": 1, "e2m3": 2, "e3m2": 3, "e2m1": 4}
+
+
+def decode(fmt: str, code: int) -> float:
+    """Value of one element code in format fmt (a key of FORMATS)."""
+    return _load().mxo_decode(FORMATS[fmt], int(code) & 0xFF)
+
+
 def e8m0(code: int) -> float:
     """Value of one E8M0 scale byte: 2**(code-127), NaN for 255."""
     return _load().mxo_e8m0(int(code) & 0xFF)
@@ -120,18 +133,21 @@ def _ptr(a: np.ndarray):
     return a.ctypes.data_as(ctypes.c_void_p)
 
 
-def rows(A, As, B, Bs, rows=None, c_in=None, threads: int | None = None):
+def rows(A, As, B, Bs, rows=None, c_in=None, threads: int | None = None,
+         a_fmt: str = "e4m3", b_fmt: str = "e4m3"):
     """Full output rows of the product.  Returns (ref, bound), float64 arrays
     of shape (len(rows), N).  ``rows=None`` means every row.  ``c_in`` (the
     accumulated-into C, any float dtype, shape (len(rows), N)) is added to
-    ref and its magnitude to bound when given (use_acc)."""
+    ref and its magnitude to bound when given (use_acc).  ``a_fmt`` and
+    ``b_fmt`` name the element formats (keys of FORMATS)."""
     A, As, B, Bs = map(_u8, (A, As, B, Bs))
     M, N, K = _shapes(A, As, B, Bs)
     idx = np.arange(M, dtype=np.int64) if rows is None else np.ascontiguousarray(rows, dtype=np.int64)
     ref = np.empty((idx.size, N), dtype=np.float64)
     bnd = np.empty((idx.size, N), dtype=np.float64)
-    rc = _load().mxo_rows(M, N, K, _ptr(A), _ptr(As), _ptr(B), _ptr(Bs), idx.size,
-                          _ptr(idx), _ptr(ref), _ptr(bnd), threads or host_threads())
+    rc = _load().mxo_rows_fmt(M, N, K, _ptr(A), _ptr(As), _ptr(B), _ptr(Bs), idx.size,
+                              _ptr(idx), _ptr(ref), _ptr(bnd), threads or host_threads(),
+                              FORMATS[a_fmt], FORMATS[b_fmt])
     if rc != 0:
         raise ValueError("mxo_rows rejected its arguments")
     if c_in is not None:
@@ -141,7 +157,8 @@ def rows(A, As, B, Bs, rows=None, c_in=None, threads: int | None = None):
     return ref, bnd
 
 
-def points(A, As, B, Bs, I, J, c_in=None, threads: int | None = None):
+def points(A, As, B, Bs, I, J, c_in=None, threads: int | None = None,
+           a_fmt: str = "e4m3", b_fmt: str = "e4m3"):
     """The product at points (I[p], J[p]).  Returns (ref, bound), float64
     vectors.  ``c_in`` (values of C at those points) is added when given."""
     A, As, B, Bs = map(_u8, (A, As, B, Bs))
@@ -152,8 +169,9 @@ def points(A, As, B, Bs, I, J, c_in=None, threads: int | None = None):
         raise ValueError("I and J differ in shape")
     ref = np.empty(I.size, dtype=np.float64)
     bnd = np.empty(I.size, dtype=np.float64)
-    rc = _load().mxo_points(M, N, K, _ptr(A), _ptr(As), _ptr(B), _ptr(Bs), I.size,
-                            _ptr(I), _ptr(J), _ptr(ref), _ptr(bnd), threads or host_threads())
+    rc = _load().mxo_points_fmt(M, N, K, _ptr(A), _ptr(As), _ptr(B), _ptr(Bs), I.size,
+                                _ptr(I), _ptr(J), _ptr(ref), _ptr(bnd), threads or host_threads(),
+                                FORMATS[a_fmt], FORMATS[b_fmt])
     if rc != 0:
         raise ValueError("mxo_points rejected its arguments")
     if c_in is not None:

@@ -8,8 +8,11 @@
  *
  * What it computes (the plain definition, no blocking or fusion):
  *
- *   ref[i][j]   = sum_{k<K} e4m3(A[i][k]) * e8m0(As[i][k/32])
- *                         * e4m3(B[k][j]) * e8m0(Bs[j][k/32])
+ *   ref[i][j]   = sum_{k<K} fa(A[i][k]) * e8m0(As[i][k/32])
+ *                         * fb(B[k][j]) * e8m0(Bs[j][k/32])
+ *
+ * fa, fb: element decoders; E4M3 for the headline path, E5M2, E2M3, E3M2
+ * or E2M1 for the other formats of the same MX family.
  *   bound[i][j] = sum_{k<K} | same term |
  *
  * accumulated in IEEE double, k ascending.
@@ -64,6 +67,61 @@ double mxo_e4m3(uint8_t code) {
   return s ? -v : v;
 }
 
+/* The other element formats of the same MX family (OCP MX v1.0), one code
+ * per byte; the sub-byte formats use the low bits of the byte and ignore
+ * the rest.
+ *
+ * E5M2: bit 7 sign, bits 6..2 exponent E (bias 15), bits 1..0 mantissa m.
+ *   E == 0  : (-1)^s * m/4 * 2^-14          (subnormal)
+ *   E == 31 : +-inf when m == 0, else NaN
+ *   else    : (-1)^s * (1 + m/4) * 2^(E-15)                               */
+double mxo_e5m2(uint8_t code) {
+  int s = (code >> 7) & 1;
+  int e = (code >> 2) & 31;
+  int m = code & 3;
+  double v;
+  if (e == 31) return m == 0 ? (s ? -INFINITY : INFINITY) : NAN;
+  if (e == 0)
+    v = ldexp((double)m, -16);
+  else
+    v = ldexp(4.0 + (double)m, e - 15 - 2);
+  return s ? -v : v;
+}
+
+/* Sub-byte formats with sign bit at position (ebits + mbits), exponent
+ * bias b, no infinities or NaN:
+ *   E == 0 : (-1)^s * m / 2^mbits * 2^(1-b)        (subnormal)
+ *   else   : (-1)^s * (1 + m / 2^mbits) * 2^(E-b)
+ * E2M3 (FP6): ebits 2, mbits 3, bias 1 (max 7.5)
+ * E3M2 (FP6): ebits 3, mbits 2, bias 3 (max 28)
+ * E2M1 (FP4): ebits 2, mbits 1, bias 1 (max 6)                           */
+static double mxo_small(uint8_t code, int ebits, int mbits, int bias) {
+  int s = (code >> (ebits + mbits)) & 1;
+  int e = (code >> mbits) & ((1 << ebits) - 1);
+  int m = code & ((1 << mbits) - 1);
+  double v;
+  if (e == 0)
+    v = ldexp((double)m, 1 - bias - mbits);
+  else
+    v = ldexp((double)((1 << mbits) + m), e - bias - mbits);
+  return s ? -v : v;
+}
+double mxo_e2m3(uint8_t code) { return mxo_small(code, 2, 3, 1); }
+double mxo_e3m2(uint8_t code) { return mxo_small(code, 3, 2, 3); }
+double mxo_e2m1(uint8_t code) { return mxo_small(code, 2, 1, 1); }
+
+/* element format ids: 0 E4M3, 1 E5M2, 2 E2M3, 3 E3M2, 4 E2M1 */
+double mxo_decode(int fmt, uint8_t code) {
+  switch (fmt) {
+    case 0: return mxo_e4m3(code);
+    case 1: return mxo_e5m2(code);
+    case 2: return mxo_e2m3(code);
+    case 3: return mxo_e3m2(code);
+    case 4: return mxo_e2m1(code);
+    default: return NAN;
+  }
+}
+
 /* E8M0: an unsigned biased exponent with no sign and no mantissa.
  *   s in [0, 254] : 2^(s - 127)     s == 255 : NaN                        */
 double mxo_e8m0(uint8_t code) {
@@ -81,7 +139,7 @@ typedef struct {
   const int64_t *rows; /* which rows of C to produce */
   int64_t nrows;
   double *ref, *bound; /* nrows x N each */
-  const double *lut_e4m3, *lut_e8m0;
+  const double *lut_a, *lut_b, *lut_e8m0;
   int64_t r_begin, r_end; /* this worker's share of `rows` */
 } rows_job;
 
@@ -97,14 +155,14 @@ static void *rows_worker(void *arg) {
       bnd[j] = 0.0;
     }
     for (int64_t k = 0; k < K; ++k) {
-      /* a = e4m3(A[i][k]) * e8m0(As[i][k/32]) */
-      const double a = jb->lut_e4m3[jb->A[i * K + k]] *
+      /* a = fa(A[i][k]) * e8m0(As[i][k/32]) */
+      const double a = jb->lut_a[jb->A[i * K + k]] *
                        jb->lut_e8m0[jb->As[i * KB + k / 32]];
       const uint8_t *brow = jb->B + k * N;
       for (int64_t j = 0; j < N; ++j) {
-        /* b = e4m3(B[k][j]) * e8m0(Bs[j][k/32]) */
+        /* b = fb(B[k][j]) * e8m0(Bs[j][k/32]) */
         const double b =
-            jb->lut_e4m3[brow[j]] * jb->lut_e8m0[jb->Bs[j * KB + k / 32]];
+            jb->lut_b[brow[j]] * jb->lut_e8m0[jb->Bs[j * KB + k / 32]];
         const double t = a * b;
         acc[j] += t;
         bnd[j] += fabs(t);
@@ -114,24 +172,29 @@ static void *rows_worker(void *arg) {
   return NULL;
 }
 
-static void build_luts(double *l4, double *l8) {
+static void build_luts(int fa, int fb, double *la, double *lb, double *l8) {
   for (int c = 0; c < 256; ++c) {
-    l4[c] = mxo_e4m3((uint8_t)c);
+    la[c] = mxo_decode(fa, (uint8_t)c);
+    lb[c] = mxo_decode(fb, (uint8_t)c);
     l8[c] = mxo_e8m0((uint8_t)c);
   }
 }
 
-/* Full rows `rows[0..nrows)` of the product.  ref and bound are nrows x N.
- * Returns 0 on success, -1 on a bad argument. */
-int mxo_rows(int64_t M, int64_t N, int64_t K, const uint8_t *A,
-             const uint8_t *As, const uint8_t *B, const uint8_t *Bs,
-             int64_t nrows, const int64_t *rows, double *ref, double *bound,
-             int nthreads) {
+static int bad_fmt(int f) { return f < 0 || f > 4; }
+
+/* Full rows `rows[0..nrows)` of the product, A's elements in format fa and
+ * B's in fb.  ref and bound are nrows x N.  Returns 0 on success, -1 on a
+ * bad argument. */
+int mxo_rows_fmt(int64_t M, int64_t N, int64_t K, const uint8_t *A,
+                 const uint8_t *As, const uint8_t *B, const uint8_t *Bs,
+                 int64_t nrows, const int64_t *rows, double *ref, double *bound,
+                 int nthreads, int fa, int fb) {
   if (M < 0 || N < 0 || K < 0 || K % 32 != 0 || nrows < 0) return -1;
+  if (bad_fmt(fa) || bad_fmt(fb)) return -1;
   for (int64_t r = 0; r < nrows; ++r)
     if (rows[r] < 0 || rows[r] >= M) return -1;
-  double l4[256], l8[256];
-  build_luts(l4, l8);
+  double la[256], lb[256], l8[256];
+  build_luts(fa, fb, la, lb, l8);
   if (nthreads < 1) nthreads = 1;
   if (nthreads > nrows) nthreads = nrows > 0 ? (int)nrows : 1;
   rows_job *jobs = (rows_job *)calloc((size_t)nthreads, sizeof(rows_job));
@@ -147,7 +210,7 @@ int mxo_rows(int64_t M, int64_t N, int64_t K, const uint8_t *A,
     jb->A = A; jb->As = As; jb->B = B; jb->Bs = Bs;
     jb->rows = rows; jb->nrows = nrows;
     jb->ref = ref; jb->bound = bound;
-    jb->lut_e4m3 = l4; jb->lut_e8m0 = l8;
+    jb->lut_a = la; jb->lut_b = lb; jb->lut_e8m0 = l8;
     jb->r_begin = nrows * t / nthreads;
     jb->r_end = nrows * (t + 1) / nthreads;
   }
@@ -174,7 +237,7 @@ typedef struct {
   const uint8_t *A, *As, *B, *Bs;
   const int64_t *I, *J;
   double *ref, *bound;
-  const double *lut_e4m3, *lut_e8m0;
+  const double *lut_a, *lut_b, *lut_e8m0;
   int64_t p_begin, p_end;
 } points_job;
 
@@ -185,9 +248,9 @@ static void *points_worker(void *arg) {
     const int64_t i = jb->I[p], j = jb->J[p];
     double acc = 0.0, bnd = 0.0;
     for (int64_t k = 0; k < K; ++k) {
-      const double a = jb->lut_e4m3[jb->A[i * K + k]] *
+      const double a = jb->lut_a[jb->A[i * K + k]] *
                        jb->lut_e8m0[jb->As[i * KB + k / 32]];
-      const double b = jb->lut_e4m3[jb->B[k * N + j]] *
+      const double b = jb->lut_b[jb->B[k * N + j]] *
                        jb->lut_e8m0[jb->Bs[j * KB + k / 32]];
       const double t = a * b;
       acc += t;
@@ -199,15 +262,16 @@ static void *points_worker(void *arg) {
   return NULL;
 }
 
-int mxo_points(int64_t M, int64_t N, int64_t K, const uint8_t *A,
-               const uint8_t *As, const uint8_t *B, const uint8_t *Bs,
-               int64_t npts, const int64_t *I, const int64_t *J, double *ref,
-               double *bound, int nthreads) {
+int mxo_points_fmt(int64_t M, int64_t N, int64_t K, const uint8_t *A,
+                   const uint8_t *As, const uint8_t *B, const uint8_t *Bs,
+                   int64_t npts, const int64_t *I, const int64_t *J, double *ref,
+                   double *bound, int nthreads, int fa, int fb) {
   if (M < 0 || N < 0 || K < 0 || K % 32 != 0 || npts < 0) return -1;
+  if (bad_fmt(fa) || bad_fmt(fb)) return -1;
   for (int64_t p = 0; p < npts; ++p)
     if (I[p] < 0 || I[p] >= M || J[p] < 0 || J[p] >= N) return -1;
-  double l4[256], l8[256];
-  build_luts(l4, l8);
+  double la[256], lb[256], l8[256];
+  build_luts(fa, fb, la, lb, l8);
   if (nthreads < 1) nthreads = 1;
   if (nthreads > npts) nthreads = npts > 0 ? (int)npts : 1;
   points_job *jobs = (points_job *)calloc((size_t)nthreads, sizeof(points_job));
@@ -223,7 +287,7 @@ int mxo_points(int64_t M, int64_t N, int64_t K, const uint8_t *A,
     jb->A = A; jb->As = As; jb->B = B; jb->Bs = Bs;
     jb->I = I; jb->J = J;
     jb->ref = ref; jb->bound = bound;
-    jb->lut_e4m3 = l4; jb->lut_e8m0 = l8;
+    jb->lut_a = la; jb->lut_b = lb; jb->lut_e8m0 = l8;
     jb->p_begin = npts * t / nthreads;
     jb->p_end = npts * (t + 1) / nthreads;
   }
@@ -238,6 +302,21 @@ int mxo_points(int64_t M, int64_t N, int64_t K, const uint8_t *A,
   free(jobs);
   free(tid);
   return 0;
+}
+
+/* E4M3 x E4M3, the format of the headline path */
+int mxo_rows(int64_t M, int64_t N, int64_t K, const uint8_t *A,
+             const uint8_t *As, const uint8_t *B, const uint8_t *Bs,
+             int64_t nrows, const int64_t *rows, double *ref, double *bound,
+             int nthreads) {
+  return mxo_rows_fmt(M, N, K, A, As, B, Bs, nrows, rows, ref, bound, nthreads, 0, 0);
+}
+
+int mxo_points(int64_t M, int64_t N, int64_t K, const uint8_t *A,
+               const uint8_t *As, const uint8_t *B, const uint8_t *Bs,
+               int64_t npts, const int64_t *I, const int64_t *J, double *ref,
+               double *bound, int nthreads) {
+  return mxo_points_fmt(M, N, K, A, As, B, Bs, npts, I, J, ref, bound, nthreads, 0, 0);
 }
 
 /* ---------------------------------------------------------------------- */

@@ -272,3 +272,102 @@ def test_quantizer_recipe_roundtrip():
     # the scale is the smallest power of two that fits the block
     blkmax = np.abs(dec).reshape(64, 8, 32).max(axis=2)
     assert np.all((blkmax >= 224) & (blkmax <= 448))
+
+
+# ---------------------------------------------------------------- other MX element formats
+
+def _other_format_values():
+    out = []
+    for line in (GOLDEN / "mx_other_formats_values.txt").read_text().splitlines():
+        if not line.strip() or line.startswith("#"):
+            continue
+        fmt, code, val = line.split()
+        out.append((fmt, int(code, 16), float(val)))
+    return out
+
+
+@pytest.mark.parametrize("fmt,code,val", _other_format_values())
+def test_other_format_spot_values(fmt, code, val):
+    got = oracle.decode(fmt, code)
+    if np.isnan(val):
+        assert np.isnan(got)
+    else:
+        assert got == val
+        assert np.signbit(got) == np.signbit(val)
+
+
+def test_e5m2_all_codes_match_library_decode():
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    lib = codes.view(torch.float8_e5m2).to(torch.float64).numpy()
+    ours = np.array([oracle.decode("e5m2", c) for c in range(256)])
+    nan = np.isnan(lib)
+    assert np.array_equal(nan, np.isnan(ours))
+    assert np.array_equal(lib[~nan], ours[~nan])
+    assert np.array_equal(np.signbit(lib[~nan]), np.signbit(ours[~nan]))
+
+
+@pytest.mark.parametrize("fmt,bits,count,vmax", [("e2m3", 6, 64, 7.5), ("e3m2", 6, 64, 28.0),
+                                                  ("e2m1", 4, 16, 6.0)])
+def test_subbyte_formats_closed_properties(fmt, bits, count, vmax):
+    vals = np.array([oracle.decode(fmt, c) for c in range(count)])
+    # finite everywhere, symmetric under the sign bit, monotone in the
+    # magnitude code, largest value as the specification states
+    assert np.all(np.isfinite(vals))
+    half = count // 2
+    assert np.array_equal(vals[half:], -vals[:half])
+    assert np.all(np.diff(vals[:half]) > 0)
+    assert vals.max() == vmax
+    # the bits above the code are ignored
+    for c in range(count):
+        assert oracle.decode(fmt, c | (0xFF << bits) & 0xFF) == vals[c]
+    # e4m3 values decoded from the same codes differ: the format is honoured
+    assert any(oracle.decode("e4m3", c) != vals[c] for c in range(count))
+
+
+@pytest.mark.parametrize("fa,fb", [("e5m2", "e5m2"), ("e4m3", "e5m2"), ("e2m3", "e3m2"),
+                                   ("e2m1", "e2m1"), ("e2m1", "e4m3")])
+def test_mixed_format_product_brute_force(fa, fb):
+    # exact rational sums of the decoded values, independent of the LUTs
+    # used inside the oracle
+    g = torch.Generator().manual_seed(17)
+    M, N, K = 2, 3, 64
+    limit = {"e4m3": 256, "e5m2": 256, "e2m3": 64, "e3m2": 64, "e2m1": 16}
+    def codes(fmt, n):
+        c = torch.randint(0, limit[fmt], (n,), generator=g).numpy().astype(np.uint8)
+        if fmt == "e4m3":
+            c[(c & 0x7F) == 0x7F] = 0x3F   # no NaN codes
+        if fmt == "e5m2":
+            c[(c & 0x7C) == 0x7C] = 0x3C   # no inf/NaN codes
+        return c
+    A = codes(fa, M * K).reshape(M, K)
+    B = codes(fb, K * N).reshape(K, N)
+    As = torch.randint(120, 135, (M, K // 32), generator=g).numpy().astype(np.uint8)
+    Bs = torch.randint(120, 135, (N, K // 32), generator=g).numpy().astype(np.uint8)
+    ref, bound = oracle.rows(A, As, B, Bs, a_fmt=fa, b_fmt=fb)
+    pts_ref, _ = oracle.points(A, As, B, Bs, np.array([0, 1]), np.array([2, 0]), a_fmt=fa, b_fmt=fb)
+    assert pts_ref[0] == ref[0, 2] and pts_ref[1] == ref[1, 0]
+
+    def value(fmt, c):
+        # written out again from the definition, with Fractions
+        spec = {"e4m3": (4, 3, 7), "e5m2": (5, 2, 15), "e2m3": (2, 3, 1), "e3m2": (3, 2, 3),
+                "e2m1": (2, 1, 1)}[fmt]
+        eb, mb, bias = spec
+        s = (c >> (eb + mb)) & 1
+        e = (c >> mb) & ((1 << eb) - 1)
+        m = c & ((1 << mb) - 1)
+        if e == 0:
+            v = Fraction(m, 2 ** mb) * Fraction(2) ** (1 - bias)
+        else:
+            v = (1 + Fraction(m, 2 ** mb)) * Fraction(2) ** (e - bias)
+        return -v if s else v
+
+    for i in range(M):
+        for j in range(N):
+            exact = sum(value(fa, int(A[i, k])) * Fraction(2) ** (int(As[i, k // 32]) - 127)
+                        * value(fb, int(B[k, j])) * Fraction(2) ** (int(Bs[j, k // 32]) - 127)
+                        for k in range(K))
+            absum = sum(abs(value(fa, int(A[i, k])) * value(fb, int(B[k, j])))
+                        * Fraction(2) ** (int(As[i, k // 32]) + int(Bs[j, k // 32]) - 254)
+                        for k in range(K))
+            assert abs(Fraction(ref[i, j]) - exact) <= Fraction(K, 2 ** 53) * absum
+            assert float(absum) == pytest.approx(bound[i, j], rel=1e-15)
