@@ -23,7 +23,8 @@ from . import _build
 
 __all__ = [
     "OUT_F32", "OUT_BF16", "OPT_MODE", "OPT_WAIT_TIMEOUT_NS", "OPT_TEST_STALL_PRODUCER",
-    "OPT_SCHEDULER", "OPT_STREAM_K", "MxgemmError", "library", "library_path", "mxgemm_create", "mxgemm_run",
+    "OPT_SCHEDULER", "OPT_STREAM_K", "OPT_A_FORMAT", "OPT_B_FORMAT", "FMT_E4M3", "FMT_E5M2",
+    "FMT_E2M3", "FMT_E3M2", "FMT_E2M1", "MxgemmError", "library", "library_path", "mxgemm_create", "mxgemm_run",
     "mxgemm_destroy", "mxgemm_set_option", "mxgemm_get_device_status", "mxgemm_status_string",
     "mxgemm_set_profile_events", "mxgemm_get_launch_count", "mxgemm_run_noalloc", "mxgemm_run_host",
     "EXPORTED_SYMBOLS", "Gemm",
@@ -37,6 +38,16 @@ OPT_WAIT_TIMEOUT_NS = 2
 OPT_TEST_STALL_PRODUCER = 3
 OPT_SCHEDULER = 4
 OPT_STREAM_K = 5
+OPT_A_FORMAT = 6
+OPT_B_FORMAT = 7
+
+# element formats (mxgemm_format_t); one element per byte, sub-byte codes in
+# the low bits
+FMT_E4M3 = 0
+FMT_E5M2 = 1
+FMT_E2M3 = 2
+FMT_E3M2 = 3
+FMT_E2M1 = 4
 
 OK = 0
 ERR_INVALID_VALUE = 1

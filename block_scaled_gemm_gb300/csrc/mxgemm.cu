@@ -38,13 +38,15 @@ struct Plan {
   int64_t M = 0, N = 0, K = 0;
   const void *A = nullptr, *As = nullptr, *B = nullptr, *Bs = nullptr;
   void *C = nullptr;
-  int use_acc = 0, out_dtype = 0, mode = 0, stall = 0, sched = 0, sk = 0;
+  int use_acc = 0, out_dtype = 0, mode = 0, stall = 0, sched = 0, sk = 0, fmts = 0;
   long long timeout_ns = 0;
   uint8_t *ws = nullptr;
   // value
   int CG = 1;
   bool pad_b = false;
   int64_t npad = 0;
+  int a_bits = 8, b_bits = 8;  // element bits; below 8 the operand is packed first
+  size_t off_a = 0;
   CUtensorMap tA, tB, tB64, tSA, tSB, tC;
   KParams kp;
   mxg::RepackArgs ra, rb;
@@ -55,10 +57,10 @@ struct Plan {
 
   bool matches(int64_t M_, int64_t N_, int64_t K_, const void *A_, const void *As_, const void *B_,
                const void *Bs_, void *C_, int ua, int od, int md, int sl, int sc, int sk_,
-               long long to, uint8_t *w) const {
+               long long to, uint8_t *w, int fm) const {
     return valid && M == M_ && N == N_ && K == K_ && A == A_ && As == As_ && B == B_ &&
            Bs == Bs_ && C == C_ && use_acc == ua && out_dtype == od && mode == md &&
-           stall == sl && sched == sc && sk == sk_ && timeout_ns == to && ws == w;
+           stall == sl && sched == sc && sk == sk_ && timeout_ns == to && ws == w && fmts == fm;
   }
 };
 
@@ -89,6 +91,7 @@ struct mxgemm_ctx {
   int stall_producer = 0;
   int scheduler = 0;
   int stream_k = 1;
+  int a_fmt = 0, b_fmt = 0;  // element formats (mxgemm_format_t)
   bool attr_set[3][8] = {};
   cudaEvent_t prof_before = nullptr;
   cudaEvent_t prof_after = nullptr;
@@ -309,20 +312,21 @@ Split plan_split(int64_t T, int64_t S, int P, bool allow_tail, bool allow_stream
   return r;
 }
 
-// Workspace layout of a run: repacked scales, re-pitched B, stream-K
-// partials and flags.
+// Workspace layout of a run: repacked scales, re-pitched (or packed) B,
+// stream-K partials and flags, packed A (6- and 4-bit A formats).
 struct Sizes {
-  size_t off_sfb, off_b, off_part, off_flags, total;
+  size_t off_sfb, off_b, off_part, off_flags, off_a, total;
 };
 
 Sizes plan_sizes(int64_t a_chunks, int64_t b_chunks, bool pad_b, int64_t K, int64_t npad,
-                 const Split &sp, int CG) {
+                 const Split &sp, int CG, size_t a_bytes) {
   Sizes z;
   z.off_sfb = round_up(static_cast<size_t>(a_chunks) * 512, 1024);
   z.off_b = round_up(z.off_sfb + static_cast<size_t>(b_chunks) * 512, 1024);
   z.off_part = round_up(z.off_b + (pad_b ? static_cast<size_t>(K) * npad : 0), 1024);
   z.off_flags = z.off_part + static_cast<size_t>(sp.sk_ctas) * CG * 128 * 256 * sizeof(float);
-  z.total = round_up(z.off_flags + static_cast<size_t>(sp.sk_ctas) * CG * sizeof(int) + 16, 1024);
+  z.off_a = round_up(z.off_flags + static_cast<size_t>(sp.sk_ctas) * CG * sizeof(int) + 16, 1024);
+  z.total = round_up(z.off_a + a_bytes, 1024);
   return z;
 }
 
@@ -332,7 +336,7 @@ int build_plan(mxgemm_ctx *h, Plan *pl, int64_t M, int64_t N, int64_t K, const v
                const void *A_scale, const void *B, const void *B_scale, void *C, int use_acc,
                int out_dtype, int CG, int64_t m_tiles, int64_t n_tiles, int64_t k_steps,
                int64_t num_tiles, int64_t a_chunks, int64_t b_chunks, bool pad_b, int64_t npad,
-               const Split &sp, const Sizes &z) {
+               const Split &sp, const Sizes &z, int a_bits, int b_bits) {
   const size_t off_sfb = z.off_sfb, off_b = z.off_b;
   const size_t esz = out_dtype == MXGEMM_OUT_F32 ? 4 : 2;
   const int64_t kb = K / 32;
@@ -340,6 +344,7 @@ int build_plan(mxgemm_ctx *h, Plan *pl, int64_t M, int64_t N, int64_t K, const v
   uint8_t *sfb = h->ws.ptr + off_sfb;
   const void *bsrc = pad_b ? static_cast<const void *>(h->ws.ptr + off_b) : B;
   const int64_t bpitch = pad_b ? npad : N;
+  const void *asrc = a_bits < 8 ? static_cast<const void *>(h->ws.ptr + z.off_a) : A;
   pl->ra = mxg::RepackArgs{static_cast<const uint8_t *>(A_scale), reinterpret_cast<uint32_t *>(sfa),
                            M, static_cast<int>(kb), static_cast<int>(k_steps), 1,
                            static_cast<int>(m_tiles * CG), static_cast<int>(cdiv(k_steps, 16))};
@@ -349,7 +354,7 @@ int build_plan(mxgemm_ctx *h, Plan *pl, int64_t M, int64_t N, int64_t K, const v
   pl->blocks_a = pl->ra.row_blocks * pl->ra.kgroups;
   pl->blocks_b = pl->rb.row_blocks * pl->rb.kgroups;
   const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
-  if (encode_2d(h, &pl->tA, u8, A, K, M, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+  if (encode_2d(h, &pl->tA, u8, asrc, K, M, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
       encode_2d(h, &pl->tB, u8, bsrc, N, K, bpitch, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
       // half-width tiles of CTA pairs: 64 columns per CTA
       encode_2d(h, &pl->tB64, u8, bsrc, N, K, bpitch, 64, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
@@ -393,17 +398,22 @@ int build_plan(mxgemm_ctx *h, Plan *pl, int64_t M, int64_t N, int64_t K, const v
   kp.partials = reinterpret_cast<float *>(h->ws.ptr + z.off_part);
   kp.flags = reinterpret_cast<int *>(h->ws.ptr + z.off_flags);
   kp.half_tiles = sp.half_tiles;
+  kp.idesc_fmt = mxg::fmt_bits(h->a_fmt, h->b_fmt);
   pl->units = sp.units;
   pl->flags = kp.flags;
   pl->nflags = sp.sk_ctas * CG;
   pl->CG = CG;
   pl->pad_b = pad_b;
   pl->npad = npad;
+  pl->a_bits = a_bits;
+  pl->b_bits = b_bits;
+  pl->off_a = z.off_a;
   pl->M = M; pl->N = N; pl->K = K;
   pl->A = A; pl->As = A_scale; pl->B = B; pl->Bs = B_scale; pl->C = C;
   pl->use_acc = use_acc; pl->out_dtype = out_dtype; pl->mode = h->mode;
   pl->stall = h->stall_producer; pl->sched = h->scheduler; pl->sk = h->stream_k;
   pl->timeout_ns = h->timeout_ns;
+  pl->fmts = h->a_fmt * 8 + h->b_fmt;
   pl->ws = h->ws.ptr;
   pl->valid = true;
   return MXGEMM_OK;
@@ -495,6 +505,11 @@ int mxgemm_set_option(mxgemm_handle_t h, int option, int64_t value) {
       if (value < 0 || value > 1) return MXGEMM_ERR_INVALID_VALUE;
       h->stream_k = static_cast<int>(value);
       return MXGEMM_OK;
+    case MXGEMM_OPT_A_FORMAT:
+    case MXGEMM_OPT_B_FORMAT:
+      if (value < MXGEMM_FMT_E4M3 || value > MXGEMM_FMT_E2M1) return MXGEMM_ERR_INVALID_VALUE;
+      (option == MXGEMM_OPT_A_FORMAT ? h->a_fmt : h->b_fmt) = static_cast<int>(value);
+      return MXGEMM_OK;
     default:
       return MXGEMM_ERR_INVALID_VALUE;
   }
@@ -541,7 +556,10 @@ int mxgemm_run(mxgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A
   if (num_tiles >= lim) return MXGEMM_ERR_INVALID_VALUE;
   const int64_t a_chunks = m_tiles * CG * k_steps;  // 512-byte chunks of A scales
   const int64_t b_chunks = n_tiles * k_steps * 2;   // 2 per 256 columns
-  const bool pad_b = (N % 16) != 0;
+  // 6- and 4-bit formats are packed 16 elements per 16-byte group first
+  const int a_bits = h->a_fmt == MXGEMM_FMT_E2M1 ? 4 : h->a_fmt >= MXGEMM_FMT_E2M3 ? 6 : 8;
+  const int b_bits = h->b_fmt == MXGEMM_FMT_E2M1 ? 4 : h->b_fmt >= MXGEMM_FMT_E2M3 ? 6 : 8;
+  const bool pad_b = (N % 16) != 0 || b_bits < 8;
   const int64_t npad = round_up(static_cast<size_t>(N), 16);
   // Cluster launch control: one cluster per work item (whole tiles, then
   // half-width items), handed out by the hardware; no stream-K, whose
@@ -549,14 +567,16 @@ int mxgemm_run(mxgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A
   const bool clc = h->scheduler == 1;
   Split sp = plan_split(num_tiles, k_steps, h->sm_count / CG, h->stream_k != 0, !clc, M);
   if (clc) sp.units = sp.dp_tiles + sp.half_tiles;
-  const Sizes z = plan_sizes(a_chunks, b_chunks, pad_b, K, npad, sp, CG);
+  const Sizes z = plan_sizes(a_chunks, b_chunks, pad_b, K, npad, sp, CG,
+                             a_bits < 8 ? static_cast<size_t>(M) * K : 0);
   const size_t off_b = z.off_b;
   const size_t ws_bytes = z.total;
 
   Plan *plan = nullptr;
   for (Plan &pl : h->plans)
     if (pl.matches(M, N, K, A, A_scale, B, B_scale, C, use_acc, out_dtype, h->mode,
-                   h->stall_producer, h->scheduler, h->stream_k, h->timeout_ns, h->ws.ptr) &&
+                   h->stall_producer, h->scheduler, h->stream_k, h->timeout_ns, h->ws.ptr,
+                   h->a_fmt * 8 + h->b_fmt) &&
         h->ws.bytes >= ws_bytes) {
       plan = &pl;
       break;
@@ -571,14 +591,20 @@ int mxgemm_run(mxgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A
     h->next_plan = (h->next_plan + 1) % kPlanCache;
     plan->valid = false;
     st = build_plan(h, plan, M, N, K, A, A_scale, B, B_scale, C, use_acc, out_dtype, CG, m_tiles,
-                    n_tiles, k_steps, num_tiles, a_chunks, b_chunks, pad_b, npad, sp, z);
+                    n_tiles, k_steps, num_tiles, a_chunks, b_chunks, pad_b, npad, sp, z, a_bits,
+                    b_bits);
     if (st != MXGEMM_OK) return st;
   }
 
   // ---- launches: [B re-pitch], scale repack, GEMM
   if (plan->pad_b) {
     mxg::pad_rows_kernel<<<launch_blocks(K * (plan->npad / 16), 256), 256, 0, stream>>>(
-        static_cast<const uint8_t *>(B), K, N, plan->npad, h->ws.ptr + off_b);
+        static_cast<const uint8_t *>(B), K, N, plan->npad, h->ws.ptr + off_b, plan->b_bits);
+    ++h->launches;
+  }
+  if (plan->a_bits < 8) {
+    mxg::pad_rows_kernel<<<launch_blocks(M * (K / 16), 256), 256, 0, stream>>>(
+        static_cast<const uint8_t *>(A), M, K, K, h->ws.ptr + plan->off_a, plan->a_bits);
     ++h->launches;
   }
   mxg::repack_scales_kernel<<<plan->blocks_a + plan->blocks_b, mxg::kRepackThreads, 0, stream>>>(
@@ -933,7 +959,7 @@ extern "C" int mxgemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A
   const int64_t npad = round_up(static_cast<size_t>(N), 16);
   // no stream-K split here: the scratch holds only the repacked scales and B
   const Split sp = plan_split(num_tiles, k_steps, nd->sm_count / CG, false, false, M);
-  const Sizes z = plan_sizes(a_chunks, b_chunks, pad_b, K, npad, sp, CG);
+  const Sizes z = plan_sizes(a_chunks, b_chunks, pad_b, K, npad, sp, CG, 0);
   const size_t off_b = z.off_b;
   const size_t ws_bytes = z.total;
   if (ws_bytes > kNoAllocScratchBytes) return MXGEMM_ERR_TOO_LARGE;
@@ -957,7 +983,7 @@ extern "C" int mxgemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A
   }
   Plan plan;
   st = build_plan(&ctx, &plan, M, N, K, A, A_scale, B, B_scale, C, use_acc, out_dtype, CG, m_tiles,
-                  n_tiles, k_steps, num_tiles, a_chunks, b_chunks, pad_b, npad, sp, z);
+                  n_tiles, k_steps, num_tiles, a_chunks, b_chunks, pad_b, npad, sp, z, 8, 8);
   if (st != MXGEMM_OK) return st;
   // the status word must start each call at zero
   if (cudaMemsetAsync(nd->status, 0, 2 * sizeof(int), stream) != cudaSuccess) {
@@ -966,7 +992,7 @@ extern "C" int mxgemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A
   }
   if (pad_b)
     mxg::pad_rows_kernel<<<launch_blocks(K * (npad / 16), 256), 256, 0, stream>>>(
-        static_cast<const uint8_t *>(B), K, N, npad, nd->scratch + off_b);
+        static_cast<const uint8_t *>(B), K, N, npad, nd->scratch + off_b, 8);
   mxg::repack_scales_kernel<<<plan.blocks_a + plan.blocks_b, mxg::kRepackThreads, 0, stream>>>(
       plan.ra, plan.rb, plan.blocks_a, plan.flags, plan.nflags);
   if (cudaGetLastError() != cudaSuccess) return MXGEMM_ERR_CUDA;

@@ -106,10 +106,25 @@ struct KParams {
   // half-width tail (see WorkIter): items [dp_tiles, dp_tiles + half_tiles)
   // of the whole-tile walk are 128-column halves of tiles dp_tiles, ...
   int half_tiles;
+  // element formats of A and B in instruction-descriptor position (bits
+  // 7-9 and 10-12); 0 for E4M3 x E4M3
+  uint32_t idesc_fmt;
 };
 
 // Instruction descriptor of tcgen05.mma.kind::mxf8f6f4.block_scale:
 // E4M3 x E4M3, A K-major, B N-major, UE8M0 scales, M x N, scale byte ids.
+// Other element formats are OR-ed in (fmt_bits).
+// Descriptor code of an element format of kind::mxf8f6f4 (PTX ISA,
+// instruction descriptor): E4M3 0, E5M2 1, E2M3 3, E3M2 4, E2M1 5; the
+// argument is the C interface's format number (E4M3, E5M2, E2M3, E3M2,
+// E2M1 = 0..4).
+__host__ __device__ constexpr uint32_t mma_format_code(int f) {
+  return f == 0 ? 0u : f == 1 ? 1u : f == 2 ? 3u : f == 3 ? 4u : 5u;
+}
+__host__ __device__ constexpr uint32_t fmt_bits(int a_fmt, int b_fmt) {
+  return (mma_format_code(a_fmt) << 7) | (mma_format_code(b_fmt) << 10);
+}
+
 __host__ __device__ constexpr uint32_t idesc_mxf8(int M, int N, int sfa_id, int sfb_id) {
   return (uint32_t(sfb_id & 3) << 4)     // B scale-factor byte id
          | (0u << 7)                     // A format E4M3
@@ -646,6 +661,7 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
     if (rank == 0) {
       const bool leader = elect_one() != 0;
       uint32_t phase = 0, acc_phase = 0;
+      const uint32_t fmt = p.idesc_fmt;  // element formats (0: E4M3 x E4M3)
       ClcRing ring = clc_ring;
       Sched<CG, C::CLC_SLOTS> wi(p, unit, units, &ring, false, rank, &wc);
       WorkItem w;
@@ -682,12 +698,12 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
         // B: N-major, 128-byte swizzle; 128-column chunks 16 KB apart,
         // 8-row K groups 1024 B apart; 32 rows (4 KB) per K=32.
         mma_mxf8<CG>(tmem + C::TM_ACC, smem_desc(sA, 0, 1024, 2), smem_desc(sB, 16384, 1024, 2),
-                     idesc_mxf8(128 * CG, 256, 0, 0), tSA, tSB, ks != w.kb);
+                     idesc_mxf8(128 * CG, 256, 0, 0) | fmt, tSA, tSB, ks != w.kb);
         const uint32_t ready = mbar_test_wait(bar_full + 8 * nst, nph);
 #pragma unroll
         for (int k = 1; k < 4; ++k)
           mma_mxf8<CG>(tmem + C::TM_ACC, smem_desc(sA + 32 * k, 0, 1024, 2),
-                       smem_desc(sB + 4096 * k, 16384, 1024, 2), idesc_mxf8(128 * CG, 256, k, k), tSA,
+                       smem_desc(sB + 4096 * k, 16384, 1024, 2), idesc_mxf8(128 * CG, 256, k, k) | fmt, tSA,
                        tSB, 1u);
         if constexpr (CG == 1) tc_commit(bar_empty + 8 * st);
         else tc_commit_pair(bar_empty + 8 * st, 0x3);
@@ -823,7 +839,7 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
 #pragma unroll
               for (int k = 0; k < 4; ++k)
                 mma_mxf8<CG>(tmem + C::TM_ACC, smem_desc(sA + 32 * k, 0, 1024, 2),
-                             bdesc | ((sB + bstep * k) >> 4), idesc_mxf8(128 * CG, 128, k, k), tSA,
+                             bdesc | ((sB + bstep * k) >> 4), idesc_mxf8(128 * CG, 128, k, k) | fmt, tSA,
                              tSB + sfb_off, (k0 != w.kb || k != 0) ? 1u : 0u);
               if constexpr (CG == 1) tc_commit(bar_empty + 8 * s);
               else tc_commit_pair(bar_empty + 8 * s, 0x3);

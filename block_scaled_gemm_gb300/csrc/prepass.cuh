@@ -82,12 +82,18 @@ __global__ void __launch_bounds__(kRepackThreads)
   }
 }
 
-// Copy B [K][N] into [K][Npad] (Npad a multiple of 16) so that its rows meet
-// the 16-byte stride rule of tensor-map loads; the pad columns are zero.
-// Each thread writes 16 bytes; it reads them with the widest loads the
-// source row's alignment allows (8, 4 or 1 byte).
+// Re-pitch the rows of an operand into the workspace: `rows` rows of `N`
+// one-byte elements become rows of `Npad` bytes (a multiple of 16, for the
+// 16-byte stride rule of tensor-map loads; the pad columns are zero).  With
+// nbits = 6 or 4 the elements are sub-byte codes (low bits of each byte) and
+// every group of 16 consecutive elements is packed, element i at bits
+// [nbits*i, nbits*i + nbits) little-endian, into the first 2*nbits bytes of
+// its 16-byte group, the rest zero: the shared-memory form that the scaled
+// MMA reads for 6- and 4-bit operands (one 16-byte group per 16 elements,
+// as for 8-bit ones).  Each thread writes 16 bytes; it reads them with the
+// widest loads the source row's alignment allows (8, 4 or 1 byte).
 __global__ void pad_rows_kernel(const uint8_t *__restrict__ B, int64_t rows, int64_t N,
-                                int64_t Npad, uint8_t *__restrict__ out) {
+                                int64_t Npad, uint8_t *__restrict__ out, int nbits) {
   const int64_t per_row = Npad / 16;
   const int64_t total = rows * per_row;
   griddep_launch_dependents();
@@ -112,6 +118,25 @@ __global__ void pad_rows_kernel(const uint8_t *__restrict__ B, int64_t rows, int
         const uint32_t b = c0 + j < N ? src[j] : 0u;
         w[j >> 2] |= b << (8 * (j & 3));
       }
+    }
+    if (nbits < 8) {
+      const uint64_t mask = (1ull << nbits) - 1;
+      uint64_t lo = 0, hi = 0;
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const uint64_t v = (w[j >> 2] >> (8 * (j & 3))) & mask;
+        const int pos = j * nbits;
+        if (pos < 64) {
+          lo |= v << pos;
+          if (pos + nbits > 64) hi |= v >> (64 - pos);
+        } else {
+          hi |= v << (pos - 64);
+        }
+      }
+      w[0] = static_cast<uint32_t>(lo);
+      w[1] = static_cast<uint32_t>(lo >> 32);
+      w[2] = static_cast<uint32_t>(hi);
+      w[3] = static_cast<uint32_t>(hi >> 32);
     }
     *reinterpret_cast<uint4 *>(out + r * Npad + c0) = make_uint4(w[0], w[1], w[2], w[3]);
   }

@@ -90,8 +90,27 @@ typedef enum {
    * FP32 partials (kept in the handle's workspace) before it stores C;
    * otherwise, when they fill at most half a wave, each is computed as two
    * 128-column halves.  0: every tile is computed whole. */
-  MXGEMM_OPT_STREAM_K = 5
+  MXGEMM_OPT_STREAM_K = 5,
+  /* Element format of A (MXGEMM_OPT_A_FORMAT) and of B
+   * (MXGEMM_OPT_B_FORMAT), an mxgemm_format_t; default MXGEMM_FMT_E4M3.
+   * The formats are those of the MX family that the tensor cores' scaled
+   * MMA takes ("TLX API Quick Reference", section "Matrix Multiply (MMA)":
+   * the A_format / B_format strings of async_dot_scaled).  A and B may
+   * differ. */
+  MXGEMM_OPT_A_FORMAT = 6,
+  MXGEMM_OPT_B_FORMAT = 7
 } mxgemm_option_t;
+
+/* Element formats (OCP Microscaling Formats v1.0).  Every element occupies
+ * one byte in A and B, also for the 6- and 4-bit formats, whose code sits
+ * in the low bits of its byte (the upper bits are ignored). */
+typedef enum {
+  MXGEMM_FMT_E4M3 = 0, /* FP8, max 448, no infinities */
+  MXGEMM_FMT_E5M2 = 1, /* FP8, max 57344, with infinities */
+  MXGEMM_FMT_E2M3 = 2, /* FP6, max 7.5 */
+  MXGEMM_FMT_E3M2 = 3, /* FP6, max 28 */
+  MXGEMM_FMT_E2M1 = 4  /* FP4, max 6 */
+} mxgemm_format_t;
 
 /* Create a handle bound to CUDA device `device`.  Fails with
  * MXGEMM_ERR_UNSUPPORTED_DEVICE unless the device is compute capability 10.3
