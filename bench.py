@@ -47,6 +47,7 @@ UNIT = "TFLOP/s"
 WORKLOAD = "square_4096"
 FP8_OVER_BF16 = 2.0  # nominal dense MXFP8 / BF16 tensor rate (4.5 / 2.25 PFLOP/s)
 FALLBACK_BF16_BURST = 1900.0  # TFLOP/s, used only when MEASURED_PEAKS.json is absent
+FORMATS = ["e4m3", "e5m2", "e2m3", "e3m2", "e2m1"]  # C interface order (mxgemm_format_t)
 FALLBACK_HBM_GBS = 6800.0     # GB/s, used only when MEASURED_PEAKS.json is absent
 KERNEL_SOURCES = ["block_scaled_gemm_gb300/csrc/mxgemm_kernel.cuh",
                   "block_scaled_gemm_gb300/csrc/ptx.cuh"]
@@ -334,6 +335,8 @@ def run_mx(args, world, rank, local):
     _build.build()
 
     prob = mx_inputs.WORKLOADS[args.workload]()
+    if (args.a_format, args.b_format) != ("e4m3", "e4m3"):
+        prob = mx_inputs.with_formats(prob, args.a_format, args.b_format)
     M, N, K = prob.M, prob.N, prob.K
     out_code = mx.OUT_F32 if prob.out_dtype == "f32" else mx.OUT_BF16
     tdt = torch.float32 if prob.out_dtype == "f32" else torch.bfloat16
@@ -349,6 +352,8 @@ def run_mx(args, world, rank, local):
     h = mx.mxgemm_create(local)
     if args.mode is not None:
         mx.mxgemm_set_option(h, mx.OPT_MODE, args.mode)
+    mx.mxgemm_set_option(h, mx.OPT_A_FORMAT, FORMATS.index(args.a_format))
+    mx.mxgemm_set_option(h, mx.OPT_B_FORMAT, FORMATS.index(args.b_format))
 
     def step():
         if flush is not None:
@@ -422,7 +427,8 @@ def run_mx(args, world, rank, local):
         import oracle
         g = np.random.default_rng(1)
         I, J = g.integers(0, M, 256), g.integers(0, N, 256)
-        ref, bound = oracle.points(prob.A, prob.As, prob.B, prob.Bs, I, J)
+        ref, bound = oracle.points(prob.A, prob.As, prob.B, prob.Bs, I, J,
+                                   a_fmt=args.a_format, b_fmt=args.b_format)
         got = C.float().cpu().numpy()[I, J]
         acc = oracle.accept(got, ref, bound, "f32" if prob.out_dtype == "f32" else "bf16")
         parity = {"points": int(I.size), "ok": acc["ok"],
@@ -483,13 +489,14 @@ def run_mx(args, world, rank, local):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "mxfp8",
             "data": "synthetic",
             "config": {"workload": args.workload, "M": M, "N": N, "K": K,
-                       "a": "E4M3 M x K (K-major), scales E8M0 per 32 K",
-                       "b": "E4M3 K x N (N-major), scales E8M0 per 32 K",
+                       "a": f"{args.a_format.upper()} M x K (K-major), scales E8M0 per 32 K",
+                       "b": f"{args.b_format.upper()} K x N (N-major), scales E8M0 per 32 K",
                        "out": prob.out_dtype, "use_acc": 0, "accumulate": "fp32",
                        "l2": ("flushed between timed steps (256 MiB write, outside the events)"
                               if flush is not None else "not flushed"),
                        "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
-                       "tile_mode": args.mode if args.mode is not None else "auto"},
+                       "tile_mode": args.mode if args.mode is not None else "auto",
+                       "a_format": args.a_format, "b_format": args.b_format},
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
@@ -514,6 +521,8 @@ def main(argv=None):
     import mx_inputs
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(mx_inputs.WORKLOADS))
     ap.add_argument("--mode", type=int, default=None, help="tile mode: 1 = 1-CTA, 2 = CTA pair")
+    ap.add_argument("--a-format", default="e4m3", choices=FORMATS)
+    ap.add_argument("--b-format", default="e4m3", choices=FORMATS)
     ap.add_argument("--no-flush", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle baseline and spot parity")
     ap.add_argument("--e2e-steps", type=int, default=20)

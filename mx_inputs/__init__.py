@@ -242,6 +242,35 @@ def skinny(M: int, seed: int = 0, N: int = 8192, K: int = 8192) -> Problem:
     return Problem(f"skinny_{M}x{N}x{K}", M, N, K, A, As, B, Bs, "f32", False)
 
 
+# bits of the element codes of each format (one code per byte)
+FORMAT_BITS = {"e4m3": 8, "e5m2": 8, "e2m3": 6, "e3m2": 6, "e2m1": 4}
+
+
+def format_codes(fmt: str, shape, g: torch.Generator) -> torch.Tensor:
+    """Uniform random element codes of format fmt, one per byte, without the
+    E4M3 NaN codes or the E5M2 infinity/NaN codes (sub-byte codes in the low
+    bits, the high bits zero)."""
+    nb = FORMAT_BITS[fmt]
+    c = torch.randint(0, 1 << nb, shape, generator=g, dtype=torch.int32).to(torch.uint8)
+    if fmt == "e4m3":
+        c[(c & 0x7F) == 0x7F] = 0x3F
+    elif fmt == "e5m2":
+        c[(c & 0x7C) == 0x7C] = 0x3C
+    return c
+
+
+def with_formats(p: Problem, a_fmt: str, b_fmt: str, seed: int = 0) -> Problem:
+    """The same problem shape and scales with A and B redrawn as random codes
+    of the given element formats (an E4M3 operand keeps its codes)."""
+    g = _gen(seed + 1)
+    A = p.A if a_fmt == "e4m3" else format_codes(a_fmt, tuple(p.A.shape), g)
+    B = p.B if b_fmt == "e4m3" else format_codes(b_fmt, tuple(p.B.shape), g)
+    q = Problem(f"{p.name}_{a_fmt}x{b_fmt}", p.M, p.N, p.K, A, p.As, B, p.Bs, p.out_dtype,
+                p.use_acc, p.mode, p.k_chunks, dict(p.meta))
+    q.meta["formats"] = (a_fmt, b_fmt)
+    return q
+
+
 WORKLOADS = {
     "square_256": square_256,
     "square_4096": square_4096,
