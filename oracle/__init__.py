@@ -73,6 +73,10 @@ def _load():
         lib.mxo_points_fmt.argtypes = [i64, i64, i64, u8p, u8p, u8p, u8p, i64,
                                        i64p, i64p, f64p, f64p, ci, ci, ci]
         lib.mxo_points_fmt.restype = ci
+        lib.mxo_e4m3_rne.argtypes = [ctypes.c_double]
+        lib.mxo_e4m3_rne.restype = ctypes.c_uint8
+        lib.mxo_quantize_e4m3.argtypes = [i64, i64, f64p, ci, u8p, u8p]
+        lib.mxo_quantize_e4m3.restype = ci
         lib.mxo_round_f32.argtypes = [ctypes.c_double]
         lib.mxo_round_f32.restype = ctypes.c_float
         lib.mxo_round_bf16.argtypes = [ctypes.c_double]
@@ -179,6 +183,28 @@ def points(A, As, B, Bs, I, J, c_in=None, threads: int | None = None,
         ref += c
         bnd += np.abs(c)
     return ref, bnd
+
+
+def e4m3_rne(y: float) -> int:
+    """E4M3 code nearest to y after clamping to +-448, ties to even."""
+    return int(_load().mxo_e4m3_rne(float(y)))
+
+
+def quantize_e4m3(x, along_cols: bool = False):
+    """MX quantization of a real R x C matrix (any float dtype, values taken
+    exactly) to E4M3 codes with E8M0 scales per 32 values: along each row
+    (scales R x C/32) or, with along_cols, down each column (scales
+    C x R/32, row j for column j).  Returns (codes uint8 R x C, scales)."""
+    if hasattr(x, "numpy"):  # torch tensor (bfloat16 and float32 widen exactly)
+        x = x.detach().to("cpu").double().numpy()
+    xd = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
+    R, C = xd.shape
+    codes = np.empty((R, C), dtype=np.uint8)
+    scales = np.empty((C, R // 32) if along_cols else (R, C // 32), dtype=np.uint8)
+    rc = _load().mxo_quantize_e4m3(R, C, _ptr(xd), int(bool(along_cols)), _ptr(codes), _ptr(scales))
+    if rc != 0:
+        raise ValueError("mxo_quantize_e4m3 rejected its arguments")
+    return codes, scales
 
 
 def round_f32(x) -> np.ndarray:

@@ -367,3 +367,85 @@ uint16_t mxo_round_bf16(double x) {
 void mxo_round_bf16_array(const double *x, uint16_t *out, int64_t n) {
   for (int64_t i = 0; i < n; ++i) out[i] = mxo_round_bf16(x[i]);
 }
+
+/* ---------------------------------------------------------------------- */
+/* MX quantization of a real matrix to E4M3 codes with E8M0 block scales.  */
+/* ---------------------------------------------------------------------- */
+/*
+ * Per block of 32 consecutive values x_0..x_31 (along a row, or down a
+ * column), the recipe of the benchmark spec (OCP MX v1.0 conversion with an
+ * E4M3 maximum of 448):
+ *   amax  = max |x_i|
+ *   scale = clamp(127 + ceil(log2(amax / 448)), 0, 254), and 127 if amax = 0
+ *   code_i = E4M3 code nearest to clamp(x_i * 2^(127 - scale), -448, 448),
+ *            ties to even (the sign of x_i kept, also for zero)
+ * Written from those definitions in double: every step is exact except the
+ * final round-to-nearest-even, which rint() performs on an exact value.
+ * Inputs must be finite.
+ */
+
+/* smallest integer t with amax <= 448 * 2^t, for amax > 0 (exact) */
+static int ceil_log2_over_448(double amax) {
+  int E;
+  const double f = frexp(amax, &E); /* amax = f * 2^E, f in [0.5, 1) */
+  /* 448 * 2^t = 0.875 * 2^(t + 9) */
+  return f <= 0.875 ? E - 9 : E - 8;
+}
+
+uint8_t mxo_e4m3_rne(double y) {
+  const uint8_t sign = signbit(y) ? 0x80u : 0u;
+  double a = fabs(y);
+  if (a > 448.0) a = 448.0;
+  if (a < ldexp(1.0, -6)) {
+    /* subnormal range: multiples of 2^-9 (q = 8 is the smallest normal) */
+    const double q = rint(ldexp(a, 9));
+    return (uint8_t)(sign | (uint8_t)q);
+  }
+  int E;
+  (void)frexp(a, &E);          /* a in [2^(E-1), 2^E) */
+  int e = E - 1;               /* unbiased exponent */
+  double q = rint(ldexp(a, 3 - e)) - 8.0; /* mantissa in eighths */
+  if (q >= 8.0) {
+    q = 0.0;
+    e += 1;
+  }
+  return (uint8_t)(sign | (uint8_t)((e + 7) << 3) | (uint8_t)q);
+}
+
+/* x: R x C row-major values.  along_cols = 0: blocks of 32 along each row
+ * (C % 32 == 0), scales R x (C/32); along_cols = 1: blocks of 32 down each
+ * column (R % 32 == 0), scales C x (R/32), row j holding column j's scales.
+ * codes: R x C.  Returns 0, or -1 on a bad argument. */
+int mxo_quantize_e4m3(int64_t R, int64_t C, const double *x, int along_cols, uint8_t *codes,
+                      uint8_t *scales) {
+  if (R < 0 || C < 0 || (along_cols ? R % 32 : C % 32) != 0) return -1;
+  const int64_t nblk = along_cols ? C * (R / 32) : R * (C / 32);
+  for (int64_t b = 0; b < nblk; ++b) {
+    /* element i of block b at x[base + i * step] */
+    int64_t base, step;
+    if (along_cols) {
+      const int64_t j = b / (R / 32), rb = b % (R / 32);
+      base = rb * 32 * C + j;
+      step = C;
+    } else {
+      const int64_t r = b / (C / 32), cb = b % (C / 32);
+      base = r * C + cb * 32;
+      step = 1;
+    }
+    double amax = 0.0;
+    for (int i = 0; i < 32; ++i) {
+      const double a = fabs(x[base + i * step]);
+      if (a > amax) amax = a;
+    }
+    int s = 127;
+    if (amax > 0.0) {
+      s = 127 + ceil_log2_over_448(amax);
+      if (s < 0) s = 0;
+      if (s > 254) s = 254;
+    }
+    scales[b] = (uint8_t)s; /* b enumerates blocks in the scales' own order */
+    for (int i = 0; i < 32; ++i)
+      codes[base + i * step] = mxo_e4m3_rne(ldexp(x[base + i * step], 127 - s));
+  }
+  return 0;
+}

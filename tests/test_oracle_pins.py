@@ -371,3 +371,75 @@ def test_mixed_format_product_brute_force(fa, fb):
                         for k in range(K))
             assert abs(Fraction(ref[i, j]) - exact) <= Fraction(K, 2 ** 53) * absum
             assert float(absum) == pytest.approx(bound[i, j], rel=1e-15)
+
+
+# ---------------------------------------------------------------- MX quantizer
+
+def test_e4m3_rne_matches_library_cast():
+    # torch's float8_e4m3fn cast rounds to nearest even inside +-448
+    g = torch.Generator().manual_seed(23)
+    x = torch.cat([
+        torch.randn(20000, generator=g) * 100,
+        torch.randn(20000, generator=g) * 0.01,          # subnormal range
+        (torch.randint(-3584, 3585, (20000,), generator=g) / 8.0),  # many exact ties
+        torch.tensor([0.0, -0.0, 448.0, -448.0, 2.0 ** -9, 2.0 ** -10, 3 * 2.0 ** -11]),
+    ]).clamp(-448, 448).to(torch.float32)
+    lib = x.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    ours = np.array([oracle.e4m3_rne(float(v)) for v in x.numpy()], dtype=np.uint8)
+    assert np.array_equal(lib, ours)
+
+
+def _quantizer_cases():
+    out = []
+    for line in (GOLDEN / "mx_quantizer_scales.txt").read_text().splitlines():
+        if not line.strip() or line.startswith("#"):
+            continue
+        a, sc = line.split()
+        out.append((float(np.float32(float(a))), int(sc)))
+    return out
+
+
+@pytest.mark.parametrize("amax,scale", _quantizer_cases())
+def test_quantizer_scale_hand_cases(amax, scale):
+    x = np.zeros((1, 32), dtype=np.float32)
+    x[0, 5] = -amax
+    codes, scales = oracle.quantize_e4m3(x)
+    assert scales[0, 0] == scale
+    # the largest element lands within E4M3's range, at 448 / 2^k scale
+    if amax > 0 and 0 < scale < 254:
+        v = abs(oracle.e4m3(codes[0, 5])) * 2.0 ** (scale - 127)
+        assert v <= 448 * 2.0 ** (scale - 127)
+        assert abs(v - amax) <= amax * 2.0 ** -4 + 2.0 ** (scale - 127 - 9)
+
+
+def test_quantizer_matches_input_recipe_rows_and_columns():
+    # the input generator's recipe uses torch's float8 cast: an independent
+    # implementation of the same conversion
+    g = torch.Generator().manual_seed(29)
+    x = torch.randn((96, 256), generator=g) * torch.exp(torch.randn((96, 1), generator=g) * 4)
+    codes, scales = oracle.quantize_e4m3(x)
+    rc, rs = mi.quantize_rows(x)
+    assert np.array_equal(codes, rc.numpy()) and np.array_equal(scales, rs.numpy())
+    # down the columns of a K x N matrix = along the rows of its transpose
+    xt = x[:, :64].contiguous()               # K = 96, N = 64
+    c2, s2 = oracle.quantize_e4m3(xt, along_cols=True)
+    rct, rst = mi.quantize_rows(xt.t().contiguous())
+    assert np.array_equal(c2, rct.numpy().T) and np.array_equal(s2, rst.numpy())
+
+
+def test_quantizer_roundtrip_error_bound():
+    # decoded value within half an E4M3 step of the scaled input (or the
+    # subnormal step), and every block's largest magnitude in (224, 448]
+    g = torch.Generator().manual_seed(31)
+    x = (torch.randn((8, 320), generator=g) * 37.0).numpy().astype(np.float32)
+    codes, scales = oracle.quantize_e4m3(x)
+    for r in range(8):
+        for c in range(320):
+            s = int(scales[r, c // 32])
+            y = float(x[r, c]) * 2.0 ** (127 - s)
+            d = oracle.e4m3(codes[r, c])
+            step = 2.0 ** -9 if abs(y) < 2.0 ** -6 else 2.0 ** (np.floor(np.log2(abs(y))) - 3)
+            assert abs(d - y) <= step / 2 + 1e-300
+        for b in range(10):
+            amax = np.abs(x[r, 32 * b:32 * b + 32]).max() * 2.0 ** (127 - int(scales[r, b]))
+            assert 224.0 < amax <= 448.0
