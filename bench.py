@@ -319,6 +319,78 @@ def run_reference(args, world, rank):
     return 0
 
 
+def run_quantize(args, world, rank, local):
+    """The MX quantizer (mxgemm_quantize) on an R x C FP32 or BF16 matrix:
+    HBM-bound, reported in GB/s of algorithmic traffic (read X, write codes
+    and scales), checked bit for bit against the oracle on a row sample."""
+    import numpy as np
+    import torch
+    import block_scaled_gemm_gb300 as mx
+    from block_scaled_gemm_gb300 import _build
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py: no CUDA device (the quantizer has no CPU path)")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = init_dist(world, True)
+    _build.build()
+    R, C = args.q_rows, args.q_cols
+    dt = torch.bfloat16 if args.q_dtype == "bf16" else torch.float32
+    g = torch.Generator().manual_seed(0)
+    x = (torch.randn((R, C), generator=g) * torch.exp(torch.randn((R, 1), generator=g) * 4)).to(dt)
+    X = x.to(dev)
+    codes = torch.empty((R, C), dtype=torch.uint8, device=dev)
+    scales = torch.empty((R, C // 32), dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if not args.no_flush else None
+    stream = torch.cuda.current_stream(dev)
+    nbytes = R * C * x.element_size() + R * C + R * C // 32
+    for _ in range(args.warmup):
+        mx.mxgemm_quantize(X, R, C, codes, scales, stream=stream)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    sampler = ClockSampler(None).start()
+    torch.cuda.synchronize(dev)
+    barrier(dist)
+    t_begin = time.perf_counter()
+    for a, b in ev:
+        if flush is not None:
+            flush.zero_()
+        a.record(stream)
+        mx.mxgemm_quantize(X, R, C, codes, scales, stream=stream)
+        b.record(stream)
+    torch.cuda.synchronize(dev)
+    t_end = time.perf_counter()
+    sampler.stop()
+    ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in ev), dist, dev)
+    gbs = nbytes * world * args.steps / (ms * 1e-3) / 1e9
+    hbm, hbm_src = measured_hbm()
+    parity = None
+    if rank == 0:
+        import oracle
+        rows = np.random.default_rng(1).integers(0, R, 64)
+        rc, rs = oracle.quantize_e4m3(x[rows])
+        parity = {"rows": int(rows.size),
+                  "codes_equal": bool(np.array_equal(codes.cpu().numpy()[rows], rc)),
+                  "scales_equal": bool(np.array_equal(scales.cpu().numpy()[rows], rs))}
+        print(json.dumps({
+            "metric": "MX quantizer GB/s (read X + write E4M3 codes + E8M0 scales)",
+            "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": args.q_dtype, "data": "synthetic",
+            "config": {"workload": f"quantize_{R}x{C}_{args.q_dtype}", "R": R, "C": C,
+                       "blocks": "32 along rows",
+                       "l2": "flushed between timed steps" if flush is not None else "not flushed"},
+            "roofline": {"bound": "hbm", "achieved": gbs / world, "peak": hbm, "unit": "GB/s",
+                         "frac": gbs / world / hbm, "peak_source": hbm_src,
+                         "algorithmic_bytes": nbytes, "kernel": "mx_quantize_rows_kernel"},
+            "gpu_launches": args.steps,
+            "clocks": sampler.summary(t_begin, t_end),
+            "parity": parity,
+        }), flush=True)
+    if dist is not None:
+        dist.destroy_process_group()
+    return 0
+
+
 def run_mx(args, world, rank, local):
     import numpy as np
     import torch
@@ -521,6 +593,11 @@ def main(argv=None):
     import mx_inputs
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(mx_inputs.WORKLOADS))
     ap.add_argument("--mode", type=int, default=None, help="tile mode: 1 = 1-CTA, 2 = CTA pair")
+    ap.add_argument("--op", default="gemm", choices=["gemm", "quantize"],
+                    help="gemm (the headline) or the MX quantizer")
+    ap.add_argument("--q-rows", type=int, default=8192)
+    ap.add_argument("--q-cols", type=int, default=8192)
+    ap.add_argument("--q-dtype", default="f32", choices=["f32", "bf16"])
     ap.add_argument("--a-format", default="e4m3", choices=FORMATS)
     ap.add_argument("--b-format", default="e4m3", choices=FORMATS)
     ap.add_argument("--no-flush", action="store_true")
@@ -535,6 +612,8 @@ def main(argv=None):
     world, rank, local = dist_env()
     if args.impl == "reference":
         return run_reference(args, world, rank)
+    if args.op == "quantize":
+        return run_quantize(args, world, rank, local)
     return run_mx(args, world, rank, local)
 
 

@@ -27,7 +27,7 @@ __all__ = [
     "FMT_E2M3", "FMT_E3M2", "FMT_E2M1", "MxgemmError", "library", "library_path", "mxgemm_create", "mxgemm_run",
     "mxgemm_destroy", "mxgemm_set_option", "mxgemm_get_device_status", "mxgemm_status_string",
     "mxgemm_set_profile_events", "mxgemm_get_launch_count", "mxgemm_run_noalloc", "mxgemm_run_host",
-    "EXPORTED_SYMBOLS", "Gemm",
+    "mxgemm_quantize", "IN_F32", "IN_BF16", "EXPORTED_SYMBOLS", "Gemm",
 ]
 
 OUT_F32 = 0
@@ -61,7 +61,7 @@ ERR_TOO_LARGE = 7
 EXPORTED_SYMBOLS = (
     "mxgemm_create", "mxgemm_run", "mxgemm_destroy", "mxgemm_set_option",
     "mxgemm_get_device_status", "mxgemm_status_string", "mxgemm_set_profile_events",
-    "mxgemm_get_launch_count", "mxgemm_run_noalloc", "mxgemm_run_host",
+    "mxgemm_get_launch_count", "mxgemm_run_noalloc", "mxgemm_run_host", "mxgemm_quantize",
 )
 
 _lib = None
@@ -102,6 +102,8 @@ def library():
         lib.mxgemm_set_profile_events.restype = i32
         lib.mxgemm_get_launch_count.argtypes = [vp, ctypes.POINTER(i64)]
         lib.mxgemm_get_launch_count.restype = i32
+        lib.mxgemm_quantize.argtypes = [vp, i32, i64, i64, i32, vp, vp, vp]
+        lib.mxgemm_quantize.restype = i32
         lib.mxgemm_run_host.argtypes = [vp, i64, i64, i64, vp, vp, vp, vp, vp, i32, i32, vp]
         lib.mxgemm_run_host.restype = i32
         lib.mxgemm_run_noalloc.argtypes = [i64, i64, i64, vp, vp, vp, vp, vp, i32, i32, vp]
@@ -150,6 +152,25 @@ def mxgemm_run(h, M, N, K, A, A_scale, B, B_scale, C, use_acc=0, out_dtype=OUT_F
                               _stream(stream))
     if check:
         _check(st, "mxgemm_run")
+    return st
+
+
+IN_F32 = 0
+IN_BF16 = 1
+
+
+def mxgemm_quantize(X, R, C, codes, scales, along_cols=False, x_dtype=None, stream=None,
+                    check: bool = True) -> int:
+    """MX-quantize the R x C device matrix X (float32 or bfloat16) into E4M3
+    codes (R x C bytes) and E8M0 scales per 32 values, along the rows
+    (scales R x C/32) or down the columns (scales C x R/32)."""
+    if x_dtype is None:
+        import torch
+        x_dtype = IN_BF16 if getattr(X, "dtype", None) == torch.bfloat16 else IN_F32
+    st = library().mxgemm_quantize(_ptr(X), int(x_dtype), int(R), int(C), int(bool(along_cols)),
+                                   _ptr(codes), _ptr(scales), _stream(stream))
+    if check:
+        _check(st, "mxgemm_quantize")
     return st
 
 

@@ -9,6 +9,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
@@ -18,6 +19,7 @@
 #include "mxgemm.h"
 #include "mxgemm_kernel.cuh"
 #include "prepass.cuh"
+#include "quantize.cuh"
 
 namespace {
 
@@ -665,6 +667,63 @@ int mxgemm_destroy(mxgemm_handle_t h) {
 }
 
 }  // extern "C"
+
+// ===========================================================================
+// mxgemm_quantize: MX quantization of a real matrix on the GPU.
+// ===========================================================================
+
+extern "C" int mxgemm_quantize(const void *X, int x_dtype, int64_t R, int64_t C, int along_cols,
+                               void *codes, void *scales, mxgemm_stream_t stream_) {
+  const int64_t lim = int64_t(1) << 31;
+  if (R < 0 || C < 0 || R >= lim || C >= lim) return MXGEMM_ERR_INVALID_VALUE;
+  if (x_dtype != MXGEMM_IN_F32 && x_dtype != MXGEMM_IN_BF16) return MXGEMM_ERR_INVALID_VALUE;
+  if (along_cols != 0 && along_cols != 1) return MXGEMM_ERR_INVALID_VALUE;
+  if ((along_cols ? R % 32 : C % 32) != 0) return MXGEMM_ERR_INVALID_VALUE;
+  if (R == 0 || C == 0) return MXGEMM_OK;
+  if (!X || !codes || !scales) return MXGEMM_ERR_INVALID_VALUE;
+  if (reinterpret_cast<uintptr_t>(X) % 16 || reinterpret_cast<uintptr_t>(codes) % 16)
+    return MXGEMM_ERR_MISALIGNED;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return MXGEMM_ERR_CUDA;
+  }
+  if (!on_device(X, dev) || !on_device(codes, dev) || !on_device(scales, dev))
+    return MXGEMM_ERR_INVALID_VALUE;
+  int sms = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return MXGEMM_ERR_CUDA;
+  }
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  uint8_t *cd = static_cast<uint8_t *>(codes), *sc = static_cast<uint8_t *>(scales);
+  // grid: a few resident blocks per SM, grid-stride loops over the work
+  const int threads = 256;
+  if (!along_cols) {
+    const int64_t nblocks = R * (C / 32);
+    const int64_t warps_needed = (nblocks + 7) / 8;  // a warp takes 8 blocks
+    int grid = static_cast<int>(std::min<int64_t>(cdiv(warps_needed, threads / 32), int64_t(sms) * 8));
+    if (grid < 1) grid = 1;
+    if (x_dtype == MXGEMM_IN_F32)
+      mxg::mx_quantize_rows_kernel<float><<<grid, threads, 0, stream>>>(
+          static_cast<const float *>(X), nblocks, cd, sc);
+    else
+      mxg::mx_quantize_rows_kernel<__nv_bfloat16><<<grid, threads, 0, stream>>>(
+          static_cast<const __nv_bfloat16 *>(X), nblocks, cd, sc);
+  } else {
+    const int64_t work = (R / 32) * C;
+    int grid = static_cast<int>(std::min<int64_t>(cdiv(work, threads), int64_t(sms) * 8));
+    if (grid < 1) grid = 1;
+    if (x_dtype == MXGEMM_IN_F32)
+      mxg::mx_quantize_cols_kernel<float><<<grid, threads, 0, stream>>>(
+          static_cast<const float *>(X), R, C, cd, sc);
+    else
+      mxg::mx_quantize_cols_kernel<__nv_bfloat16><<<grid, threads, 0, stream>>>(
+          static_cast<const __nv_bfloat16 *>(X), R, C, cd, sc);
+  }
+  if (cudaGetLastError() != cudaSuccess) return MXGEMM_ERR_CUDA;
+  return MXGEMM_OK;
+}
 
 // ===========================================================================
 // mxgemm_run_host: operands and result in host memory.

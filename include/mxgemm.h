@@ -154,6 +154,28 @@ int mxgemm_run_host(mxgemm_handle_t h, int64_t M, int64_t N, int64_t K,
                     const void *B_scale, void *C, int use_acc, int out_dtype,
                     mxgemm_stream_t stream);
 
+/* MX quantization on the GPU: a real matrix X (R x C, row-major, dense) to
+ * E4M3 codes with one E8M0 scale per block of 32 values -- the operands of
+ * mxgemm_run.  Per block (OCP Microscaling Formats v1.0 conversion, E4M3
+ * maximum 448):
+ *   scale  = clamp(127 + ceil(log2(amax / 448)), 0, 254); 127 when amax = 0
+ *   code_i = nearest E4M3 value to clamp(x_i * 2^(127 - scale), +-448),
+ *            ties to even, sign kept.
+ *   x_dtype    : MXGEMM_IN_F32 or MXGEMM_IN_BF16.
+ *   along_cols : 0 -> blocks run along each row (C % 32 == 0); scales is
+ *                R x (C/32): X = A (M x K) gives A and A_scale.
+ *                1 -> blocks run down each column (R % 32 == 0); scales is
+ *                C x (R/32), row j holding column j's scales: X = B (K x N)
+ *                gives B and B_scale.
+ *   X, codes, scales : device pointers; X and codes 16-byte aligned
+ *                (MXGEMM_ERR_MISALIGNED).  codes is R x C bytes.
+ * X must hold finite values (the codes of non-finite inputs are
+ * unspecified).  Needs no handle: nothing is allocated; enqueued on
+ * `stream`.  Errors as for mxgemm_run. */
+typedef enum { MXGEMM_IN_F32 = 0, MXGEMM_IN_BF16 = 1 } mxgemm_in_dtype_t;
+int mxgemm_quantize(const void *X, int x_dtype, int64_t R, int64_t C, int along_cols,
+                    void *codes, void *scales, mxgemm_stream_t stream);
+
 /* Set an option (mxgemm_option_t) on the handle; applies to later runs. */
 int mxgemm_set_option(mxgemm_handle_t h, int option, int64_t value);
 
