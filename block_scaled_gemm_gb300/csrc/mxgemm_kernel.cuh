@@ -820,7 +820,8 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
                                                        0x02 | ((w.tile & 0xFFFF) << 16)));
           if (!run) break;
           tc_fence_after();
-          const uint32_t sfb_off = 4u * static_cast<uint32_t>(w.half);
+          // the B scales of this half: one of the chunk's two 128-row halves
+          const uint32_t sfb_half = 512u * static_cast<uint32_t>(w.half);
           for (int k0 = w.kb; k0 < w.ke; ++k0) {
             if (!__all_sync(0xFFFFFFFFu, wait_phase<false>(bar_full + 8 * s, ph, wc, 0x03 | (s << 8)))) {
               run = false;
@@ -833,14 +834,15 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
               const uint32_t sSB = base + C::OFF_SFB + s * C::SFB_BYTES;
               const uint32_t tSA = tmem + C::TM_SFA + 4 * s;
               const uint32_t tSB = tmem + C::TM_SFB + 8 * s;
+              // two scale copies, not three: at N = 128 the copies are not
+              // hidden behind the MMAs
               tmem_cp_32x128b_x4<CG>(tSA, smem_desc(sSA, 0, 128, 0));
-              tmem_cp_32x128b_x4<CG>(tSB, smem_desc(sSB, 0, 128, 0));
-              tmem_cp_32x128b_x4<CG>(tSB + 4, smem_desc(sSB + 512, 0, 128, 0));
+              tmem_cp_32x128b_x4<CG>(tSB, smem_desc(sSB + sfb_half, 0, 128, 0));
 #pragma unroll
               for (int k = 0; k < 4; ++k)
                 mma_mxf8<CG>(tmem + C::TM_ACC, smem_desc(sA + 32 * k, 0, 1024, 2),
                              bdesc | ((sB + bstep * k) >> 4), idesc_mxf8(128 * CG, 128, k, k) | fmt, tSA,
-                             tSB + sfb_off, (k0 != w.kb || k != 0) ? 1u : 0u);
+                             tSB, (k0 != w.kb || k != 0) ? 1u : 0u);
               if constexpr (CG == 1) tc_commit(bar_empty + 8 * s);
               else tc_commit_pair(bar_empty + 8 * s, 0x3);
             }
