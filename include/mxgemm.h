@@ -12,10 +12,12 @@
  * Microscaling Formats specification v1.0.  Accumulation is FP32.
  *
  * Layouts (every pointer is caller-owned DEVICE memory on the handle's GPU,
- * dense row-major, no leading-dimension parameters):
- *   A       : M x K      uint8 E4M3 codes, K contiguous
+ * dense row-major, no leading-dimension parameters; mxgemm_run_host takes
+ * host memory instead):
+ *   A       : M x K      uint8 element codes (E4M3 by default, see
+ *                        MXGEMM_OPT_A_FORMAT), K contiguous
  *   A_scale : M x (K/32) uint8 E8M0 codes
- *   B       : K x N      uint8 E4M3 codes, N contiguous
+ *   B       : K x N      uint8 element codes (MXGEMM_OPT_B_FORMAT), N contiguous
  *   B_scale : N x (K/32) uint8 E8M0 codes (row j holds column j's scales)
  *   C       : M x N      float (MXGEMM_OUT_F32) or bfloat16 (MXGEMM_OUT_BF16)
  *
@@ -33,6 +35,11 @@
  * Threads and streams: a handle may be used from one host thread at a time,
  * and its internal workspace is reused in stream order, so concurrent calls
  * on different streams need different handles.
+ *
+ * Entry points: mxgemm_run (device operands), mxgemm_run_host (host
+ * operands, copies pipelined with the GEMM), mxgemm_run_noalloc (no device
+ * allocation, fixed scratch), mxgemm_quantize (FP32/BF16 -> E4M3 codes and
+ * E8M0 scales on the GPU), plus handle, option, status and timing helpers.
  */
 #ifndef MXGEMM_H_
 #define MXGEMM_H_
