@@ -77,6 +77,8 @@ struct HostPipe {
   cudaEvent_t in_ready[2] = {};     // slot s holds its slab's inputs
   cudaEvent_t gemm_done[2] = {};    // slot s's GEMM has finished
   cudaEvent_t out_done[2] = {};     // slot s's C rows are back on the host
+  cudaEvent_t b_used[2] = {};       // the last GEMM reading B slot b has finished
+  int bslot = 0;                    // B slot of the next call
   Workspace stage;
 };
 
@@ -657,7 +659,8 @@ int mxgemm_destroy(mxgemm_handle_t h) {
     HostPipe &hp = h->hp;
     if (hp.stage.ptr) cudaFree(hp.stage.ptr);
     for (cudaEvent_t e : {hp.start, hp.b_ready, hp.in_ready[0], hp.in_ready[1], hp.gemm_done[0],
-                          hp.gemm_done[1], hp.out_done[0], hp.out_done[1]})
+                          hp.gemm_done[1], hp.out_done[0], hp.out_done[1], hp.b_used[0],
+                          hp.b_used[1]})
       if (e) cudaEventDestroy(e);
     if (hp.h2d) cudaStreamDestroy(hp.h2d);
     if (hp.d2h) cudaStreamDestroy(hp.d2h);
@@ -745,7 +748,8 @@ int host_pipe_init(mxgemm_ctx *h) {
     return MXGEMM_ERR_CUDA;
   }
   cudaEvent_t *evs[] = {&hp.start,        &hp.b_ready,      &hp.in_ready[0], &hp.in_ready[1],
-                        &hp.gemm_done[0], &hp.gemm_done[1], &hp.out_done[0], &hp.out_done[1]};
+                        &hp.gemm_done[0], &hp.gemm_done[1], &hp.out_done[0], &hp.out_done[1],
+                        &hp.b_used[0],    &hp.b_used[1]};
   for (cudaEvent_t *e : evs)
     if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) {
       cudaGetLastError();
@@ -755,9 +759,12 @@ int host_pipe_init(mxgemm_ctx *h) {
   return MXGEMM_OK;
 }
 
-int ensure_stage(mxgemm_ctx *h, size_t bytes, cudaStream_t stream) {
+// *grown is set when the staging area was (re)allocated on `stream`.
+int ensure_stage(mxgemm_ctx *h, size_t bytes, cudaStream_t stream, bool *grown) {
   Workspace &w = h->hp.stage;
+  *grown = false;
   if (w.bytes >= bytes) return MXGEMM_OK;
+  *grown = true;
   if (w.ptr) {
     // every earlier use is ordered before this point of `stream`
     cudaFreeAsync(w.ptr, stream);
@@ -840,22 +847,37 @@ extern "C" int mxgemm_run_host(mxgemm_handle_t h, int64_t M, int64_t N, int64_t 
   const size_t b_bytes = static_cast<size_t>(K) * N, bs_bytes = static_cast<size_t>(N) * kb;
   const size_t a_bytes = static_cast<size_t>(ms) * K, as_bytes = static_cast<size_t>(ms) * kb;
   const size_t c_bytes = static_cast<size_t>(ms) * N * esz;
+  // staging: two B slots (consecutive calls alternate, so that one call's
+  // B copy overlaps the previous call's last slabs), then two row slots
   const size_t off_bs = round_up(b_bytes, 256);
-  const size_t off_slot = round_up(off_bs + bs_bytes, 256);
+  const size_t bslot_bytes = round_up(off_bs + bs_bytes, 256);
+  const size_t off_slot = 2 * bslot_bytes;
   const size_t off_as = round_up(a_bytes, 256);
   const size_t off_c = round_up(off_as + as_bytes, 256);
   const size_t slot_bytes = round_up(off_c + c_bytes, 256);
-  st = ensure_stage(h, off_slot + 2 * slot_bytes, stream);
+  bool grown = false;
+  st = ensure_stage(h, off_slot + 2 * slot_bytes, stream, &grown);
   if (st != MXGEMM_OK) return st;
-  uint8_t *base = hp.stage.ptr;
   const uint8_t *hA = static_cast<const uint8_t *>(A), *hAs = static_cast<const uint8_t *>(A_scale);
   uint8_t *hC = static_cast<uint8_t *>(C);
+  const int bs = hp.bslot;
+  hp.bslot ^= 1;
+  uint8_t *dB = hp.stage.ptr + bs * bslot_bytes;
+  uint8_t *base = hp.stage.ptr;
 
-  // the copy streams start where the caller's stream is
-  if (!record_event(hp.start, stream) || !wait_event(hp.h2d, hp.start) || !wait_event(hp.d2h, hp.start))
+  // The copies do not wait for the caller's stream: the host operands are
+  // ready when the call is made, and every staging slot is reused only after
+  // the events of its previous use (also from earlier calls; an event never
+  // recorded is no wait).  The copy streams are ordered after the caller's
+  // stream only when the staging area was just (re)allocated there, or when
+  // C is read (use_acc): C on the host may still be arriving from an
+  // earlier call.
+  if ((grown || use_acc) &&
+      (!record_event(hp.start, stream) || !wait_event(hp.h2d, hp.start) || !wait_event(hp.d2h, hp.start)))
     return MXGEMM_ERR_CUDA;
-  if (!copy_async(base, B, b_bytes, cudaMemcpyHostToDevice, hp.h2d) ||
-      !copy_async(base + off_bs, B_scale, bs_bytes, cudaMemcpyHostToDevice, hp.h2d) ||
+  if (!wait_event(hp.h2d, hp.b_used[bs]) ||
+      !copy_async(dB, B, b_bytes, cudaMemcpyHostToDevice, hp.h2d) ||
+      !copy_async(dB + off_bs, B_scale, bs_bytes, cudaMemcpyHostToDevice, hp.h2d) ||
       !record_event(hp.b_ready, hp.h2d))
     return MXGEMM_ERR_CUDA;
   for (int64_t j = 0; j < nslab; ++j) {
@@ -865,9 +887,9 @@ extern "C" int mxgemm_run_host(mxgemm_handle_t h, int64_t M, int64_t N, int64_t 
     uint8_t *dAs = dA + off_as;
     uint8_t *dC = dA + off_c;
     const size_t crow = static_cast<size_t>(N) * esz;
-    // inputs of slab j into slot s, once slab j-2's GEMM (and, when C is
-    // read, its copy out) no longer needs the slot
-    if (j >= 2 && (!wait_event(hp.h2d, hp.gemm_done[s]) || (use_acc && !wait_event(hp.h2d, hp.out_done[s]))))
+    // inputs of slab j into slot s, once the slot's previous GEMM (and,
+    // when C is read, its copy out) no longer needs it
+    if (!wait_event(hp.h2d, hp.gemm_done[s]) || (use_acc && !wait_event(hp.h2d, hp.out_done[s])))
       return MXGEMM_ERR_CUDA;
     if (!copy_async(dA, hA + m0 * K, static_cast<size_t>(mj) * K, cudaMemcpyHostToDevice, hp.h2d) ||
         !copy_async(dAs, hAs + m0 * kb, static_cast<size_t>(mj) * kb, cudaMemcpyHostToDevice, hp.h2d) ||
@@ -876,9 +898,9 @@ extern "C" int mxgemm_run_host(mxgemm_handle_t h, int64_t M, int64_t N, int64_t 
       return MXGEMM_ERR_CUDA;
     // the GEMM of slab j on the caller's stream
     if (!wait_event(stream, hp.in_ready[s]) || (j == 0 && !wait_event(stream, hp.b_ready)) ||
-        (j >= 2 && !wait_event(stream, hp.out_done[s])))
+        !wait_event(stream, hp.out_done[s]))
       return MXGEMM_ERR_CUDA;
-    st = mxgemm_run(h, mj, N, K, dA, dAs, base, base + off_bs, dC, use_acc, out_dtype, stream);
+    st = mxgemm_run(h, mj, N, K, dA, dAs, dB, dB + off_bs, dC, use_acc, out_dtype, stream);
     if (st != MXGEMM_OK) return st;
     if (!record_event(hp.gemm_done[s], stream)) return MXGEMM_ERR_CUDA;
     // its C rows back to the host
@@ -887,8 +909,10 @@ extern "C" int mxgemm_run_host(mxgemm_handle_t h, int64_t M, int64_t N, int64_t 
         !record_event(hp.out_done[s], hp.d2h))
       return MXGEMM_ERR_CUDA;
   }
-  // the caller's stream completes once every slab is back
-  if (!wait_event(stream, hp.out_done[0]) || (nslab > 1 && !wait_event(stream, hp.out_done[1])))
+  // B slot bs is free once this call's last GEMM is done; the caller's
+  // stream completes once every slab is back
+  if (!record_event(hp.b_used[bs], stream) || !wait_event(stream, hp.out_done[0]) ||
+      (nslab > 1 && !wait_event(stream, hp.out_done[1])))
     return MXGEMM_ERR_CUDA;
   return MXGEMM_OK;
 }

@@ -149,8 +149,11 @@ int mxgemm_run(mxgemm_handle_t h, int64_t M, int64_t N, int64_t K,
  * its C rows) are copied in on an internal stream and the previous slab's
  * C rows are copied out on another.  `stream` waits for the last copy, so
  * C on the host is complete once `stream` is: synchronize it before reading
- * C.  Page-locked (pinned) host buffers let the copies overlap; pageable
- * ones work but the copies then block the calling thread.  The handle owns
+ * C.  The host buffers must hold their values when the call is made and
+ * stay unchanged until `stream` has completed it; consecutive calls on one
+ * handle overlap (one call's copies in run while the previous call's
+ * copies out finish).  Page-locked (pinned) host buffers let the copies
+ * overlap; pageable ones work but the copies then block the calling thread.  The handle owns
  * the device staging buffers (B, B_scale and the two slots), which grow
  * lazily in stream order on `stream`, and two internal streams.  Use one
  * stream per handle.  K == 0 synchronizes `stream` and then zeroes C (use_acc

@@ -91,3 +91,42 @@ def test_run_host_rejects_bad_arguments(h):
     C.fill_(3.0)
     assert mx.mxgemm_run_host(h, 4, 4, 0, z, z, z, z, C, 0, mx.OUT_F32, None, check=False) == mx.OK
     assert torch.all(C == 0)
+
+
+def test_run_host_back_to_back_calls_overlap_correctly(h):
+    # consecutive calls overlap on the copy streams (one call's B copy runs
+    # while the previous call's last slabs come back); four different
+    # problems, each with its own host C, enqueued without synchronizing
+    probs = [mi.random_problem(1100, 640, 384, seed=200 + i, kind="normal", out_dtype="f32")
+             for i in range(4)]
+    outs = []
+    stream = torch.cuda.current_stream()
+    for p in probs:
+        A, As, B, Bs = (t.contiguous().pin_memory() for t in (p.A, p.As, p.B, p.Bs))
+        C = torch.full((p.M, p.N), float("nan"), dtype=torch.float32).pin_memory()
+        mx.mxgemm_run_host(h, p.M, p.N, p.K, A, As, B, Bs, C, 0, mx.OUT_F32, stream)
+        outs.append((A, As, B, Bs, C))
+    stream.synchronize()
+    for p, (_, _, _, _, C) in zip(probs, outs):
+        _check(p, C)
+
+
+def test_run_host_use_acc_chain_on_one_host_c(h):
+    # C accumulated over two K halves by two calls on the same host C, with
+    # no synchronization between them: the second call must read the first
+    # call's result
+    M, N, K = 700, 520, 1024
+    p = mi.random_problem(M, N, K, seed=210, kind="normal", out_dtype="f32")
+    C = torch.full((M, N), float("nan"), dtype=torch.float32).pin_memory()
+    stream = torch.cuda.current_stream()
+    halves = []
+    for c in range(2):
+        k0, k1 = c * K // 2, (c + 1) * K // 2
+        A = p.A[:, k0:k1].contiguous().pin_memory()
+        As = p.As[:, k0 // 32:k1 // 32].contiguous().pin_memory()
+        B = p.B[k0:k1].contiguous().pin_memory()
+        Bs = p.Bs[:, k0 // 32:k1 // 32].contiguous().pin_memory()
+        halves.append((A, As, B, Bs))
+        mx.mxgemm_run_host(h, M, N, K // 2, A, As, B, Bs, C, c, mx.OUT_F32, stream)
+    stream.synchronize()
+    _check(p, C)
