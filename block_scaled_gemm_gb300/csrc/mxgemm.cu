@@ -367,7 +367,7 @@ int build_plan(mxgemm_ctx *h, Plan *pl, int64_t M, int64_t N, int64_t K, const v
       encode_2d(h, &pl->tSA, u8, sfa, 128, a_chunks * 4, 128, 128, 4, CU_TENSOR_MAP_SWIZZLE_NONE) ||
       encode_2d(h, &pl->tSB, u8, sfb, 128, b_chunks * 4, 128, 128, 8, CU_TENSOR_MAP_SWIZZLE_NONE))
     return MXGEMM_ERR_CUDA;
-  // C: stored through TMA (64-byte-wide boxes, 32 rows) when its row pitch
+  // C: stored through TMA (128-byte-wide boxes, 16 rows) when its row pitch
   // allows it; otherwise the kernel stores directly and tC is unused.
   const bool tma_store = (static_cast<size_t>(N) * esz) % 16 == 0;
   std::memset(&pl->tC, 0, sizeof(pl->tC));
@@ -375,8 +375,8 @@ int build_plan(mxgemm_ctx *h, Plan *pl, int64_t M, int64_t N, int64_t K, const v
       encode_2d(h, &pl->tC,
                 out_dtype == MXGEMM_OUT_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
                                             : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16,
-                C, N, M, static_cast<uint64_t>(N) * esz, static_cast<uint32_t>(64 / esz), 32,
-                CU_TENSOR_MAP_SWIZZLE_64B))
+                C, N, M, static_cast<uint64_t>(N) * esz, static_cast<uint32_t>(128 / esz), 16,
+                CU_TENSOR_MAP_SWIZZLE_128B))
     return MXGEMM_ERR_CUDA;
   KParams &kp = pl->kp;
   std::memset(&kp, 0, sizeof(kp));

@@ -895,9 +895,10 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
       if (kAcc && kTma && w.kind != kPartial && lane == 0) {
         // pull this warp's part of C_in into L2 while the tile's MMAs run
         const int r0 = mt * (128 * CG) + 128 * (int)rank + 32 * q;
-        const int cw = kBF16 ? 32 : 16;
-        for (int c0 = colb; c0 < colb + ncols && c0 < p.N && r0 < p.M; c0 += cw)
-          tma_prefetch_l2_2d(&tmC, c0, r0);
+        const int cw = kBF16 ? 64 : 32;  // the store boxes: 128 bytes x 16 rows
+        for (int c0 = colb; c0 < colb + ncols && c0 < p.N; c0 += cw)
+          for (int rh = 0; rh < 2; ++rh)
+            if (r0 + 16 * rh < p.M) tma_prefetch_l2_2d(&tmC, c0, r0 + 16 * rh);
       }
       // all lanes wait (warp-uniform control flow)
       if (!__all_sync(0xFFFFFFFFu,
@@ -1021,49 +1022,56 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
       }
 
       if constexpr (kTma) {
-        // 64-byte-wide column chunks through this warp's staging buffer: lane
-        // l writes row l (64-byte swizzle: 16-byte unit u of row r sits at
-        // u ^ ((r >> 1) & 3)), then one lane issues the TMA store, which
-        // clips rows >= M and columns >= N.
+        // Chunks of 16 rows x 128 bytes through this warp's 2 KB staging
+        // buffer, so that every row of a TMA store is a whole 128-byte line
+        // in C (64-byte-wide chunks wrote each line in two halves, from two
+        // stores): the 16 lanes holding the chunk's rows write them
+        // (128-byte swizzle: 16-byte unit u of row r sits at u ^ (r & 7)),
+        // then one lane issues the store, which clips rows >= M and columns
+        // >= N.
         const uint32_t buf = base + C::OFF_EPI + ew * C::EPI_BUF;
-        const uint32_t rowaddr = buf + lane * 64;
-        const uint32_t swz = (lane >> 1) & 3;
-        constexpr int CHUNKS = 8;  // FP32: 16 columns per chunk; BF16: 32 columns per chunk
-        if (row0w < p.M) {
+        const int r16 = lane & 15;
+        const uint32_t rowaddr = buf + r16 * 128;
+        const uint32_t swz = r16 & 7;
+        constexpr int CCOLS = kBF16 ? 64 : 32;  // columns per chunk: 128 bytes
 #pragma unroll
-          for (int ch = 0; ch < CHUNKS; ++ch) {
-            const int ccols = kBF16 ? 32 : 16;
-            if (kBF16 && ch >= 4) break;
-            if (ch * ccols >= ncols) break;
-            const int c0 = colb + ch * ccols;
-            if (c0 >= p.N) break;
+        for (int cc = 0; cc < 128 / CCOLS; ++cc) {
+          if (cc * CCOLS >= ncols) break;
+          const int c0 = colb + cc * CCOLS;
+          if (c0 >= p.N) break;
+#pragma unroll
+          for (int rh = 0; rh < 2; ++rh) {
+            const int r0 = row0w + 16 * rh;
+            if (r0 >= p.M) break;
             if (lane == 0) bulk_wait_read_all();
             __syncwarp();
-            if constexpr (!kBF16) {
+            if ((lane >> 4) == rh) {
+              if constexpr (!kBF16) {
 #pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                const int c = ch * 16 + 4 * u;
-                st_shared_v4(rowaddr + ((u ^ swz) << 4), v[c >> 5][c & 31], v[c >> 5][(c & 31) + 1],
-                             v[c >> 5][(c & 31) + 2], v[c >> 5][(c & 31) + 3]);
-              }
-            } else {
-#pragma unroll
-              for (int u = 0; u < 4; ++u) {
-                uint32_t w[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                  const int c = (ch & 3) * 32 + 8 * u + 2 * e;
-                  const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[c >> 5][c & 31]),
-                                                                  __uint_as_float(v[c >> 5][(c & 31) + 1]));
-                  w[e] = *reinterpret_cast<const uint32_t *>(&b2);
+                for (int u = 0; u < 8; ++u) {
+                  const int c = cc * 32 + 4 * u;
+                  st_shared_v4(rowaddr + ((u ^ swz) << 4), v[c >> 5][c & 31], v[c >> 5][(c & 31) + 1],
+                               v[c >> 5][(c & 31) + 2], v[c >> 5][(c & 31) + 3]);
                 }
-                st_shared_v4(rowaddr + ((u ^ swz) << 4), w[0], w[1], w[2], w[3]);
+              } else {
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                  uint32_t w[4];
+#pragma unroll
+                  for (int e = 0; e < 4; ++e) {
+                    const int c = cc * 64 + 8 * u + 2 * e;
+                    const __nv_bfloat162 b2 = __floats2bfloat162_rn(__uint_as_float(v[c >> 5][c & 31]),
+                                                                    __uint_as_float(v[c >> 5][(c & 31) + 1]));
+                    w[e] = *reinterpret_cast<const uint32_t *>(&b2);
+                  }
+                  st_shared_v4(rowaddr + ((u ^ swz) << 4), w[0], w[1], w[2], w[3]);
+                }
               }
             }
             fence_proxy_async_smem();
             __syncwarp();
             if (lane == 0) {
-              tma_store_2d(&tmC, buf, c0, row0w);
+              tma_store_2d(&tmC, buf, c0, r0);
               bulk_commit_group();
             }
           }
