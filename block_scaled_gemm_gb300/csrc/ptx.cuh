@@ -108,19 +108,6 @@ __device__ __forceinline__ bool mbar_try_wait_cluster_acquire(uint32_t bar, uint
   return ok != 0;
 }
 
-// Non-blocking probe with cluster-scope acquire (arrivals from the peer CTA).
-__device__ __forceinline__ uint32_t mbar_test_wait_cluster_acquire(uint32_t bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.test_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(bar), "r"(parity)
-      : "memory");
-  return ok;
-}
-
 // ---------------------------------------------------------------- TMA
 __device__ __forceinline__ void tma_prefetch_desc(const CUtensorMap *tm) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(tm)) : "memory");
