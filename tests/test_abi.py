@@ -74,3 +74,45 @@ def test_product_path_does_not_import_the_oracle():
     for f in src:
         text = f.read_text()
         assert "import oracle" not in text and "from oracle" not in text, f
+
+
+C_PROGRAM = r"""
+#include <stdio.h>
+#include <string.h>
+#include "mxgemm.h"
+
+int main(void) {
+  /* plain C: the header compiles as C, the library links and answers */
+  if (strcmp(mxgemm_status_string(MXGEMM_OK), "ok") != 0) return 1;
+  if (mxgemm_run(NULL, 1, 1, 32, NULL, NULL, NULL, NULL, NULL, 0, MXGEMM_OUT_F32, NULL) !=
+      MXGEMM_ERR_INVALID_VALUE) return 2;
+  if (mxgemm_set_option(NULL, MXGEMM_OPT_A_FORMAT, MXGEMM_FMT_E2M1) != MXGEMM_ERR_INVALID_VALUE) return 3;
+  if (mxgemm_quantize(NULL, MXGEMM_IN_F32, 4, 48, 0, NULL, NULL, NULL) != MXGEMM_ERR_INVALID_VALUE)
+    return 4;
+  /* without a GPU: create fails cleanly, no handle */
+  mxgemm_handle_t h = (mxgemm_handle_t)1;
+  int st = mxgemm_create(&h, 0);
+  if (st == MXGEMM_OK) { mxgemm_destroy(h); printf("gpu\n"); return 0; }
+  if (h != NULL) return 5;
+  printf("nogpu %d\n", st);
+  return 0;
+}
+"""
+
+
+def test_header_is_plain_c_and_links(lib, tmp_path):
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc")
+    if gcc is None:
+        pytest.skip("no gcc")
+    src = tmp_path / "abi_check.c"
+    src.write_text(C_PROGRAM)
+    exe = tmp_path / "abi_check"
+    so = mx.library_path()
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Werror", "-I", str(HEADER), str(src), "-o", str(exe),
+                        str(so), f"-Wl,-rpath,{so.parent}"], capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, (r.returncode, r.stdout, r.stderr)
+    assert r.stdout.split()[0] in ("gpu", "nogpu")
