@@ -742,8 +742,9 @@ namespace {
 int host_pipe_init(mxgemm_ctx *h) {
   HostPipe &hp = h->hp;
   if (hp.ready) return MXGEMM_OK;
-  if (cudaStreamCreateWithFlags(&hp.h2d, cudaStreamNonBlocking) != cudaSuccess ||
-      cudaStreamCreateWithFlags(&hp.d2h, cudaStreamNonBlocking) != cudaSuccess) {
+  // anything created by an earlier, failed attempt is kept, not re-created
+  if ((!hp.h2d && cudaStreamCreateWithFlags(&hp.h2d, cudaStreamNonBlocking) != cudaSuccess) ||
+      (!hp.d2h && cudaStreamCreateWithFlags(&hp.d2h, cudaStreamNonBlocking) != cudaSuccess)) {
     cudaGetLastError();
     return MXGEMM_ERR_CUDA;
   }
@@ -751,7 +752,7 @@ int host_pipe_init(mxgemm_ctx *h) {
                         &hp.gemm_done[0], &hp.gemm_done[1], &hp.out_done[0], &hp.out_done[1],
                         &hp.b_used[0],    &hp.b_used[1]};
   for (cudaEvent_t *e : evs)
-    if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) {
+    if (!*e && cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) {
       cudaGetLastError();
       return MXGEMM_ERR_CUDA;
     }
