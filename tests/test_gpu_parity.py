@@ -347,3 +347,31 @@ def test_skinny_split_k(h, M, out_dtype, use_acc):
             assert res["ok"], f"stream_k={sk}: {res}"
     finally:
         mx.mxgemm_set_option(h, mx.OPT_STREAM_K, 1)
+
+
+def test_plan_cache_churn_and_workspace_growth(h):
+    # more distinct problems than the handle caches plans for, cycled twice
+    # without synchronizing between calls, growing and reusing the workspace
+    # (stream-ordered); every result checked against the oracle
+    _mode(h, 0)
+    shapes = [(64, 96, 64), (300, 520, 256), (1000, 200, 512), (129, 1000, 1024), (520, 520, 2048),
+              (2048, 64, 320), (17, 4000, 128), (700, 700, 640), (256, 4096, 512), (1500, 300, 96),
+              (33, 65, 8192), (900, 1300, 160)]
+    probs = [mi.random_problem(M, N, K, seed=300 + i, kind="normal", out_dtype="f32" if i % 3 else "bf16")
+             for i, (M, N, K) in enumerate(shapes)]
+    dev = [tuple(t.to(gu.DEV) for t in (p.A, p.As, p.B, p.Bs)) for p in probs]
+    outs = []
+    stream = torch.cuda.current_stream()
+    for rnd in range(2):
+        for p, (A, As, B, Bs) in zip(probs, dev):
+            tdt = torch.float32 if p.out_dtype == "f32" else torch.bfloat16
+            C = torch.full((p.M, p.N), float("nan"), dtype=tdt, device=gu.DEV)
+            mx.mxgemm_run(h, p.M, p.N, p.K, A, As, B, Bs, C, 0, gu.out_code(p.out_dtype), stream)
+            outs.append((p, C))
+    torch.cuda.synchronize()
+    st, det = mx.mxgemm_get_device_status(h)
+    assert st == 0, (st, det)
+    for p, C in outs:
+        ref, bound = oracle.rows(p.A, p.As, p.B, p.Bs)
+        res = oracle.accept(gu.to_numpy_out(C, p.out_dtype), ref, bound, p.out_dtype)
+        assert res["ok"], f"{p.name}: {res}"
