@@ -16,6 +16,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <cstdint>
+#include <type_traits>
 
 #include "ptx.cuh"
 
@@ -106,30 +107,58 @@ __global__ void mx_quantize_rows_kernel(const T *__restrict__ X, int64_t nblocks
 }
 
 // Blocks down the columns (X is R x C, R % 32 == 0; scales C x R/32, row j
-// for column j): one thread per (column, 32-row block); neighbouring threads
-// take neighbouring columns, so every row access of a warp is contiguous.
-template <typename T>
+// for column j): one thread per (NC adjacent columns, 32-row block);
+// neighbouring threads take neighbouring column pairs, so every row access
+// of a warp is contiguous, NC x 32 x sizeof(T) bytes wide.  The thread holds
+// its 32 rows as loaded words (all loads issued before the first use) and
+// stores NC codes per row.  NC = 2 needs C even.
+template <typename T, int NC>
 __global__ void mx_quantize_cols_kernel(const T *__restrict__ X, int64_t R, int64_t C,
                                         uint8_t *__restrict__ codes, uint8_t *__restrict__ scales) {
+  static_assert(NC == 1 || NC == 2, "one or two columns per thread");
+  constexpr int kWordBytes = NC * static_cast<int>(sizeof(T));
+  using Word = typename std::conditional<
+      kWordBytes == 8, uint2,
+      typename std::conditional<kWordBytes == 4, uint32_t, uint16_t>::type>::type;
+  static_assert(sizeof(Word) == kWordBytes, "one load per row");
   const int64_t rblocks = R / 32;
-  const int64_t total = rblocks * C;
+  const int64_t groups = C / NC;
+  const int64_t total = rblocks * groups;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-    const int64_t rb = i / C, j = i - rb * C;
+    const int64_t rb = i / groups, j = (i - rb * groups) * NC;
     const T *src = X + rb * 32 * C + j;
-    float v[32];
-    float amax = 0.0f;
+    Word raw[32];
+#pragma unroll
+    for (int e = 0; e < 32; ++e) raw[e] = *reinterpret_cast<const Word *>(src + e * C);
+    float amax[NC];
+#pragma unroll
+    for (int c = 0; c < NC; ++c) amax[c] = 0.0f;
 #pragma unroll
     for (int e = 0; e < 32; ++e) {
-      v[e] = mx_to_float<T>(src[e * C]);
-      amax = fmaxf(amax, fabsf(v[e]));
+      const T *t = reinterpret_cast<const T *>(&raw[e]);
+#pragma unroll
+      for (int c = 0; c < NC; ++c) amax[c] = fmaxf(amax[c], fabsf(mx_to_float<T>(t[c])));
     }
-    const int s = mx_scale_of(amax);
-    const float m = mx_pow2(s);
+    int s[NC];
+    float m[NC];
+#pragma unroll
+    for (int c = 0; c < NC; ++c) {
+      s[c] = mx_scale_of(amax[c]);
+      m[c] = mx_pow2(s[c]);
+    }
     uint8_t *dst = codes + rb * 32 * C + j;
 #pragma unroll
-    for (int e = 0; e < 32; ++e) dst[e * C] = static_cast<uint8_t>(mx_e4m3(v[e] * m));
-    scales[j * rblocks + rb] = static_cast<uint8_t>(s);
+    for (int e = 0; e < 32; ++e) {
+      const T *t = reinterpret_cast<const T *>(&raw[e]);
+      if constexpr (NC == 2)
+        *reinterpret_cast<uint16_t *>(dst + e * C) = static_cast<uint16_t>(
+            mx_e4m3x2(mx_to_float<T>(t[0]) * m[0], mx_to_float<T>(t[1]) * m[1]));
+      else
+        dst[e * C] = static_cast<uint8_t>(mx_e4m3(mx_to_float<T>(t[0]) * m[0]));
+    }
+#pragma unroll
+    for (int c = 0; c < NC; ++c) scales[(j + c) * rblocks + rb] = static_cast<uint8_t>(s[c]);
   }
 }
 

@@ -1,6 +1,7 @@
 """mxgemm_quantize (MX quantization on the GPU) against the oracle's
 quantizer, bit for bit: every code and every scale byte, FP32 and BF16
-inputs, blocks along rows and down columns, value ranges from FP32
+inputs, blocks along rows and down columns (odd column counts take one
+column per thread, even ones two), value ranges from FP32
 subnormals to 3e38, exact E4M3 ties and all-zero blocks.  Then the
 quantized operands feed the GEMM."""
 import numpy as np
@@ -57,7 +58,10 @@ def _gpu_quantize(x, along_cols, dtype):
 
 @pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
 @pytest.mark.parametrize("along_cols,R,C", [(False, 77, 320), (False, 1, 32), (False, 513, 4096),
-                                            (True, 96, 77), (True, 32, 1), (True, 4096, 515)])
+                                            (True, 96, 77), (True, 32, 1), (True, 4096, 515), (True, 64, 130),
+                                            # more blocks than one grid covers: grid-stride
+                                            # passes, the last one partly live
+                                            (False, 4099, 640), (True, 4096, 2600)])
 def test_quantize_bit_exact(built, dtype, along_cols, R, C):
     x = _values(R, C, seed=R * 7 + C)
     xin = x.to(dtype)
