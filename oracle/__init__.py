@@ -77,6 +77,10 @@ def _load():
         lib.mxo_e4m3_rne.restype = ctypes.c_uint8
         lib.mxo_quantize_e4m3.argtypes = [i64, i64, f64p, ci, u8p, u8p]
         lib.mxo_quantize_e4m3.restype = ci
+        lib.mxo_e4m3_sr.argtypes = [ctypes.c_double, ctypes.c_uint32]
+        lib.mxo_e4m3_sr.restype = ctypes.c_uint8
+        lib.mxo_quantize_e4m3_sr.argtypes = [i64, i64, f64p, ci, ctypes.c_void_p, u8p, u8p]
+        lib.mxo_quantize_e4m3_sr.restype = ci
         lib.mxo_round_f32.argtypes = [ctypes.c_double]
         lib.mxo_round_f32.restype = ctypes.c_float
         lib.mxo_round_bf16.argtypes = [ctypes.c_double]
@@ -190,20 +194,41 @@ def e4m3_rne(y: float) -> int:
     return int(_load().mxo_e4m3_rne(float(y)))
 
 
-def quantize_e4m3(x, along_cols: bool = False):
+def e4m3_sr(y: float, r: int) -> int:
+    """E4M3 code of y by stochastic rounding with the random word r: with
+    lo <= |y| < lo + q adjacent E4M3 magnitudes (|y| clamped to 448), lo + q
+    when r < 2^32 (|y| - lo) / q, else lo; sign kept."""
+    return int(_load().mxo_e4m3_sr(float(y), int(r) & 0xFFFFFFFF))
+
+
+def quantize_e4m3(x, along_cols: bool = False, rand_bits=None):
     """MX quantization of a real R x C matrix (any float dtype, values taken
     exactly) to E4M3 codes with E8M0 scales per 32 values: along each row
     (scales R x C/32) or, with along_cols, down each column (scales
-    C x R/32, row j for column j).  Returns (codes uint8 R x C, scales)."""
+    C x R/32, row j for column j).  The codes round to nearest even, or,
+    given rand_bits (R x C uint32, one random word per value), stochastically
+    (``e4m3_sr`` of the scaled value as an FP32 number).  Returns (codes
+    uint8 R x C, scales)."""
     if hasattr(x, "numpy"):  # torch tensor (bfloat16 and float32 widen exactly)
         x = x.detach().to("cpu").double().numpy()
     xd = np.ascontiguousarray(np.asarray(x, dtype=np.float64))
     R, C = xd.shape
     codes = np.empty((R, C), dtype=np.uint8)
     scales = np.empty((C, R // 32) if along_cols else (R, C // 32), dtype=np.uint8)
-    rc = _load().mxo_quantize_e4m3(R, C, _ptr(xd), int(bool(along_cols)), _ptr(codes), _ptr(scales))
+    if rand_bits is None:
+        rc = _load().mxo_quantize_e4m3(R, C, _ptr(xd), int(bool(along_cols)), _ptr(codes),
+                                       _ptr(scales))
+    else:
+        if hasattr(rand_bits, "numpy"):
+            rand_bits = rand_bits.detach().to("cpu").numpy()
+        rb = np.ascontiguousarray(np.asarray(rand_bits).view(np.uint32))
+        if rb.shape != (R, C):
+            raise ValueError("rand_bits must be R x C")
+        rc = _load().mxo_quantize_e4m3_sr(R, C, _ptr(xd), int(bool(along_cols)),
+                                          rb.ctypes.data_as(ctypes.c_void_p), _ptr(codes),
+                                          _ptr(scales))
     if rc != 0:
-        raise ValueError("mxo_quantize_e4m3 rejected its arguments")
+        raise ValueError("the oracle's quantizer rejected its arguments")
     return codes, scales
 
 

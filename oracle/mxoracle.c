@@ -412,12 +412,42 @@ uint8_t mxo_e4m3_rne(double y) {
   return (uint8_t)(sign | (uint8_t)((e + 7) << 3) | (uint8_t)q);
 }
 
+/*
+ * Stochastic rounding to E4M3 ("TLX API Quick Reference", section "Utility",
+ * row `tlx.stoch_round`: FP32 -> FP8 with random bits the caller supplies).
+ * The pages do not say how the random bits are used; the reading taken here
+ * is the textbook one.  |y| (clamped to 448) lies between two adjacent E4M3
+ * magnitudes lo <= |y| < lo + q, q the E4M3 spacing at |y| (2^(e-3) in the
+ * binade [2^e, 2^(e+1)), 2^-9 below 2^-6).  With one random 32-bit word r per
+ * value the result is lo + q when r < 2^32 * (|y| - lo) / q and lo otherwise:
+ * it rounds away from zero with probability (|y| - lo) / q, to within 2^-32.
+ * The sign is kept, also for zero.  Every step below is exact in double.
+ */
+uint8_t mxo_e4m3_sr(double y, uint32_t r) {
+  const uint8_t sign = signbit(y) ? 0x80u : 0u;
+  double a = fabs(y);
+  if (a > 448.0) a = 448.0;
+  if (a == 0.0) return sign;
+  int E;
+  (void)frexp(a, &E);        /* a in [2^(E-1), 2^E) */
+  int e = E - 1;
+  if (e < -6) e = -6;        /* below 2^-6 the grid is the subnormal one */
+  const double q = ldexp(1.0, e - 3);
+  const double lo = floor(a / q) * q;
+  const double frac = (a - lo) / q; /* in [0, 1) */
+  const double mag = (double)r < ldexp(frac, 32) ? lo + q : lo;
+  return (uint8_t)(sign | mxo_e4m3_rne(mag)); /* mag is on the grid: its own code */
+}
+
 /* x: R x C row-major values.  along_cols = 0: blocks of 32 along each row
  * (C % 32 == 0), scales R x (C/32); along_cols = 1: blocks of 32 down each
  * column (R % 32 == 0), scales C x (R/32), row j holding column j's scales.
- * codes: R x C.  Returns 0, or -1 on a bad argument. */
-int mxo_quantize_e4m3(int64_t R, int64_t C, const double *x, int along_cols, uint8_t *codes,
-                      uint8_t *scales) {
+ * codes: R x C.  rbits: NULL for round-to-nearest-even, else R x C random
+ * words (row-major, the same index as x) for stochastic rounding of the
+ * scaled value taken as an FP32 number.  Returns 0, or -1 on a bad
+ * argument. */
+static int quantize_e4m3(int64_t R, int64_t C, const double *x, int along_cols,
+                         const uint32_t *rbits, uint8_t *codes, uint8_t *scales) {
   if (R < 0 || C < 0 || (along_cols ? R % 32 : C % 32) != 0) return -1;
   const int64_t nblk = along_cols ? C * (R / 32) : R * (C / 32);
   for (int64_t b = 0; b < nblk; ++b) {
@@ -444,8 +474,22 @@ int mxo_quantize_e4m3(int64_t R, int64_t C, const double *x, int along_cols, uin
       if (s > 254) s = 254;
     }
     scales[b] = (uint8_t)s; /* b enumerates blocks in the scales' own order */
-    for (int i = 0; i < 32; ++i)
-      codes[base + i * step] = mxo_e4m3_rne(ldexp(x[base + i * step], 127 - s));
+    for (int i = 0; i < 32; ++i) {
+      const int64_t at = base + i * step;
+      const double y = ldexp(x[at], 127 - s);
+      codes[at] = rbits ? mxo_e4m3_sr((double)(float)y, rbits[at]) : mxo_e4m3_rne(y);
+    }
   }
   return 0;
+}
+
+int mxo_quantize_e4m3(int64_t R, int64_t C, const double *x, int along_cols, uint8_t *codes,
+                      uint8_t *scales) {
+  return quantize_e4m3(R, C, x, along_cols, NULL, codes, scales);
+}
+
+int mxo_quantize_e4m3_sr(int64_t R, int64_t C, const double *x, int along_cols,
+                         const uint32_t *rbits, uint8_t *codes, uint8_t *scales) {
+  if (!rbits) return -1;
+  return quantize_e4m3(R, C, x, along_cols, rbits, codes, scales);
 }

@@ -443,3 +443,82 @@ def test_quantizer_roundtrip_error_bound():
         for b in range(10):
             amax = np.abs(x[r, 32 * b:32 * b + 32]).max() * 2.0 ** (127 - int(scales[r, b]))
             assert 224.0 < amax <= 448.0
+
+
+# ------------------------------------------------- stochastic rounding (E4M3)
+
+def _sr_cases():
+    out = []
+    for line in (GOLDEN / "mx_stochastic_rounding.txt").read_text().splitlines():
+        line = line.split("#")[0].strip()
+        if not line:
+            continue
+        y, r, code = line.split()
+        out.append((float(y), int(r), int(code, 16)))
+    return out
+
+
+@pytest.mark.parametrize("y,r,code", _sr_cases())
+def test_stochastic_rounding_hand_cases(y, r, code):
+    assert oracle.e4m3_sr(y, r) == code
+
+
+def _sr_values(n, seed):
+    g = torch.Generator().manual_seed(seed)
+    y = torch.cat([torch.randn(n, generator=g) * 100, torch.randn(n, generator=g) * 0.01,
+                   torch.randn(n, generator=g) * 1e-30,
+                   torch.randint(-3584, 3585, (n,), generator=g) / 8.0])
+    return y.clamp(-448, 448).to(torch.float32)
+
+
+def test_stochastic_rounding_brackets_and_matches_nearest():
+    # r = 0 rounds away from zero, the largest r toward zero (no value here has
+    # a fraction above 1 - 2^-32); the two are the same or adjacent grid
+    # points around y, and the library's round-to-nearest lands on one of them
+    y = _sr_values(3000, 41)
+    rn = y.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    for v, near in zip(y.numpy(), rn):
+        v = float(v)
+        up = oracle.e4m3(oracle.e4m3_sr(v, 0))
+        down = oracle.e4m3(oracle.e4m3_sr(v, 0xFFFFFFFF))
+        a = abs(v)
+        q = 2.0 ** -9 if a < 2.0 ** -6 else 2.0 ** (np.floor(np.log2(a)) - 3)
+        assert abs(down) <= a <= abs(up)
+        assert abs(up) - abs(down) in (0.0, q)
+        if abs(up) == abs(down):
+            assert abs(up) == a  # only values on the grid are left alone
+        assert oracle.e4m3(int(near)) in (up, down) or (a == 0.0)
+
+
+def test_stochastic_rounding_is_unbiased():
+    # over r spread evenly across [0, 2^32), the mean result is y, to within
+    # the spread's resolution (q / 4096 for 4096 words)
+    rs = [k * (1 << 20) + 777 for k in range(4096)]
+    for v in list(_sr_values(8, 47).numpy()) + [1.0625, -0.00146484375, 447.0, 300.1]:
+        v = float(v)
+        if v == 0.0:
+            continue
+        a = abs(v)
+        q = 2.0 ** -9 if a < 2.0 ** -6 else 2.0 ** (np.floor(np.log2(a)) - 3)
+        mean = np.mean([oracle.e4m3(oracle.e4m3_sr(v, r)) for r in rs])
+        assert abs(mean - v) <= q / 4096 * 1.0001, (v, mean)
+
+
+def test_stochastic_quantizer_keeps_scales_and_brackets_codes():
+    g = torch.Generator().manual_seed(53)
+    x = torch.randn((64, 128), generator=g) * torch.exp(torch.randn((64, 1), generator=g) * 6)
+    rb = np.random.default_rng(59).integers(0, 2 ** 32, (64, 128), dtype=np.uint64).astype(np.uint32)
+    rn_codes, rn_scales = oracle.quantize_e4m3(x)
+    sr_codes, sr_scales = oracle.quantize_e4m3(x, rand_bits=rb)
+    up, _ = oracle.quantize_e4m3(x, rand_bits=np.zeros((64, 128), np.uint32))
+    down, _ = oracle.quantize_e4m3(x, rand_bits=np.full((64, 128), 0xFFFFFFFF, np.uint32))
+    assert np.array_equal(sr_scales, rn_scales)     # the block scale does not depend on r
+    dec = np.vectorize(oracle.e4m3)
+    for codes in (sr_codes, rn_codes):
+        d = np.abs(dec(codes))
+        assert np.all((d == np.abs(dec(up))) | (d == np.abs(dec(down))))
+    # down the columns = along the rows of the transpose, with the words transposed
+    xt = x[:, :64].contiguous()
+    c2, s2 = oracle.quantize_e4m3(xt, along_cols=True, rand_bits=rb[:, :64])
+    ct, st = oracle.quantize_e4m3(xt.t().contiguous(), rand_bits=np.ascontiguousarray(rb[:, :64].T))
+    assert np.array_equal(c2, ct.T) and np.array_equal(s2, st)
