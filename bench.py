@@ -339,13 +339,17 @@ def run_quantize(args, world, rank, local):
     x = (torch.randn((R, C), generator=g) * torch.exp(torch.randn((R, 1), generator=g) * 4)).to(dt)
     X = x.to(dev)
     cols = args.q_along == "cols"
+    sr = args.q_round == "sr"
+    # stochastic rounding reads one random 32-bit word per value (an input)
+    rbits = (torch.randint(-2 ** 31, 2 ** 31, (R, C), generator=g, dtype=torch.int64)
+             .to(torch.int32).to(dev) if sr else None)
     codes = torch.empty((R, C), dtype=torch.uint8, device=dev)
     scales = torch.empty((C, R // 32) if cols else (R, C // 32), dtype=torch.uint8, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev) if not args.no_flush else None
     stream = torch.cuda.current_stream(dev)
-    nbytes = R * C * x.element_size() + R * C + R * C // 32
+    nbytes = R * C * x.element_size() + R * C + R * C // 32 + (R * C * 4 if sr else 0)
     for _ in range(args.warmup):
-        mx.mxgemm_quantize(X, R, C, codes, scales, along_cols=cols, stream=stream)
+        mx.mxgemm_quantize(X, R, C, codes, scales, along_cols=cols, stream=stream, rand_bits=rbits)
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
           for _ in range(args.steps)]
     sampler = ClockSampler(None).start()
@@ -356,7 +360,7 @@ def run_quantize(args, world, rank, local):
         if flush is not None:
             flush.zero_()
         a.record(stream)
-        mx.mxgemm_quantize(X, R, C, codes, scales, along_cols=cols, stream=stream)
+        mx.mxgemm_quantize(X, R, C, codes, scales, along_cols=cols, stream=stream, rand_bits=rbits)
         b.record(stream)
     torch.cuda.synchronize(dev)
     t_end = time.perf_counter()
@@ -367,26 +371,31 @@ def run_quantize(args, world, rank, local):
     parity = None
     if rank == 0:
         import oracle
+        rb = rbits.cpu().numpy().view(np.uint32) if sr else None
         if cols:
             # a sample of whole columns (a column's blocks run down all R rows)
             cs = np.random.default_rng(1).integers(0, C, 64)
-            rc, rs = oracle.quantize_e4m3(x[:, cs], along_cols=True)
+            rc, rs = oracle.quantize_e4m3(x[:, cs], along_cols=True,
+                                          rand_bits=None if rb is None else rb[:, cs])
             parity = {"cols": int(cs.size),
                       "codes_equal": bool(np.array_equal(codes.cpu().numpy()[:, cs], rc)),
                       "scales_equal": bool(np.array_equal(scales.cpu().numpy()[cs], rs))}
         else:
             rows = np.random.default_rng(1).integers(0, R, 64)
-            rc, rs = oracle.quantize_e4m3(x[rows])
+            rc, rs = oracle.quantize_e4m3(x[rows], rand_bits=None if rb is None else rb[rows])
             parity = {"rows": int(rows.size),
                       "codes_equal": bool(np.array_equal(codes.cpu().numpy()[rows], rc)),
                       "scales_equal": bool(np.array_equal(scales.cpu().numpy()[rows], rs))}
         print(json.dumps({
-            "metric": "MX quantizer GB/s (read X + write E4M3 codes + E8M0 scales)",
+            "metric": "MX quantizer GB/s (read X + write E4M3 codes + E8M0 scales"
+                      + (" + read random words)" if sr else ")"),
             "value": gbs, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": args.q_dtype, "data": "synthetic",
-            "config": {"workload": f"quantize_{R}x{C}_{args.q_dtype}_{args.q_along}", "R": R,
+            "config": {"workload": f"quantize_{R}x{C}_{args.q_dtype}_{args.q_along}"
+                                   + ("_sr" if sr else ""), "R": R,
                        "C": C, "blocks": "32 down columns" if cols else "32 along rows",
+                       "rounding": "stochastic" if sr else "nearest even",
                        "l2": "flushed between timed steps" if flush is not None else "not flushed"},
             "roofline": {"bound": "hbm", "achieved": gbs / world, "peak": hbm, "unit": "GB/s",
                          "frac": gbs / world / hbm, "peak_source": hbm_src,
@@ -610,6 +619,8 @@ def main(argv=None):
     ap.add_argument("--q-dtype", default="f32", choices=["f32", "bf16"])
     ap.add_argument("--q-along", default="rows", choices=["rows", "cols"],
                     help="quantizer blocks: 32 along rows (A) or down columns (B)")
+    ap.add_argument("--q-round", default="rn", choices=["rn", "sr"],
+                    help="quantizer rounding: nearest even, or stochastic with one random word per value")
     ap.add_argument("--a-format", default="e4m3", choices=FORMATS)
     ap.add_argument("--b-format", default="e4m3", choices=FORMATS)
     ap.add_argument("--no-flush", action="store_true")

@@ -62,6 +62,7 @@ EXPORTED_SYMBOLS = (
     "mxgemm_create", "mxgemm_run", "mxgemm_destroy", "mxgemm_set_option",
     "mxgemm_get_device_status", "mxgemm_status_string", "mxgemm_set_profile_events",
     "mxgemm_get_launch_count", "mxgemm_run_noalloc", "mxgemm_run_host", "mxgemm_quantize",
+    "mxgemm_quantize_sr",
 )
 
 _lib = None
@@ -104,6 +105,8 @@ def library():
         lib.mxgemm_get_launch_count.restype = i32
         lib.mxgemm_quantize.argtypes = [vp, i32, i64, i64, i32, vp, vp, vp]
         lib.mxgemm_quantize.restype = i32
+        lib.mxgemm_quantize_sr.argtypes = [vp, i32, i64, i64, i32, vp, vp, vp, vp]
+        lib.mxgemm_quantize_sr.restype = i32
         lib.mxgemm_run_host.argtypes = [vp, i64, i64, i64, vp, vp, vp, vp, vp, i32, i32, vp]
         lib.mxgemm_run_host.restype = i32
         lib.mxgemm_run_noalloc.argtypes = [i64, i64, i64, vp, vp, vp, vp, vp, i32, i32, vp]
@@ -160,17 +163,27 @@ IN_BF16 = 1
 
 
 def mxgemm_quantize(X, R, C, codes, scales, along_cols=False, x_dtype=None, stream=None,
-                    check: bool = True) -> int:
+                    check: bool = True, rand_bits=None) -> int:
     """MX-quantize the R x C device matrix X (float32 or bfloat16) into E4M3
     codes (R x C bytes) and E8M0 scales per 32 values, along the rows
-    (scales R x C/32) or down the columns (scales C x R/32)."""
+    (scales R x C/32) or down the columns (scales C x R/32).  With rand_bits
+    (an R x C device tensor of 32-bit words) the codes round stochastically
+    (mxgemm_quantize_sr), else to nearest even."""
     if x_dtype is None:
         import torch
         x_dtype = IN_BF16 if getattr(X, "dtype", None) == torch.bfloat16 else IN_F32
-    st = library().mxgemm_quantize(_ptr(X), int(x_dtype), int(R), int(C), int(bool(along_cols)),
-                                   _ptr(codes), _ptr(scales), _stream(stream))
+    if rand_bits is None:
+        st = library().mxgemm_quantize(_ptr(X), int(x_dtype), int(R), int(C),
+                                       int(bool(along_cols)), _ptr(codes), _ptr(scales),
+                                       _stream(stream))
+        name = "mxgemm_quantize"
+    else:
+        st = library().mxgemm_quantize_sr(_ptr(X), int(x_dtype), int(R), int(C),
+                                          int(bool(along_cols)), _ptr(rand_bits), _ptr(codes),
+                                          _ptr(scales), _stream(stream))
+        name = "mxgemm_quantize_sr"
     if check:
-        _check(st, "mxgemm_quantize")
+        _check(st, name)
     return st
 
 

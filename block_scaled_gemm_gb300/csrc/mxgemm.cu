@@ -675,23 +675,58 @@ int mxgemm_destroy(mxgemm_handle_t h) {
 // mxgemm_quantize: MX quantization of a real matrix on the GPU.
 // ===========================================================================
 
-extern "C" int mxgemm_quantize(const void *X, int x_dtype, int64_t R, int64_t C, int along_cols,
-                               void *codes, void *scales, mxgemm_stream_t stream_) {
+namespace {
+
+template <typename T, bool SR>
+void launch_quantize(const T *x, int64_t R, int64_t C, int along_cols, const uint32_t *rbits,
+                     uint8_t *cd, uint8_t *sc, int sms, cudaStream_t stream) {
+  // grid: a few resident blocks per SM, grid-stride loops over the work
+  const int threads = 256;
+  if (!along_cols) {
+    const int64_t nblocks = R * (C / 32);
+    const int64_t warps_needed = (nblocks + 7) / 8;  // a warp takes 8 blocks
+    int grid = static_cast<int>(std::min<int64_t>(cdiv(warps_needed, threads / 32), int64_t(sms) * 8));
+    if (grid < 1) grid = 1;
+    mxg::mx_quantize_rows_kernel<T, SR><<<grid, threads, 0, stream>>>(x, nblocks, rbits, cd, sc);
+  } else {
+    // two adjacent columns per thread when C is even (wider loads and
+    // stores); one with stochastic rounding, whose random words take as many
+    // registers again (two columns measured slower there: spills for FP32
+    // input, lower occupancy for BF16)
+    constexpr bool kPairsOk = !SR;
+    const bool pairs = kPairsOk && C % 2 == 0;
+    const int64_t work = (R / 32) * (pairs ? C / 2 : C);
+    int grid = static_cast<int>(std::min<int64_t>(cdiv(work, threads), int64_t(sms) * 8));
+    if (grid < 1) grid = 1;
+    if constexpr (kPairsOk) {
+      if (pairs) {
+        mxg::mx_quantize_cols_kernel<T, 2, SR><<<grid, threads, 0, stream>>>(x, R, C, rbits, cd, sc);
+        return;
+      }
+    }
+    mxg::mx_quantize_cols_kernel<T, 1, SR><<<grid, threads, 0, stream>>>(x, R, C, rbits, cd, sc);
+  }
+}
+
+int quantize_impl(const void *X, int x_dtype, int64_t R, int64_t C, int along_cols,
+                  const void *rand_bits, bool sr, void *codes, void *scales, mxgemm_stream_t stream_) {
   const int64_t lim = int64_t(1) << 31;
   if (R < 0 || C < 0 || R >= lim || C >= lim) return MXGEMM_ERR_INVALID_VALUE;
   if (x_dtype != MXGEMM_IN_F32 && x_dtype != MXGEMM_IN_BF16) return MXGEMM_ERR_INVALID_VALUE;
   if (along_cols != 0 && along_cols != 1) return MXGEMM_ERR_INVALID_VALUE;
   if ((along_cols ? R % 32 : C % 32) != 0) return MXGEMM_ERR_INVALID_VALUE;
   if (R == 0 || C == 0) return MXGEMM_OK;
-  if (!X || !codes || !scales) return MXGEMM_ERR_INVALID_VALUE;
-  if (reinterpret_cast<uintptr_t>(X) % 16 || reinterpret_cast<uintptr_t>(codes) % 16)
+  if (!X || !codes || !scales || (sr && !rand_bits)) return MXGEMM_ERR_INVALID_VALUE;
+  if (reinterpret_cast<uintptr_t>(X) % 16 || reinterpret_cast<uintptr_t>(codes) % 16 ||
+      reinterpret_cast<uintptr_t>(rand_bits) % 16)
     return MXGEMM_ERR_MISALIGNED;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) {
     cudaGetLastError();
     return MXGEMM_ERR_CUDA;
   }
-  if (!on_device(X, dev) || !on_device(codes, dev) || !on_device(scales, dev))
+  if (!on_device(X, dev) || !on_device(codes, dev) || !on_device(scales, dev) ||
+      (sr && !on_device(rand_bits, dev)))
     return MXGEMM_ERR_INVALID_VALUE;
   int sms = 0;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
@@ -700,41 +735,31 @@ extern "C" int mxgemm_quantize(const void *X, int x_dtype, int64_t R, int64_t C,
   }
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   uint8_t *cd = static_cast<uint8_t *>(codes), *sc = static_cast<uint8_t *>(scales);
-  // grid: a few resident blocks per SM, grid-stride loops over the work
-  const int threads = 256;
-  if (!along_cols) {
-    const int64_t nblocks = R * (C / 32);
-    const int64_t warps_needed = (nblocks + 7) / 8;  // a warp takes 8 blocks
-    int grid = static_cast<int>(std::min<int64_t>(cdiv(warps_needed, threads / 32), int64_t(sms) * 8));
-    if (grid < 1) grid = 1;
-    if (x_dtype == MXGEMM_IN_F32)
-      mxg::mx_quantize_rows_kernel<float><<<grid, threads, 0, stream>>>(
-          static_cast<const float *>(X), nblocks, cd, sc);
-    else
-      mxg::mx_quantize_rows_kernel<__nv_bfloat16><<<grid, threads, 0, stream>>>(
-          static_cast<const __nv_bfloat16 *>(X), nblocks, cd, sc);
+  const uint32_t *rb = static_cast<const uint32_t *>(rand_bits);
+  if (x_dtype == MXGEMM_IN_F32) {
+    const float *x = static_cast<const float *>(X);
+    if (sr) launch_quantize<float, true>(x, R, C, along_cols, rb, cd, sc, sms, stream);
+    else launch_quantize<float, false>(x, R, C, along_cols, nullptr, cd, sc, sms, stream);
   } else {
-    // two adjacent columns per thread when C is even (wider loads and stores)
-    const bool pairs = C % 2 == 0;
-    const int64_t work = (R / 32) * (pairs ? C / 2 : C);
-    int grid = static_cast<int>(std::min<int64_t>(cdiv(work, threads), int64_t(sms) * 8));
-    if (grid < 1) grid = 1;
-    if (x_dtype == MXGEMM_IN_F32) {
-      const float *x = static_cast<const float *>(X);
-      if (pairs)
-        mxg::mx_quantize_cols_kernel<float, 2><<<grid, threads, 0, stream>>>(x, R, C, cd, sc);
-      else
-        mxg::mx_quantize_cols_kernel<float, 1><<<grid, threads, 0, stream>>>(x, R, C, cd, sc);
-    } else {
-      const __nv_bfloat16 *x = static_cast<const __nv_bfloat16 *>(X);
-      if (pairs)
-        mxg::mx_quantize_cols_kernel<__nv_bfloat16, 2><<<grid, threads, 0, stream>>>(x, R, C, cd, sc);
-      else
-        mxg::mx_quantize_cols_kernel<__nv_bfloat16, 1><<<grid, threads, 0, stream>>>(x, R, C, cd, sc);
-    }
+    const __nv_bfloat16 *x = static_cast<const __nv_bfloat16 *>(X);
+    if (sr) launch_quantize<__nv_bfloat16, true>(x, R, C, along_cols, rb, cd, sc, sms, stream);
+    else launch_quantize<__nv_bfloat16, false>(x, R, C, along_cols, nullptr, cd, sc, sms, stream);
   }
   if (cudaGetLastError() != cudaSuccess) return MXGEMM_ERR_CUDA;
   return MXGEMM_OK;
+}
+
+}  // namespace
+
+extern "C" int mxgemm_quantize(const void *X, int x_dtype, int64_t R, int64_t C, int along_cols,
+                               void *codes, void *scales, mxgemm_stream_t stream) {
+  return quantize_impl(X, x_dtype, R, C, along_cols, nullptr, false, codes, scales, stream);
+}
+
+extern "C" int mxgemm_quantize_sr(const void *X, int x_dtype, int64_t R, int64_t C,
+                                  int along_cols, const void *rand_bits, void *codes,
+                                  void *scales, mxgemm_stream_t stream) {
+  return quantize_impl(X, x_dtype, R, C, along_cols, rand_bits, true, codes, scales, stream);
 }
 
 // ===========================================================================

@@ -11,6 +11,13 @@
 // conversion (round to nearest even, saturating at +-448, which equals the
 // clamp).  Inputs must be finite.
 //
+// Stochastic rounding (the FP32 -> FP8 rounding with caller-supplied random
+// bits of "TLX API Quick Reference", section "Utility", `tlx.stoch_round`):
+// each value has its own 32-bit random word r, and the scaled FP32 value
+// y = x * 2^(127 - scale) rounds to the E4M3 magnitude above |y| with
+// probability (|y| - lo) / q, lo the E4M3 magnitude below and q the spacing
+// there, decided exactly as r < 2^32 (|y| - lo) / q (see mx_e4m3_sr).
+//
 // HBM-bound: each value is read once and its code written once.
 #pragma once
 #include <cuda_bf16.h>
@@ -47,6 +54,43 @@ __device__ __forceinline__ uint32_t mx_e4m3(float y) {
   return static_cast<uint32_t>(__nv_cvt_float_to_fp8(y, __NV_SATFINITE, __NV_E4M3));
 }
 
+// E4M3 code of y by stochastic rounding with the random word r.  |y| is
+// clamped to 448 and written m * 2^-sh * q with q = 2^qe the E4M3 spacing at
+// |y| (2^(e-3) in the binade [2^e, 2^(e+1)) for e >= -6, else 2^-9) and m the
+// FP32 significand; lo = floor(m / 2^sh) q, and the rounding goes up when
+// r * 2^sh < rem * 2^32, rem = m mod 2^sh.  32-bit integer arithmetic, exact.
+//   |y| >= 2^-6 (E4M3 normal): sh = 20, so lo is |y| with the low 20 FP32
+//   mantissa bits cleared, the test is r < rem * 2^12, and rounding up adds
+//   one unit of the 21st bit (a carry into the exponent is the next binade).
+//   The FP32 encoding of the result then maps to the E4M3 code directly:
+//   exponent - 120 and the top three mantissa bits.
+//   |y| < 2^-6 (subnormal grid, q = 2^-9): sh = 21..140; for sh <= 32 the
+//   test is r < rem * 2^(32-sh) (below 2^32, as rem < 2^sh), for sh = 32 + t
+//   it is r < ceil(rem / 2^t), which is 1 once 2^t > rem.
+// The sign is kept, also for zero.
+__device__ __forceinline__ uint32_t mx_e4m3_sr(float y, uint32_t r) {
+  const uint32_t bits = __float_as_uint(y);
+  const uint32_t sign = (bits >> 24) & 0x80u;
+  const uint32_t a = min(bits & 0x7FFFFFFFu, 0x43E00000u);  // 0x43E00000 = 448.0f
+  if (a >= 0x3C800000u) {                                    // 0x3C800000 = 2^-6
+    const uint32_t v = (a & ~0xFFFFFu) + (r < ((a & 0xFFFFFu) << 12) ? 0x100000u : 0u);
+    return sign | ((v >> 20) - (120u << 3));
+  }
+  const int be = static_cast<int>(a >> 23);                 // 0 when FP32-subnormal
+  const uint32_t m = be ? (a & 0x7FFFFFu) | 0x800000u : a;  // |y| = m * 2^(max(be,1) - 150)
+  const int sh = 141 - max(be, 1);                          // log2(2^-9 / 2^(max(be,1) - 150))
+  const uint32_t n = sh < 32 ? m >> sh : 0u;                // |y| / 2^-9, rounded down (< 8)
+  const uint32_t rem = sh < 32 ? m & ((1u << sh) - 1u) : m;
+  bool up;
+  if (sh <= 32) {
+    up = r < (rem << (32 - sh));
+  } else {
+    const int t = sh - 32;  // rem = m < 2^24
+    up = t < 24 ? r < ((rem + (1u << t) - 1u) >> t) : (r == 0u && rem != 0u);
+  }
+  return sign | (n + (up ? 1u : 0u));  // 8 is the code of 2^-6 too
+}
+
 template <typename T>
 __device__ __forceinline__ float mx_to_float(T v);
 template <>
@@ -59,8 +103,10 @@ __device__ __forceinline__ float mx_to_float<__nv_bfloat16>(__nv_bfloat16 v) {
 // Blocks along the rows (X is R x C, C % 32 == 0; scales R x C/32): the
 // blocks are contiguous in memory, block b = elements [32b, 32b + 32).
 // Four lanes share a block, eight values each; a warp covers eight blocks.
-template <typename T>
+// SR: rbits holds one random word per element, at the element's index.
+template <typename T, bool SR>
 __global__ void mx_quantize_rows_kernel(const T *__restrict__ X, int64_t nblocks,
+                                        const uint32_t *__restrict__ rbits,
                                         uint8_t *__restrict__ codes, uint8_t *__restrict__ scales) {
   const int lane = threadIdx.x & 31;
   const int sub = lane & 3;  // lane within the block's four
@@ -71,9 +117,19 @@ __global__ void mx_quantize_rows_kernel(const T *__restrict__ X, int64_t nblocks
     const int64_t b = gw * 8 + (lane >> 2);
     const bool live = b < nblocks;
     float v[8];
+    uint32_t r[8];  // random words (stochastic rounding), loaded with the values
 #pragma unroll
-    for (int e = 0; e < 8; ++e) v[e] = 0.0f;
+    for (int e = 0; e < 8; ++e) {
+      v[e] = 0.0f;
+      r[e] = 0u;
+    }
     if (live) {
+      if constexpr (SR) {
+        const uint4 r0 = reinterpret_cast<const uint4 *>(rbits + b * 32 + sub * 8)[0];
+        const uint4 r1 = reinterpret_cast<const uint4 *>(rbits + b * 32 + sub * 8)[1];
+        r[0] = r0.x; r[1] = r0.y; r[2] = r0.z; r[3] = r0.w;
+        r[4] = r1.x; r[5] = r1.y; r[6] = r1.z; r[7] = r1.w;
+      }
       const T *src = X + b * 32 + sub * 8;
       if constexpr (sizeof(T) == 4) {
         const float4 q0 = reinterpret_cast<const float4 *>(src)[0];
@@ -97,8 +153,17 @@ __global__ void mx_quantize_rows_kernel(const T *__restrict__ X, int64_t nblocks
     amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
     const int s = mx_scale_of(amax);
     const float m = mx_pow2(s);
-    uint32_t w0 = mx_e4m3x2(v[0] * m, v[1] * m) | (mx_e4m3x2(v[2] * m, v[3] * m) << 16);
-    uint32_t w1 = mx_e4m3x2(v[4] * m, v[5] * m) | (mx_e4m3x2(v[6] * m, v[7] * m) << 16);
+    uint32_t w0, w1;
+    if constexpr (SR) {
+      uint32_t c[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) c[e] = mx_e4m3_sr(v[e] * m, r[e]);
+      w0 = c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24);
+      w1 = c[4] | (c[5] << 8) | (c[6] << 16) | (c[7] << 24);
+    } else {
+      w0 = mx_e4m3x2(v[0] * m, v[1] * m) | (mx_e4m3x2(v[2] * m, v[3] * m) << 16);
+      w1 = mx_e4m3x2(v[4] * m, v[5] * m) | (mx_e4m3x2(v[6] * m, v[7] * m) << 16);
+    }
     if (live) {
       *reinterpret_cast<uint2 *>(codes + b * 32 + sub * 8) = make_uint2(w0, w1);
       if (sub == 0) scales[b] = static_cast<uint8_t>(s);
@@ -111,9 +176,12 @@ __global__ void mx_quantize_rows_kernel(const T *__restrict__ X, int64_t nblocks
 // neighbouring threads take neighbouring column pairs, so every row access
 // of a warp is contiguous, NC x 32 x sizeof(T) bytes wide.  The thread holds
 // its 32 rows as loaded words (all loads issued before the first use) and
-// stores NC codes per row.  NC = 2 needs C even.
-template <typename T, int NC>
+// stores NC codes per row.  NC = 2 needs C even.  SR (NC = 1): rbits holds
+// one random word per element, at the element's index; they are loaded with
+// the values.
+template <typename T, int NC, bool SR>
 __global__ void mx_quantize_cols_kernel(const T *__restrict__ X, int64_t R, int64_t C,
+                                        const uint32_t *__restrict__ rbits,
                                         uint8_t *__restrict__ codes, uint8_t *__restrict__ scales) {
   static_assert(NC == 1 || NC == 2, "one or two columns per thread");
   constexpr int kWordBytes = NC * static_cast<int>(sizeof(T));
@@ -128,9 +196,15 @@ __global__ void mx_quantize_cols_kernel(const T *__restrict__ X, int64_t R, int6
        i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
     const int64_t rb = i / groups, j = (i - rb * groups) * NC;
     const T *src = X + rb * 32 * C + j;
+    static_assert(!SR || NC == 1, "stochastic rounding takes one column per thread");
     Word raw[32];
+    uint32_t rw[SR ? 32 : 1];  // random words (stochastic rounding), loaded with the values
+    const uint32_t *rsrc = SR ? rbits + rb * 32 * C + j : nullptr;
 #pragma unroll
-    for (int e = 0; e < 32; ++e) raw[e] = *reinterpret_cast<const Word *>(src + e * C);
+    for (int e = 0; e < 32; ++e) {
+      raw[e] = *reinterpret_cast<const Word *>(src + e * C);
+      if constexpr (SR) rw[e] = rsrc[e * C];
+    }
     float amax[NC];
 #pragma unroll
     for (int c = 0; c < NC; ++c) amax[c] = 0.0f;
@@ -151,11 +225,14 @@ __global__ void mx_quantize_cols_kernel(const T *__restrict__ X, int64_t R, int6
 #pragma unroll
     for (int e = 0; e < 32; ++e) {
       const T *t = reinterpret_cast<const T *>(&raw[e]);
-      if constexpr (NC == 2)
+      if constexpr (SR) {
+        dst[e * C] = static_cast<uint8_t>(mx_e4m3_sr(mx_to_float<T>(t[0]) * m[0], rw[e]));
+      } else if constexpr (NC == 2) {
         *reinterpret_cast<uint16_t *>(dst + e * C) = static_cast<uint16_t>(
             mx_e4m3x2(mx_to_float<T>(t[0]) * m[0], mx_to_float<T>(t[1]) * m[1]));
-      else
+      } else {
         dst[e * C] = static_cast<uint8_t>(mx_e4m3(mx_to_float<T>(t[0]) * m[0]));
+      }
     }
 #pragma unroll
     for (int c = 0; c < NC; ++c) scales[(j + c) * rblocks + rb] = static_cast<uint8_t>(s[c]);

@@ -38,8 +38,9 @@
  *
  * Entry points: mxgemm_run (device operands), mxgemm_run_host (host
  * operands, copies pipelined with the GEMM), mxgemm_run_noalloc (no device
- * allocation, fixed scratch), mxgemm_quantize (FP32/BF16 -> E4M3 codes and
- * E8M0 scales on the GPU), plus handle, option, status and timing helpers.
+ * allocation, fixed scratch), mxgemm_quantize and mxgemm_quantize_sr
+ * (FP32/BF16 -> E4M3 codes and E8M0 scales on the GPU, rounding to nearest
+ * or stochastically), plus handle, option, status and timing helpers.
  */
 #ifndef MXGEMM_H_
 #define MXGEMM_H_
@@ -185,6 +186,22 @@ int mxgemm_run_host(mxgemm_handle_t h, int64_t M, int64_t N, int64_t K,
 typedef enum { MXGEMM_IN_F32 = 0, MXGEMM_IN_BF16 = 1 } mxgemm_in_dtype_t;
 int mxgemm_quantize(const void *X, int x_dtype, int64_t R, int64_t C, int along_cols,
                     void *codes, void *scales, mxgemm_stream_t stream);
+
+/* mxgemm_quantize with stochastic rounding of the codes: the FP32 -> FP8
+ * rounding with caller-supplied random bits ("TLX API Quick Reference",
+ * section "Utility", tlx.stoch_round).  The scales are those of
+ * mxgemm_quantize.  Element (i, j) is scaled to the FP32 value
+ * y = X[i][j] * 2^(127 - scale); with lo <= |y| < lo + q the E4M3
+ * magnitudes around |y| (|y| clamped to 448) and r = rand_bits[i * C + j],
+ * the code is lo + q when r < 2^32 * (|y| - lo) / q, else lo (so it rounds up
+ * with probability (|y| - lo) / q); the sign is kept.
+ *   rand_bits : device pointer, R x C uint32 words, row-major (the index of
+ *               X, for either block direction), 16-byte aligned
+ *               (MXGEMM_ERR_MISALIGNED); read only.  NULL is invalid.
+ * Other arguments, layouts and errors as for mxgemm_quantize. */
+int mxgemm_quantize_sr(const void *X, int x_dtype, int64_t R, int64_t C, int along_cols,
+                       const void *rand_bits, void *codes, void *scales,
+                       mxgemm_stream_t stream);
 
 /* Set an option (mxgemm_option_t) on the handle; applies to later runs. */
 int mxgemm_set_option(mxgemm_handle_t h, int option, int64_t value);
