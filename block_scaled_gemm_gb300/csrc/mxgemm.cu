@@ -54,8 +54,7 @@ struct Plan {
   mxg::RepackArgs ra, rb;
   int blocks_a = 0, blocks_b = 0;
   int units = 0;     // persistent CTAs (pairs) of the GEMM grid
-  int *flags = nullptr;
-  int nflags = 0;
+  bool repack = false;  // pairs: the scale chunks come from the repack prepass
 
   bool matches(int64_t M_, int64_t N_, int64_t K_, const void *A_, const void *As_, const void *B_,
                const void *Bs_, void *C_, int ua, int od, int md, int sl, int sc, int sk_,
@@ -88,6 +87,10 @@ struct mxgemm_ctx {
   int device = 0;
   int sm_count = 0;
   int *d_status = nullptr;  // [0] status code, [1] detail
+  // partial-sum flags: one slot per (CTA, epilogue warp), zeroed once at
+  // creation; each launch writes and waits for its own epoch (never 0)
+  unsigned *flags = nullptr;
+  unsigned epoch = 0;
   Workspace ws;
   PFN_cuTensorMapEncodeTiled_v12000 encode = nullptr;
   long long timeout_ns = 2000000000LL;
@@ -316,10 +319,10 @@ Split plan_split(int64_t T, int64_t S, int P, bool allow_tail, bool allow_stream
   return r;
 }
 
-// Workspace layout of a run: repacked scales, re-pitched (or packed) B,
-// stream-K partials and flags, packed A (6- and 4-bit A formats).
+// Workspace layout of a run: repacked scales (pairs), re-pitched (or
+// packed) B, stream-K partials, packed A (6- and 4-bit A formats).
 struct Sizes {
-  size_t off_sfb, off_b, off_part, off_flags, off_a, total;
+  size_t off_sfb, off_b, off_part, off_a, total;
 };
 
 Sizes plan_sizes(int64_t a_chunks, int64_t b_chunks, bool pad_b, int64_t K, int64_t npad,
@@ -328,8 +331,8 @@ Sizes plan_sizes(int64_t a_chunks, int64_t b_chunks, bool pad_b, int64_t K, int6
   z.off_sfb = round_up(static_cast<size_t>(a_chunks) * 512, 1024);
   z.off_b = round_up(z.off_sfb + static_cast<size_t>(b_chunks) * 512, 1024);
   z.off_part = round_up(z.off_b + (pad_b ? static_cast<size_t>(K) * npad : 0), 1024);
-  z.off_flags = z.off_part + static_cast<size_t>(sp.sk_ctas) * CG * 128 * 256 * sizeof(float);
-  z.off_a = round_up(z.off_flags + static_cast<size_t>(sp.sk_ctas) * CG * sizeof(int) + 16, 1024);
+  z.off_a = round_up(z.off_part + static_cast<size_t>(sp.sk_ctas) * CG * 128 * 256 * sizeof(float),
+                     1024);
   z.total = round_up(z.off_a + a_bytes, 1024);
   return z;
 }
@@ -340,7 +343,7 @@ int build_plan(mxgemm_ctx *h, Plan *pl, int64_t M, int64_t N, int64_t K, const v
                const void *A_scale, const void *B, const void *B_scale, void *C, int use_acc,
                int out_dtype, int CG, int64_t m_tiles, int64_t n_tiles, int64_t k_steps,
                int64_t num_tiles, int64_t a_chunks, int64_t b_chunks, bool pad_b, int64_t npad,
-               const Split &sp, const Sizes &z, int a_bits, int b_bits) {
+               const Split &sp, const Sizes &z, int a_bits, int b_bits, bool fused) {
   const size_t off_sfb = z.off_sfb, off_b = z.off_b;
   const size_t esz = out_dtype == MXGEMM_OUT_F32 ? 4 : 2;
   const int64_t kb = K / 32;
@@ -361,11 +364,27 @@ int build_plan(mxgemm_ctx *h, Plan *pl, int64_t M, int64_t N, int64_t K, const v
   if (encode_2d(h, &pl->tA, u8, asrc, K, M, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
       encode_2d(h, &pl->tB, u8, bsrc, N, K, bpitch, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
       // half-width tiles of CTA pairs: 64 columns per CTA
-      encode_2d(h, &pl->tB64, u8, bsrc, N, K, bpitch, 64, 128, CU_TENSOR_MAP_SWIZZLE_64B) ||
-      // scale chunks are contiguous 512-byte blocks; fetched as rows of 128
-      // bytes (4 rows per chunk) so each chunk is a handful of TMA requests
-      encode_2d(h, &pl->tSA, u8, sfa, 128, a_chunks * 4, 128, 128, 4, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-      encode_2d(h, &pl->tSB, u8, sfb, 128, b_chunks * 4, 128, 128, 8, CU_TENSOR_MAP_SWIZZLE_NONE))
+      encode_2d(h, &pl->tB64, u8, bsrc, N, K, bpitch, 64, 128, CU_TENSOR_MAP_SWIZZLE_64B))
+    return MXGEMM_ERR_CUDA;
+  // Repacked scale chunks are contiguous 512-byte blocks, fetched as rows of
+  // 128 bytes (4 rows per chunk) so each chunk is a handful of TMA requests.
+  // With fused scales (single CTAs) the kernel builds the chunks; the scale
+  // maps then describe the row-major scales themselves (16-byte segments of
+  // 128 A rows or 256 B rows), usable when the row pitch K/32 and both bases
+  // are multiples of 16 bytes.
+  std::memset(&pl->tSA, 0, sizeof(pl->tSA));
+  std::memset(&pl->tSB, 0, sizeof(pl->tSB));
+  pl->repack = !fused;
+  const bool scale_tma = fused && kb % 16 == 0 &&
+                         reinterpret_cast<uintptr_t>(A_scale) % 16 == 0 &&
+                         reinterpret_cast<uintptr_t>(B_scale) % 16 == 0;
+  if (pl->repack &&
+      (encode_2d(h, &pl->tSA, u8, sfa, 128, a_chunks * 4, 128, 128, 4, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+       encode_2d(h, &pl->tSB, u8, sfb, 128, b_chunks * 4, 128, 128, 8, CU_TENSOR_MAP_SWIZZLE_NONE)))
+    return MXGEMM_ERR_CUDA;
+  if (scale_tma &&
+      (encode_2d(h, &pl->tSA, u8, A_scale, kb, M, kb, 16, 128, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+       encode_2d(h, &pl->tSB, u8, B_scale, kb, N, kb, 16, 256, CU_TENSOR_MAP_SWIZZLE_NONE)))
     return MXGEMM_ERR_CUDA;
   // C: stored through TMA (128-byte-wide boxes, 16 rows) when its row pitch
   // allows it; otherwise the kernel stores directly and tC is unused.
@@ -400,12 +419,16 @@ int build_plan(mxgemm_ctx *h, Plan *pl, int64_t M, int64_t N, int64_t K, const v
   kp.sk_ctas = sp.sk_ctas;
   kp.sk_units = sp.sk_units;
   kp.partials = reinterpret_cast<float *>(h->ws.ptr + z.off_part);
-  kp.flags = reinterpret_cast<int *>(h->ws.ptr + z.off_flags);
+  kp.flags = h->flags;
+  kp.epoch = 0;  // set per launch
   kp.half_tiles = sp.half_tiles;
   kp.idesc_fmt = mxg::fmt_bits(h->a_fmt, h->b_fmt);
+  kp.a_scale = static_cast<const uint8_t *>(A_scale);
+  kp.b_scale = static_cast<const uint8_t *>(B_scale);
+  kp.kb_count = static_cast<int>(kb);
+  kp.fused_scales = fused ? 1 : 0;
+  kp.scale_tma = scale_tma ? 1 : 0;
   pl->units = sp.units;
-  pl->flags = kp.flags;
-  pl->nflags = sp.sk_ctas * CG;
   pl->CG = CG;
   pl->pad_b = pad_b;
   pl->npad = npad;
@@ -478,6 +501,21 @@ int mxgemm_create(mxgemm_handle_t *out, int device) {
     return MXGEMM_ERR_OUT_OF_MEMORY;
   }
   if (cudaMemset(h->d_status, 0, 2 * sizeof(int)) != cudaSuccess) {
+    cudaFree(h->d_status);
+    delete h;
+    return MXGEMM_ERR_CUDA;
+  }
+  // a flag slot per epilogue warp of every CTA a grid can have
+  const size_t flag_bytes = static_cast<size_t>(h->sm_count) * mxg::Cfg<1>::EPI_WARPS * sizeof(unsigned);
+  if (cudaMalloc(&h->flags, flag_bytes) != cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(h->d_status);
+    delete h;
+    return MXGEMM_ERR_OUT_OF_MEMORY;
+  }
+  if (cudaMemset(h->flags, 0, flag_bytes) != cudaSuccess) {
+    cudaGetLastError();
+    cudaFree(h->flags);
     cudaFree(h->d_status);
     delete h;
     return MXGEMM_ERR_CUDA;
@@ -558,8 +596,15 @@ int mxgemm_run(mxgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A
   const int64_t k_steps = cdiv(K, 128);
   const int64_t num_tiles = m_tiles * n_tiles;
   if (num_tiles >= lim) return MXGEMM_ERR_INVALID_VALUE;
-  const int64_t a_chunks = m_tiles * CG * k_steps;  // 512-byte chunks of A scales
-  const int64_t b_chunks = n_tiles * k_steps * 2;   // 2 per 256 columns
+  // Scale chunks: built in the kernel from the row-major scales (single
+  // CTAs on one row of tiles, M <= 128: the kernel streams B and has SM time
+  // to spare, and no prepass runs before it), else repacked by a prepass into
+  // 512-byte chunks.  On full tiles the in-kernel build measured slower: its
+  // 16-byte row segments cost TMA and shared-memory transactions that the
+  // mainloop needs (1-CTA square 4096: 64.1 us against 58.0 with the prepass).
+  const bool fused = CG == 1 && M <= 128;
+  const int64_t a_chunks = fused ? 0 : m_tiles * CG * k_steps;
+  const int64_t b_chunks = fused ? 0 : n_tiles * k_steps * 2;  // 2 per 256 columns
   // 6- and 4-bit formats are packed 16 elements per 16-byte group first
   const int a_bits = h->a_fmt == MXGEMM_FMT_E2M1 ? 4 : h->a_fmt >= MXGEMM_FMT_E2M3 ? 6 : 8;
   const int b_bits = h->b_fmt == MXGEMM_FMT_E2M1 ? 4 : h->b_fmt >= MXGEMM_FMT_E2M3 ? 6 : 8;
@@ -596,7 +641,7 @@ int mxgemm_run(mxgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A
     plan->valid = false;
     st = build_plan(h, plan, M, N, K, A, A_scale, B, B_scale, C, use_acc, out_dtype, CG, m_tiles,
                     n_tiles, k_steps, num_tiles, a_chunks, b_chunks, pad_b, npad, sp, z, a_bits,
-                    b_bits);
+                    b_bits, fused);
     if (st != MXGEMM_OK) return st;
   }
 
@@ -611,14 +656,19 @@ int mxgemm_run(mxgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A
         static_cast<const uint8_t *>(A), M, K, K, h->ws.ptr + plan->off_a, plan->a_bits);
     ++h->launches;
   }
-  mxg::repack_scales_kernel<<<plan->blocks_a + plan->blocks_b, mxg::kRepackThreads, 0, stream>>>(
-      plan->ra, plan->rb, plan->blocks_a, plan->flags, plan->nflags);
-  h->launches += 1;
+  if (plan->repack) {
+    mxg::repack_scales_kernel<<<plan->blocks_a + plan->blocks_b, mxg::kRepackThreads, 0, stream>>>(
+        plan->ra, plan->rb, plan->blocks_a);
+    h->launches += 1;
+  }
   if (cudaGetLastError() != cudaSuccess) return MXGEMM_ERR_CUDA;
+  mxg::KParams kp = plan->kp;
+  if (++h->epoch == 0) h->epoch = 1;  // 0 is the flags' initial value
+  kp.epoch = h->epoch;
   return plan->CG == 2 ? launch_gemm<2>(h, plan->tA, plan->tB, plan->tB64, plan->tSA, plan->tSB, plan->tC,
-                                        plan->kp, plan->units, stream)
+                                        kp, plan->units, stream)
                        : launch_gemm<1>(h, plan->tA, plan->tB, plan->tB64, plan->tSA, plan->tSB, plan->tC,
-                                        plan->kp, plan->units, stream);
+                                        kp, plan->units, stream);
 }
 
 int mxgemm_get_device_status(mxgemm_handle_t h, mxgemm_stream_t stream_, int *status_out,
@@ -656,6 +706,7 @@ int mxgemm_destroy(mxgemm_handle_t h) {
     cudaDeviceSynchronize();
     if (h->ws.ptr) cudaFree(h->ws.ptr);
     if (h->d_status) cudaFree(h->d_status);
+    if (h->flags) cudaFree(h->flags);
     HostPipe &hp = h->hp;
     if (hp.stage.ptr) cudaFree(hp.stage.ptr);
     for (cudaEvent_t e : {hp.start, hp.b_ready, hp.in_ready[0], hp.in_ready[1], hp.gemm_done[0],
@@ -1071,11 +1122,13 @@ extern "C" int mxgemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A
   const int64_t k_steps = cdiv(K, 128);
   const int64_t num_tiles = m_tiles * n_tiles;
   if (num_tiles >= lim) return MXGEMM_ERR_INVALID_VALUE;
-  const int64_t a_chunks = m_tiles * CG * k_steps;
-  const int64_t b_chunks = n_tiles * k_steps * 2;
+  // the kernel builds the scale chunks itself (fused scales, whatever M):
+  // no repacked scales in the scratch
+  const int64_t a_chunks = 0, b_chunks = 0;
   const bool pad_b = (N % 16) != 0;
   const int64_t npad = round_up(static_cast<size_t>(N), 16);
-  // no stream-K split here: the scratch holds only the repacked scales and B
+  // no stream-K split here (no partial sums or flags): the scratch holds
+  // only a re-pitched B
   const Split sp = plan_split(num_tiles, k_steps, nd->sm_count / CG, false, false, M);
   const Sizes z = plan_sizes(a_chunks, b_chunks, pad_b, K, npad, sp, CG, 0);
   const size_t off_b = z.off_b;
@@ -1101,7 +1154,8 @@ extern "C" int mxgemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A
   }
   Plan plan;
   st = build_plan(&ctx, &plan, M, N, K, A, A_scale, B, B_scale, C, use_acc, out_dtype, CG, m_tiles,
-                  n_tiles, k_steps, num_tiles, a_chunks, b_chunks, pad_b, npad, sp, z, 8, 8);
+                  n_tiles, k_steps, num_tiles, a_chunks, b_chunks, pad_b, npad, sp, z, 8, 8,
+                  true);
   if (st != MXGEMM_OK) return st;
   // the status word must start each call at zero
   if (cudaMemsetAsync(nd->status, 0, 2 * sizeof(int), stream) != cudaSuccess) {
@@ -1111,10 +1165,10 @@ extern "C" int mxgemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A
   if (pad_b)
     mxg::pad_rows_kernel<<<launch_blocks(K * (npad / 16), 256), 256, 0, stream>>>(
         static_cast<const uint8_t *>(B), K, N, npad, nd->scratch + off_b, 8);
-  mxg::repack_scales_kernel<<<plan.blocks_a + plan.blocks_b, mxg::kRepackThreads, 0, stream>>>(
-      plan.ra, plan.rb, plan.blocks_a, plan.flags, plan.nflags);
   if (cudaGetLastError() != cudaSuccess) return MXGEMM_ERR_CUDA;
-  st = launch_gemm<1>(&ctx, plan.tA, plan.tB, plan.tB64, plan.tSA, plan.tSB, plan.tC, plan.kp, plan.units,
+  mxg::KParams kp = plan.kp;
+  kp.epoch = 1;  // no partial sums: the flags are not used
+  st = launch_gemm<1>(&ctx, plan.tA, plan.tB, plan.tB64, plan.tSA, plan.tSB, plan.tC, kp, plan.units,
                       stream);
   {
     std::lock_guard<std::mutex> lock(g_noalloc_mu);

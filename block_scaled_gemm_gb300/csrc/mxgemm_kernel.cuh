@@ -5,9 +5,9 @@
 // Design (one CTA per SM, persistent, warp-specialised):
 //   warp 0      TMA producer: per 128-deep K step loads the A tile (K-major,
 //               128-byte swizzle), the B tile (N-major, 128-byte swizzle) and
-//               the A/B scale chunks into a STAGES-deep shared-memory ring;
-//               each stage has a "full" barrier (arrive + expected bytes) and
-//               an "empty" barrier (released by the MMA's commit).
+//               (pairs) the A/B scale chunks into a STAGES-deep shared-memory
+//               ring; each stage has a "full" barrier (arrives + expected
+//               bytes) and an "empty" barrier (released by the MMA's commit).
 //   warp 1      allocates TMEM; one thread issues, per K step, tcgen05.cp of
 //               the scale chunks SMEM -> TMEM, then four
 //               tcgen05.mma.kind::mxf8f6f4.block_scale (K = 32 each) into an
@@ -16,6 +16,10 @@
 //   warps 2..9  epilogue: wait acc_full, tcgen05.ld the whole accumulator into
 //               registers, release it (acc_empty) so the next tile's MMAs
 //               start, then (optionally + C_in) round to FP32/BF16 and store.
+//   warp 10     (single CTAs) scale loader: builds each stage's A and B scale
+//               chunks in shared memory straight from the row-major A_scale
+//               and B_scale, so no prepass runs before the kernel; pairs
+//               load chunks that a prepass repacked.
 //
 // Pair mode (CG = 2, cluster of 2 CTAs, tcgen05 cta_group::2): the pair
 // computes a 256 x 256 tile; each CTA loads its own 128 rows of A and its own
@@ -53,7 +57,17 @@ struct Cfg {
   static constexpr int B_BYTES = BK * BN_CTA;
   static constexpr int SFA_BYTES = 512;   // 128 rows x 4 K-blocks
   static constexpr int SFB_BYTES = 1024;  // 256 columns x 4 K-blocks
+  // Scale chunks come either from a repack prepass (contiguous 512-byte
+  // chunks, loaded by the producer's TMA with the stage) or, for single CTAs
+  // when the kernel is told so (KParams::fused_scales), from the scale
+  // loader warp, which builds them in shared memory from the row-major
+  // scales.  Pairs always take the prepass: a chunk written by threads of one
+  // CTA and read by the MMA that the other CTA issues would need a
+  // cluster-scope release and acquire on every K step (a cluster-scope wait
+  // there cost ~40% of the MMA rate).
+  static constexpr bool HAS_SCALE_WARP = CG == 1;
   static constexpr uint32_t STAGE_TX = (A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES) * CG;
+  static constexpr uint32_t CHUNK_TX = (SFA_BYTES + SFB_BYTES) * CG;  // the scale chunks
   // half-width (128-column) tile: each CTA loads half of its B columns
   static constexpr uint32_t STAGE_TX_HALF = STAGE_TX - (B_BYTES / 2) * CG;
   static constexpr int OFF_A = 0;
@@ -62,24 +76,33 @@ struct Cfg {
   static constexpr int OFF_SFB = OFF_SFA + STAGES * SFA_BYTES;
   static constexpr int OFF_BAR = OFF_SFB + STAGES * SFB_BYTES;
   static constexpr int CLC_SLOTS = 4;  // cluster-launch-control response ring
-  // full[], empty[], acc_full, acc_empty, final, clc_full[], clc_empty[]
-  static constexpr int NUM_BARS = 2 * STAGES + 3 + 2 * CLC_SLOTS;
+  // full[], empty[], acc_full, acc_empty, final, clc_full[], clc_empty[],
+  // stg (the scale loader's staging buffer has landed), stg_go (the scale
+  // loader has issued its first staging load)
+  static constexpr int NUM_BARS = 2 * STAGES + 3 + 2 * CLC_SLOTS + 2;
   static constexpr int OFF_CLC = (OFF_BAR + NUM_BARS * 8 + 15) / 16 * 16;  // 16-byte responses
   static constexpr int OFF_MISC = OFF_CLC + 16 * CLC_SLOTS;
   // epilogue staging: one 32-row x 64-byte buffer per epilogue warp
   static constexpr int EPI_BUF = 2048;
   static constexpr int OFF_EPI = (OFF_MISC + 16 + 1023) / 1024 * 1024;
-  static constexpr int SMEM_BYTES = OFF_EPI + 8 * EPI_BUF + 1024;  // + slack for 1 KB alignment
+  // scale loader staging (fused scales): one group of four K steps of raw
+  // scale rows, 16 bytes per row: the tile's 128 A rows, then its 256 B rows
+  static constexpr int STG_A_BYTES = 128 * 16;
+  static constexpr int STG_BYTES = HAS_SCALE_WARP ? STG_A_BYTES + 256 * 16 : 0;
+  static constexpr int OFF_STG = OFF_EPI + 8 * EPI_BUF;
+  static constexpr int SMEM_BYTES = OFF_STG + STG_BYTES + 1024;  // + slack for 1 KB alignment
   static constexpr int TM_ACC = 0;
   static constexpr int TM_SFA = BN;               // STAGES x 4 columns
   static constexpr int TM_SFB = BN + 4 * STAGES;  // STAGES x 8 columns
   static constexpr uint32_t TM_COLS = 512;
   static constexpr int EPI_WARPS = 8;
-  static constexpr int THREADS = 32 * (2 + EPI_WARPS);
+  static constexpr int SCALE_WARP = 2 + EPI_WARPS;  // with HAS_SCALE_WARP
+  static constexpr int THREADS = 32 * (2 + EPI_WARPS + (HAS_SCALE_WARP ? 1 : 0));
   static_assert(TM_SFB + 8 * STAGES <= (int)TM_COLS, "TMEM budget");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(OFF_B % 1024 == 0 && A_BYTES % 1024 == 0 && B_BYTES % 1024 == 0, "align");
   static_assert(OFF_BAR % 8 == 0 && OFF_CLC % 16 == 0, "barrier and response alignment");
+  static_assert(OFF_STG % 1024 == 0, "staging alignment");
 };
 
 struct KParams {
@@ -102,13 +125,29 @@ struct KParams {
   int sk_ctas;         // CTAs (pairs) sharing the K steps of tiles [dp_tiles, num_tiles)
   long long sk_units;  // (num_tiles - dp_tiles) * k_steps
   float *partials;     // per CTA: 128 x 256 FP32 partial accumulator
-  int *flags;          // per CTA: epilogue warps that have written its partial
+  // per CTA and epilogue warp: the epoch of the launch whose partial rows
+  // that warp has written (a value never equal to this launch's epoch until
+  // it has been written in this launch, whatever earlier launches left)
+  unsigned *flags;
+  unsigned epoch;      // this launch's number, never 0
   // half-width tail (see WorkIter): items [dp_tiles, dp_tiles + half_tiles)
   // of the whole-tile walk are 128-column halves of tiles dp_tiles, ...
   int half_tiles;
   // element formats of A and B in instruction-descriptor position (bits
   // 7-9 and 10-12); 0 for E4M3 x E4M3
   uint32_t idesc_fmt;
+  // the row-major scales, read by the scale loader (single CTAs):
+  // A_scale M x kb_count, B_scale N x kb_count
+  const uint8_t *a_scale;
+  const uint8_t *b_scale;
+  int kb_count;  // K / 32
+  // single CTAs: the scale loader builds the chunks (else the producer loads
+  // repacked chunks)
+  int fused_scales;
+  // with fused_scales: the scale maps (tmSFA, tmSFB) describe the row-major
+  // scales (16-byte row pitch and base) and the scale loader stages its rows
+  // by TMA; else it loads them with per-lane loads
+  int scale_tma;
 };
 
 // Instruction descriptor of tcgen05.mma.kind::mxf8f6f4.block_scale:
@@ -267,22 +306,25 @@ constexpr int kEpiBF16 = 1;    // BF16 output (else FP32)
 constexpr int kEpiAcc = 2;     // use_acc: C_in is read and added
 constexpr int kEpiTma = 4;     // C's rows are 16-byte aligned: TMA stores
 
-// Bounded wait until *flag (written by other CTAs with release atomics)
-// reaches `target`.
-__device__ __forceinline__ bool wait_flag(const int *flag, int target, const WaitCtl &w,
-                                          int detail) {
+// Bounded wait (whole warp) until the n flag slots at `slots` (written by
+// other CTAs after a fence) all hold `epoch`; lane i < n polls slot i.
+__device__ __forceinline__ bool wait_flags(const unsigned *slots, int n, unsigned epoch,
+                                           const WaitCtl &w, int detail) {
+  const int lane = threadIdx.x & 31;
   const uint64_t t0 = globaltimer_ns();
   for (uint32_t it = 0;; ++it) {
-    int v;
-    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
-    if (v >= target) return true;
+    unsigned v = epoch;
+    if (lane < n)
+      asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(slots + lane) : "memory");
+    if (__all_sync(0xFFFFFFFFu, v == epoch)) return true;
     if ((it & 15u) == 15u) {
-      if (*w.abort_flag) return false;
-      if (globaltimer_ns() - t0 > w.timeout_ns) {
-        if (atomicCAS(w.status, 0, kStatusTimeout) == 0) atomicExch(w.status + 1, detail);
+      bool give_up = *w.abort_flag != 0;
+      if (!give_up && globaltimer_ns() - t0 > w.timeout_ns) {
+        if (lane == 0 && atomicCAS(w.status, 0, kStatusTimeout) == 0) atomicExch(w.status + 1, detail);
         *w.abort_flag = 1;
-        return false;
+        give_up = true;
       }
+      if (__any_sync(0xFFFFFFFFu, give_up)) return false;
     }
     __nanosleep(64);
   }
@@ -410,12 +452,17 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
   const uint32_t bar_final = bar_acc_empty + 8;
   const uint32_t bar_clc_full = bar_final + 8;
   const uint32_t bar_clc_empty = bar_clc_full + 8 * C::CLC_SLOTS;
+  const uint32_t bar_stg = bar_clc_empty + 8 * C::CLC_SLOTS;
+  const uint32_t bar_stg_go = bar_stg + 8;
+  const bool fused = C::HAS_SCALE_WARP && p.fused_scales != 0;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + C::OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + C::OFF_MISC + 4);
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
-      mbar_init(bar_full + 8 * s, 1);
+      // full: the producer's arrive (with the TMA bytes), and with fused
+      // scales the scale loader's arrive once its chunks are written
+      mbar_init(bar_full + 8 * s, fused ? 2 : 1);
       mbar_init(bar_empty + 8 * s, 1);
     }
     mbar_init(bar_acc_full, 1);
@@ -423,9 +470,12 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
     mbar_init(bar_final, 1);
     for (int s = 0; s < C::CLC_SLOTS; ++s) {
       mbar_init(bar_clc_full + 8 * s, 1);
-      // readers of a response: producer + 8 epilogue warps per CTA, and the MMA issuer
-      mbar_init(bar_clc_empty + 8 * s, (1 + C::EPI_WARPS) * CG + 1);
+      // readers of a response: producer + 8 epilogue warps per CTA, the MMA
+      // issuer, and the scale loader with fused scales
+      mbar_init(bar_clc_empty + 8 * s, (1 + C::EPI_WARPS) * CG + 1 + (fused ? 1 : 0));
     }
+    mbar_init(bar_stg, 1);
+    mbar_init(bar_stg_go, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -433,8 +483,10 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
     tma_prefetch_desc(&tmA);
     tma_prefetch_desc(&tmB);
     if (CG == 2 && p.half_tiles > 0) tma_prefetch_desc(&tmB64);
-    tma_prefetch_desc(&tmSFA);
-    tma_prefetch_desc(&tmSFB);
+    if (!fused || p.scale_tma) {
+      tma_prefetch_desc(&tmSFA);
+      tma_prefetch_desc(&tmSFB);
+    }
     if (kTma) tma_prefetch_desc(&tmC);
   }
   if (warp == 1) {
@@ -445,9 +497,10 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
   if constexpr (CG == 2) cluster_sync(); else __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  // The set-up above overlaps the tail of the scale prepass (programmatic
-  // dependent launch); nothing below reads or writes global memory before
-  // that grid has finished.
+  // The set-up above overlaps the tail of the prepass before the kernel, if
+  // any (the scale repack for pairs, the B re-pitch; programmatic dependent
+  // launch); nothing below reads or writes global memory before that grid
+  // has finished.
   griddep_wait();
 
   const WaitCtl wc{p.status, abort_flag, p.timeout_ns};
@@ -484,6 +537,11 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
       Sched<CG, C::CLC_SLOTS> wi(p, unit, units, &ring, true, rank, &wc);
       WorkItem w;
       bool ok = !p.stall_producer && wi.next(w);
+      // fused scales: the scale loader's first staging load goes to the TMA
+      // unit ahead of the stages' A and B loads (behind them it would wait
+      // for a whole ring of operand bytes and hold up the first MMA)
+      if (fused && ok)
+        ok = __all_sync(0xFFFFFFFFu, wait_phase<false>(bar_stg_go, 0, wc, 0x0C));
       int ks = w.kb, mt = 0, nt = 0;
       if (ok) tile_coords(w.tile, p.m_tiles, p.n_tiles, mt, nt);
       // whole tiles in the unrolled loop below; half-width tiles (only ever
@@ -505,12 +563,15 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
         const int col0 = nt * 256;
         const int k0 = ks * 128;
         if constexpr (CG == 1) {
-          mbar_arrive_expect_tx(fb, C::STAGE_TX);
+          // (fused: the scale chunks come from the scale loader)
+          mbar_arrive_expect_tx(fb, fused ? C::STAGE_TX - C::CHUNK_TX : C::STAGE_TX);
           tma_load_2d(sA, &tmA, k0, row0, fb);
           tma_load_2d(sB, &tmB, col0, k0, fb);
           tma_load_2d(sB + 16384, &tmB, col0 + 128, k0, fb);
-          tma_load_2d(sSA, &tmSFA, 0, (mblk * p.k_steps + ks) * 4, fb);
-          tma_load_2d(sSB, &tmSFB, 0, (nt * p.k_steps + ks) * 8, fb);
+          if (!fused) {
+            tma_load_2d(sSA, &tmSFA, 0, (mblk * p.k_steps + ks) * 4, fb);
+            tma_load_2d(sSB, &tmSFB, 0, (nt * p.k_steps + ks) * 8, fb);
+          }
         } else {
           if (rank == 0) mbar_arrive_expect_tx(fb, C::STAGE_TX);
           const uint32_t fbl = mapa_shared(fb, 0);  // leader's barrier
@@ -613,11 +674,13 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
           const int col0 = nt * 256 + 128 * w.half;
           const int k0 = ks * 128;
           if constexpr (CG == 1) {
-            mbar_arrive_expect_tx(fb, C::STAGE_TX_HALF);
+            mbar_arrive_expect_tx(fb, fused ? C::STAGE_TX_HALF - C::CHUNK_TX : C::STAGE_TX_HALF);
             tma_load_2d(sA, &tmA, k0, row0, fb);
             tma_load_2d(sB, &tmB, col0, k0, fb);
-            tma_load_2d(sSA, &tmSFA, 0, (mblk * p.k_steps + ks) * 4, fb);
-            tma_load_2d(sSB, &tmSFB, 0, (nt * p.k_steps + ks) * 8, fb);
+            if (!fused) {
+              tma_load_2d(sSA, &tmSFA, 0, (mblk * p.k_steps + ks) * 4, fb);
+              tma_load_2d(sSB, &tmSFB, 0, (nt * p.k_steps + ks) * 8, fb);
+            }
           } else {
             if (rank == 0) mbar_arrive_expect_tx(fb, C::STAGE_TX_HALF);
             const uint32_t fbl = mapa_shared(fb, 0);
@@ -874,6 +937,148 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
       __syncwarp();
       wait_phase<false>(bar_final, 0, wf, 0x04);
     }
+  } else if (C::HAS_SCALE_WARP && warp == C::SCALE_WARP) {
+    // ------------------------------------------------------------ scale loader
+    // Per K step, the stage's A scale chunk (the tile's 128 rows) and B scale
+    // chunks (its 256 columns, as two 128-row chunks) in the byte order that
+    // tcgen05.cp .32x128b.warpx4 takes: lane l writes the 16-byte row l of
+    // each chunk, whose 4-byte word q holds the step's four K-block scales of
+    // row l + 32 q.  Those are four consecutive bytes of that row of A_scale
+    // (B_scale), so a group of four K steps needs 16 bytes of each of the
+    // tile's rows, and a chunk row is one word of each of four such 16-byte
+    // row segments.
+    //   The segments of a group are staged by TMA (2-D boxes of 16 bytes x
+    // 128 A rows and x 256 B rows; rows beyond M or N read as zero, i.e.
+    // 2^-127, and meet only the zero-filled operand rows there) while the
+    // previous group's chunks are written; lane l then reads its rows from
+    // the staging buffer.  Per-lane global loads of the segments (32 rows per
+    // load instruction) measured ~27% off the MMA rate of single-CTA tiles,
+    // so they serve only scales whose row pitch or base rules out TMA (K not
+    // a multiple of 512, or an unaligned pointer): byte loads, 127 past the
+    // end of a row.
+    //   A stage is handed to the MMA issuer by an arrive on its full barrier
+    // after a proxy fence (tcgen05.cp reads the chunks through the async
+    // proxy).
+    if (C::HAS_SCALE_WARP && fused) {
+      ClcRing ring = clc_ring;
+      Sched<CG, C::CLC_SLOTS> wi(p, unit, units, &ring, false, rank, &wc);
+      WorkItem w, wn;
+      int st = 0;
+      uint32_t ph = 0;
+      bool ok = true;
+      const bool tma = p.scale_tma != 0;
+      const uint32_t stg = base + C::OFF_STG;
+      uint32_t sph = 0;     // phase of the staging barrier
+      bool staged = false;  // a staging load is issued and not yet read
+      const int kbn = p.kb_count;
+      uint4 ca[4], cb[8];   // the current group's segments: A rows lane + 32 q, B rows
+      // group g (K steps 4g .. 4g+3) of item `it`: start its staging load
+      auto stage = [&](const WorkItem &it, int g) {
+        if (!tma) return;
+        int mt = 0, nt = 0;
+        tile_coords(it.tile, p.m_tiles, p.n_tiles, mt, nt);
+        if (lane == 0) {
+          mbar_arrive_expect_tx(bar_stg, C::STG_BYTES);
+          tma_load_2d(stg, &tmSFA, 16 * g, mt * 128, bar_stg);
+          tma_load_2d(stg + C::STG_A_BYTES, &tmSFB, 16 * g, nt * 256, bar_stg);
+        }
+        __syncwarp();
+        staged = true;
+      };
+      // 16 scale bytes (K-blocks 16 g .. 16 g + 15) of row `row` of S, byte by byte
+      auto load16 = [&](const uint8_t *S, int64_t row, int64_t rows, int g) -> uint4 {
+        uint32_t x[4] = {0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu};
+        if (row < rows) {
+          const uint8_t *src = S + row * kbn + 16 * g;
+#pragma unroll
+          for (int b = 0; b < 16; ++b) {
+            const uint32_t v = 16 * g + b < kbn ? static_cast<uint32_t>(src[b]) : 127u;
+            x[b >> 2] = (x[b >> 2] & ~(0xFFu << (8 * (b & 3)))) | (v << (8 * (b & 3)));
+          }
+        }
+        return make_uint4(x[0], x[1], x[2], x[3]);
+      };
+      // make group g of item `it` the current one
+      auto take = [&](const WorkItem &it, int g) -> bool {
+        if (tma) {
+          if (!__all_sync(0xFFFFFFFFu, wait_phase<false>(bar_stg, sph, wc, 0x0A)))
+            return false;
+          sph ^= 1u;
+          staged = false;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) ca[q] = ld_shared_v4(stg + 16 * (lane + 32 * q));
+#pragma unroll
+          for (int q = 0; q < 8; ++q) cb[q] = ld_shared_v4(stg + C::STG_A_BYTES + 16 * (lane + 32 * q));
+          // the reads are ordered before the next staging load's writes
+          fence_proxy_async_smem();
+          __syncwarp();
+        } else {
+          int mt = 0, nt = 0;
+          tile_coords(it.tile, p.m_tiles, p.n_tiles, mt, nt);
+          const int64_t arow = static_cast<int64_t>(mt) * 128 + lane;
+          const int64_t brow = static_cast<int64_t>(nt) * 256 + lane;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) ca[q] = load16(p.a_scale, arow + 32 * q, p.M, g);
+#pragma unroll
+          for (int q = 0; q < 8; ++q) cb[q] = load16(p.b_scale, brow + 32 * q, p.N, g);
+        }
+        return true;
+      };
+      auto pick = [](const uint4 &x, int t) -> uint32_t {
+        return t == 0 ? x.x : t == 1 ? x.y : t == 2 ? x.z : x.w;
+      };
+      bool have = wi.next(w), have_n = false;
+      if (have) stage(w, w.kb >> 2);
+      if (lane == 0) mbar_arrive(bar_stg_go);  // the producer may start
+      while (ok && have) {
+        for (int ks = w.kb; ks < w.ke; ++ks) {
+          const int g = ks >> 2;
+          if (ks == w.kb || (ks & 3) == 0) {
+            // this group becomes current; the next one (of this item, else
+            // the first of the next item) is staged meanwhile
+            if (!take(w, g)) {
+              ok = false;
+              break;
+            }
+            if (4 * (g + 1) < w.ke) {
+              stage(w, g + 1);
+            } else {
+              have_n = wi.next(wn);
+              if (have_n) stage(wn, wn.kb >> 2);
+            }
+          }
+          if (!__all_sync(0xFFFFFFFFu,
+                          wait_phase<false>(bar_empty + 8 * st, ph ^ 1u, wc, 0x09 | (st << 8)))) {
+            ok = false;
+            break;
+          }
+          const int t = ks & 3;
+          const uint32_t sSA = base + C::OFF_SFA + st * C::SFA_BYTES + 16 * lane;
+          const uint32_t sSB = base + C::OFF_SFB + st * C::SFB_BYTES + 16 * lane;
+          st_shared_v4(sSA, pick(ca[0], t), pick(ca[1], t), pick(ca[2], t), pick(ca[3], t));
+          st_shared_v4(sSB, pick(cb[0], t), pick(cb[1], t), pick(cb[2], t), pick(cb[3], t));
+          st_shared_v4(sSB + 512, pick(cb[4], t), pick(cb[5], t), pick(cb[6], t), pick(cb[7], t));
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bar_full + 8 * st);
+          if (++st == C::STAGES) {
+            st = 0;
+            ph ^= 1u;
+          }
+        }
+        w = wn;
+        have = have_n;
+      }
+      // after a failed wait: a staging load still in flight lands before
+      // the CTA may finish
+      if (staged) {
+        WaitCtl wf = wc;
+        wf.abort_flag = reinterpret_cast<volatile int *>(sm + C::OFF_MISC + 12);  // never raised
+        if (lane == 0) *wf.abort_flag = 0;
+        __syncwarp();
+        __all_sync(0xFFFFFFFFu, wait_phase<false>(bar_stg, sph, wf, 0x0B));
+      }
+    }
   } else {
     // ------------------------------------------------------------ epilogue
     const int ew = warp - 2;  // 0..7
@@ -926,7 +1131,7 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
       const bool row_ok = mt * (128 * CG) + 128 * (int)rank + 32 * q + lane < p.M;
       if (w.kind == kPartial) {
         // first part of a split tile: the FP32 partial to this CTA's slot,
-        // then count this warp in the slot's flag.  The slot is laid out by
+        // then this warp's flag slot set to the launch's epoch.  The slot is laid out by
         // (warp, 4-column group, lane) -- the reader uses the same warp/lane
         // to row mapping -- so every warp access covers 512 contiguous bytes.
         // Rows beyond M are neither written nor read.
@@ -941,16 +1146,16 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
         }
         __threadfence();
         __syncwarp();
-        if (lane == 0) atomicAdd(p.flags + unit * CG + (int)rank, 1);
+        if (lane == 0) atomicExch(p.flags + (unit * CG + (int)rank) * C::EPI_WARPS + ew, p.epoch);
         continue;
       }
       if (w.kind == kOwner) {
         // last part: add the partials of the CTAs that computed the earlier parts
         bool got = true;
         for (int c = w.first_contrib; c < unit && got; ++c) {
-          const int *flag = p.flags + c * CG + (int)rank;
-          const bool ready =
-              __all_sync(0xFFFFFFFFu, wait_flag(flag, C::EPI_WARPS, wc, 0x06 | ((t & 0xFFFF) << 16)));
+          // all eight epilogue warps of contributor c have written
+          const bool ready = wait_flags(p.flags + (c * CG + (int)rank) * C::EPI_WARPS, C::EPI_WARPS,
+                                        p.epoch, wc, 0x06 | ((t & 0xFFFF) << 16));
           if (!ready) {
             got = false;
             break;

@@ -10,7 +10,8 @@ namespace mxg {
 
 // ---------------------------------------------------------------- prepasses
 
-// Scale repack: row-major scales S[rows][kb_count] -> 512-byte chunks.  Chunk
+// Scale repack (CTA-pair tiles; single CTAs build the same chunks in the
+// kernel): row-major scales S[rows][kb_count] -> 512-byte chunks.  Chunk
 // g = (tile * k_steps + ks) * atoms + a covers rows (tile*atoms + a)*128 + r,
 // r in [0,128), and K-blocks ks*4 + j, j in [0,4); its byte
 // (r % 32) * 16 + (r / 32) * 4 + j holds that scale (127 = 1.0 where the row
@@ -36,10 +37,7 @@ struct RepackArgs {
 constexpr int kRepackThreads = 512;
 
 __global__ void __launch_bounds__(kRepackThreads)
-    repack_scales_kernel(RepackArgs a0, RepackArgs a1, int blocks0, int *flags, int nflags) {
-  // the GEMM's stream-K flags start every launch at zero
-  if (blockIdx.x == 0)
-    for (int i = threadIdx.x; i < nflags; i += kRepackThreads) flags[i] = 0;
+    repack_scales_kernel(RepackArgs a0, RepackArgs a1, int blocks0) {
   __shared__ __align__(16) uint32_t tile[128 * 16];  // 128 rows x 64 bytes
   const bool second = static_cast<int>(blockIdx.x) >= blocks0;
   const RepackArgs a = second ? a1 : a0;

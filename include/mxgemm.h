@@ -122,7 +122,8 @@ typedef enum {
 
 /* Create a handle bound to CUDA device `device`.  Fails with
  * MXGEMM_ERR_UNSUPPORTED_DEVICE unless the device is compute capability 10.3
- * (sm_103, GB300).  Allocates the handle's device status word. */
+ * (sm_103, GB300).  Allocates the handle's device status word and its
+ * partial-sum flag slots. */
 int mxgemm_create(mxgemm_handle_t *out, int device);
 
 /* Enqueue C (+)= A.B on `stream` (NULL = the legacy default stream).
@@ -235,13 +236,12 @@ int mxgemm_destroy(mxgemm_handle_t h);
  * cudaFree or allocating library call) and runs on the current device and
  * the given stream.  The paper has no counterpart to this entry point.
  *
- * Scratch: the repacked scales (and B re-pitched to a 16-byte row pitch when
- * N % 16 != 0) go to one file-scope device array of 16 MiB, which every GPU
- * that loads this library holds until the process exits.  A problem needs
- *   ceil(M/128)*ceil(K/128)*512 rounded up to 1 KiB
- *   + ceil(N/256)*ceil(K/128)*1024 rounded up to 1 KiB
- *   + (N % 16 ? K * round_up(N, 16) : 0)  bytes;
- * more than 16 MiB is rejected with MXGEMM_ERR_TOO_LARGE before anything is
+ * Scratch: B re-pitched to a 16-byte row pitch when N % 16 != 0 goes to one
+ * file-scope device array of 16 MiB, which every GPU that loads this library
+ * holds until the process exits (the single-CTA kernel reads the scales in
+ * their row-major layout and needs no other scratch).  A problem with
+ * N % 16 != 0 needs K * round_up(N, 16) bytes rounded up to 1 KiB; more than
+ * 16 MiB is rejected with MXGEMM_ERR_TOO_LARGE before anything is
  * enqueued.  All calls share that array and it keeps the last call's
  * contents, so calls whose work overlaps on the GPU (different streams, or
  * different host threads) race and must be serialised by the caller.

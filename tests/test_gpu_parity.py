@@ -375,3 +375,32 @@ def test_plan_cache_churn_and_workspace_growth(h):
         ref, bound = oracle.rows(p.A, p.As, p.B, p.Bs)
         res = oracle.accept(gu.to_numpy_out(C, p.out_dtype), ref, bound, p.out_dtype)
         assert res["ok"], f"{p.name}: {res}"
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("K", [1024, 384, 160])
+def test_scales_at_unaligned_addresses(h, mode, K):
+    # A_scale and B_scale one byte past a 16-byte boundary: the scale chunks
+    # are built from byte loads instead of 16-byte ones (single CTAs in the
+    # kernel, pairs in the repack); the result is the same, bit for bit
+    _mode(h, mode)
+    p = mi.random_problem(300, 520, K, seed=K + mode, kind="normal")
+    ref_c = gu.run_gpu(h, p).cpu()
+    dev = gu.DEV
+
+    def unaligned(t):
+        buf = torch.empty(t.numel() + 16, dtype=torch.uint8, device=dev)
+        v = buf[1:1 + t.numel()].view(t.shape)
+        v.copy_(t.to(dev))
+        assert v.data_ptr() % 16 == 1
+        return v
+
+    A, B = p.A.to(dev), p.B.to(dev)
+    As, Bs = unaligned(p.As), unaligned(p.Bs)
+    C = torch.full((p.M, p.N), float("nan"), dtype=torch.float32, device=dev)
+    mx.mxgemm_run(h, p.M, p.N, K, A, As, B, Bs, C, 0, mx.OUT_F32)
+    torch.cuda.synchronize()
+    assert mx.mxgemm_get_device_status(h)[0] == 0
+    assert torch.equal(C.cpu().view(torch.int32), ref_c.view(torch.int32))
+    ref, bound = oracle.rows(p.A, p.As, p.B, p.Bs)
+    assert oracle.accept(C.cpu().numpy(), ref, bound, "f32")["ok"]

@@ -73,8 +73,9 @@ def test_noalloc_rejects_problems_beyond_its_scratch():
         pytest.skip("no CUDA device")
     small = torch.zeros(1024, dtype=torch.uint8, device=gu.DEV)
     C = torch.zeros(16, dtype=torch.float32, device=gu.DEV)
-    # scales alone: (16384/128 * 512 + 16384/256 * 1024) * 32768/128 bytes = 32 MiB > 16 MiB
-    st = mx.mxgemm_run_noalloc(16384, 16384, 32768, small, small, small, small, C, 0, mx.OUT_F32,
+    # B re-pitched for N % 16 != 0: K * round_up(N, 16) = 2048 * 16384 bytes = 32 MiB > 16 MiB
+    # (rejected before anything is read or enqueued)
+    st = mx.mxgemm_run_noalloc(256, 16383, 2048, small, small, small, small, C, 0, mx.OUT_F32,
                                None, check=False)
     assert st == mx.ERR_TOO_LARGE
     assert "scratch" in mx.mxgemm_status_string(st)
