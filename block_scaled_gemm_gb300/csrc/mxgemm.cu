@@ -1009,10 +1009,11 @@ extern "C" int mxgemm_run_host(mxgemm_handle_t h, int64_t M, int64_t N, int64_t 
 // Callers that cannot allocate device memory where they call the GEMM (a
 // plug-in whose host framework owns all device memory, code that must not
 // allocate after start-up, a stream that is being captured) use this entry
-// point.  Its scratch (the repacked scales, and B re-pitched when N % 16 != 0)
-// lives in the file-scope array below, which the CUDA runtime places when it
-// loads this library's device code: every GPU that loads the library holds
-// these kNoAllocScratchBytes until the process exits.
+// point.  The kernel builds the scale chunks itself (fused scales), so its
+// only scratch is B re-pitched when N % 16 != 0.  That lives in the
+// file-scope array below, which the CUDA runtime places when it loads this
+// library's device code: every GPU that loads the library holds these
+// kNoAllocScratchBytes until the process exits.
 // ===========================================================================
 
 namespace {

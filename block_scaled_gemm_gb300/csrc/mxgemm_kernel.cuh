@@ -16,10 +16,12 @@
 //   warps 2..9  epilogue: wait acc_full, tcgen05.ld the whole accumulator into
 //               registers, release it (acc_empty) so the next tile's MMAs
 //               start, then (optionally + C_in) round to FP32/BF16 and store.
-//   warp 10     (single CTAs) scale loader: builds each stage's A and B scale
-//               chunks in shared memory straight from the row-major A_scale
-//               and B_scale, so no prepass runs before the kernel; pairs
-//               load chunks that a prepass repacked.
+//   warp 10     (single CTAs) scale loader: when the launch asks for it
+//               (fused_scales: one row of tiles, M <= 128), builds each
+//               stage's A and B scale chunks in shared memory straight from
+//               the row-major A_scale and B_scale, so no prepass runs before
+//               the kernel; otherwise (and always for pairs) the producer
+//               loads chunks that a prepass repacked.
 //
 // Pair mode (CG = 2, cluster of 2 CTAs, tcgen05 cta_group::2): the pair
 // computes a 256 x 256 tile; each CTA loads its own 128 rows of A and its own
@@ -498,7 +500,7 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   // The set-up above overlaps the tail of the prepass before the kernel, if
-  // any (the scale repack for pairs, the B re-pitch; programmatic dependent
+  // any (the scale repack, the B re-pitch; programmatic dependent
   // launch); nothing below reads or writes global memory before that grid
   // has finished.
   griddep_wait();
