@@ -433,7 +433,12 @@ def run_mx(args, world, rank, local):
     tdt = torch.float32 if prob.out_dtype == "f32" else torch.bfloat16
     flops = 2.0 * M * N * K
 
-    A, As, B, Bs = (t.to(dev) for t in (prob.A, prob.As, prob.B, prob.Bs))
+    # scales as the run takes them: row-major (the default), or already in
+    # the packed order the tensor cores read (no repack prepass)
+    packed = args.scale_layout == "packed"
+    sA = mx_inputs.pack_scales(prob.As) if packed else prob.As
+    sB = mx_inputs.pack_scales(prob.Bs, along_cols=True) if packed else prob.Bs
+    A, As, B, Bs = (t.to(dev) for t in (prob.A, sA, prob.B, sB))
     C = torch.empty((M, N), dtype=tdt, device=dev)
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 126 << 20)
@@ -445,6 +450,8 @@ def run_mx(args, world, rank, local):
         mx.mxgemm_set_option(h, mx.OPT_MODE, args.mode)
     mx.mxgemm_set_option(h, mx.OPT_A_FORMAT, FORMATS.index(args.a_format))
     mx.mxgemm_set_option(h, mx.OPT_B_FORMAT, FORMATS.index(args.b_format))
+    if packed:
+        mx.mxgemm_set_option(h, mx.OPT_SCALE_LAYOUT, mx.SCALES_PACKED)
 
     def step():
         if flush is not None:
@@ -527,7 +534,7 @@ def run_mx(args, world, rank, local):
 
     # end to end through the C interface: pinned host operands in, C out
     e2e_steps = max(1, min(args.steps, args.e2e_steps))
-    hA, hAs, hB, hBs = (t.contiguous().pin_memory() for t in (prob.A, prob.As, prob.B, prob.Bs))
+    hA, hAs, hB, hBs = (t.contiguous().pin_memory() for t in (prob.A, sA, prob.B, sB))
     hC = torch.empty((M, N), dtype=tdt).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in (hA, hAs, hB, hBs))
     d2h = hC.numel() * hC.element_size()
@@ -587,7 +594,8 @@ def run_mx(args, world, rank, local):
                               if flush is not None else "not flushed"),
                        "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
                        "tile_mode": args.mode if args.mode is not None else "auto",
-                       "a_format": args.a_format, "b_format": args.b_format},
+                       "a_format": args.a_format, "b_format": args.b_format,
+                       "scale_layout": args.scale_layout},
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
@@ -623,6 +631,9 @@ def main(argv=None):
                     help="quantizer rounding: nearest even, or stochastic with one random word per value")
     ap.add_argument("--a-format", default="e4m3", choices=FORMATS)
     ap.add_argument("--b-format", default="e4m3", choices=FORMATS)
+    ap.add_argument("--scale-layout", default="row-major", choices=["row-major", "packed"],
+                    help="scales row-major (the workload's form; the run repacks them) or "
+                         "pre-packed in the tensor cores' order (as mxgemm_quantize_ex writes them)")
     ap.add_argument("--no-flush", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle baseline and spot parity")
     ap.add_argument("--e2e-steps", type=int, default=20)

@@ -27,7 +27,8 @@ __all__ = [
     "FMT_E2M3", "FMT_E3M2", "FMT_E2M1", "MxgemmError", "library", "library_path", "mxgemm_create", "mxgemm_run",
     "mxgemm_destroy", "mxgemm_set_option", "mxgemm_get_device_status", "mxgemm_status_string",
     "mxgemm_set_profile_events", "mxgemm_get_launch_count", "mxgemm_run_noalloc", "mxgemm_run_host",
-    "mxgemm_quantize", "IN_F32", "IN_BF16", "EXPORTED_SYMBOLS", "Gemm",
+    "mxgemm_quantize", "IN_F32", "IN_BF16", "EXPORTED_SYMBOLS", "Gemm", "OPT_SCALE_LAYOUT",
+    "SCALES_ROW_MAJOR", "SCALES_PACKED", "mxgemm_scale_bytes",
 ]
 
 OUT_F32 = 0
@@ -40,6 +41,11 @@ OPT_SCHEDULER = 4
 OPT_STREAM_K = 5
 OPT_A_FORMAT = 6
 OPT_B_FORMAT = 7
+OPT_SCALE_LAYOUT = 8
+
+# scale layouts (mxgemm_scale_layout_t)
+SCALES_ROW_MAJOR = 0
+SCALES_PACKED = 1
 
 # element formats (mxgemm_format_t); one element per byte, sub-byte codes in
 # the low bits
@@ -62,7 +68,7 @@ EXPORTED_SYMBOLS = (
     "mxgemm_create", "mxgemm_run", "mxgemm_destroy", "mxgemm_set_option",
     "mxgemm_get_device_status", "mxgemm_status_string", "mxgemm_set_profile_events",
     "mxgemm_get_launch_count", "mxgemm_run_noalloc", "mxgemm_run_host", "mxgemm_quantize",
-    "mxgemm_quantize_sr",
+    "mxgemm_quantize_sr", "mxgemm_quantize_ex", "mxgemm_scale_bytes",
 )
 
 _lib = None
@@ -107,6 +113,10 @@ def library():
         lib.mxgemm_quantize.restype = i32
         lib.mxgemm_quantize_sr.argtypes = [vp, i32, i64, i64, i32, vp, vp, vp, vp]
         lib.mxgemm_quantize_sr.restype = i32
+        lib.mxgemm_quantize_ex.argtypes = [vp, i32, i64, i64, i32, vp, i32, vp, vp, vp]
+        lib.mxgemm_quantize_ex.restype = i32
+        lib.mxgemm_scale_bytes.argtypes = [i64, i64, i32, i32, ctypes.POINTER(i64)]
+        lib.mxgemm_scale_bytes.restype = i32
         lib.mxgemm_run_host.argtypes = [vp, i64, i64, i64, vp, vp, vp, vp, vp, i32, i32, vp]
         lib.mxgemm_run_host.restype = i32
         lib.mxgemm_run_noalloc.argtypes = [i64, i64, i64, vp, vp, vp, vp, vp, i32, i32, vp]
@@ -163,28 +173,44 @@ IN_BF16 = 1
 
 
 def mxgemm_quantize(X, R, C, codes, scales, along_cols=False, x_dtype=None, stream=None,
-                    check: bool = True, rand_bits=None) -> int:
+                    check: bool = True, rand_bits=None, scale_layout=SCALES_ROW_MAJOR) -> int:
     """MX-quantize the R x C device matrix X (float32 or bfloat16) into E4M3
     codes (R x C bytes) and E8M0 scales per 32 values, along the rows
-    (scales R x C/32) or down the columns (scales C x R/32).  With rand_bits
-    (an R x C device tensor of 32-bit words) the codes round stochastically
-    (mxgemm_quantize_sr), else to nearest even."""
+    (A_scale of an M x K X) or down the columns (B_scale of a K x N X).
+    With rand_bits (an R x C device tensor of 32-bit words) the codes round
+    stochastically, else to nearest even.  scale_layout SCALES_ROW_MAJOR
+    gives R x C/32 (rows) or C x R/32 (columns) scales, SCALES_PACKED the
+    order a run with OPT_SCALE_LAYOUT = SCALES_PACKED reads
+    (mxgemm_scale_bytes bytes)."""
     if x_dtype is None:
         import torch
         x_dtype = IN_BF16 if getattr(X, "dtype", None) == torch.bfloat16 else IN_F32
-    if rand_bits is None:
-        st = library().mxgemm_quantize(_ptr(X), int(x_dtype), int(R), int(C),
-                                       int(bool(along_cols)), _ptr(codes), _ptr(scales),
-                                       _stream(stream))
+    lib = library()
+    if rand_bits is None and scale_layout == SCALES_ROW_MAJOR:
+        st = lib.mxgemm_quantize(_ptr(X), int(x_dtype), int(R), int(C), int(bool(along_cols)),
+                                 _ptr(codes), _ptr(scales), _stream(stream))
         name = "mxgemm_quantize"
-    else:
-        st = library().mxgemm_quantize_sr(_ptr(X), int(x_dtype), int(R), int(C),
-                                          int(bool(along_cols)), _ptr(rand_bits), _ptr(codes),
-                                          _ptr(scales), _stream(stream))
+    elif scale_layout == SCALES_ROW_MAJOR:
+        st = lib.mxgemm_quantize_sr(_ptr(X), int(x_dtype), int(R), int(C), int(bool(along_cols)),
+                                    _ptr(rand_bits), _ptr(codes), _ptr(scales), _stream(stream))
         name = "mxgemm_quantize_sr"
+    else:
+        st = lib.mxgemm_quantize_ex(_ptr(X), int(x_dtype), int(R), int(C), int(bool(along_cols)),
+                                    _ptr(rand_bits), int(scale_layout), _ptr(codes), _ptr(scales),
+                                    _stream(stream))
+        name = "mxgemm_quantize_ex"
     if check:
         _check(st, name)
     return st
+
+
+def mxgemm_scale_bytes(R, C, along_cols=False, scale_layout=SCALES_ROW_MAJOR) -> int:
+    """Bytes of the scales of an R x C matrix quantized along the rows or
+    down the columns, in the given layout."""
+    out = ctypes.c_int64(0)
+    _check(library().mxgemm_scale_bytes(int(R), int(C), int(bool(along_cols)), int(scale_layout),
+                                        ctypes.byref(out)), "mxgemm_scale_bytes")
+    return int(out.value)
 
 
 def mxgemm_run_host(h, M, N, K, A, A_scale, B, B_scale, C, use_acc=0, out_dtype=OUT_F32,

@@ -40,7 +40,7 @@ struct Plan {
   int64_t M = 0, N = 0, K = 0;
   const void *A = nullptr, *As = nullptr, *B = nullptr, *Bs = nullptr;
   void *C = nullptr;
-  int use_acc = 0, out_dtype = 0, mode = 0, stall = 0, sched = 0, sk = 0, fmts = 0;
+  int use_acc = 0, out_dtype = 0, mode = 0, stall = 0, sched = 0, sk = 0, fmts = 0, layout = 0;
   long long timeout_ns = 0;
   uint8_t *ws = nullptr;
   // value
@@ -58,10 +58,11 @@ struct Plan {
 
   bool matches(int64_t M_, int64_t N_, int64_t K_, const void *A_, const void *As_, const void *B_,
                const void *Bs_, void *C_, int ua, int od, int md, int sl, int sc, int sk_,
-               long long to, uint8_t *w, int fm) const {
+               long long to, uint8_t *w, int fm, int lay) const {
     return valid && M == M_ && N == N_ && K == K_ && A == A_ && As == As_ && B == B_ &&
            Bs == Bs_ && C == C_ && use_acc == ua && out_dtype == od && mode == md &&
-           stall == sl && sched == sc && sk == sk_ && timeout_ns == to && ws == w && fmts == fm;
+           stall == sl && sched == sc && sk == sk_ && timeout_ns == to && ws == w && fmts == fm &&
+           layout == lay;
   }
 };
 
@@ -99,6 +100,7 @@ struct mxgemm_ctx {
   int scheduler = 0;
   int stream_k = 1;
   int a_fmt = 0, b_fmt = 0;  // element formats (mxgemm_format_t)
+  int scale_layout = MXGEMM_SCALES_ROW_MAJOR;
   bool attr_set[3][8] = {};
   cudaEvent_t prof_before = nullptr;
   cudaEvent_t prof_after = nullptr;
@@ -343,19 +345,25 @@ int build_plan(mxgemm_ctx *h, Plan *pl, int64_t M, int64_t N, int64_t K, const v
                const void *A_scale, const void *B, const void *B_scale, void *C, int use_acc,
                int out_dtype, int CG, int64_t m_tiles, int64_t n_tiles, int64_t k_steps,
                int64_t num_tiles, int64_t a_chunks, int64_t b_chunks, bool pad_b, int64_t npad,
-               const Split &sp, const Sizes &z, int a_bits, int b_bits, bool fused) {
+               const Split &sp, const Sizes &z, int a_bits, int b_bits, bool fused, bool packed) {
   const size_t off_sfb = z.off_sfb, off_b = z.off_b;
   const size_t esz = out_dtype == MXGEMM_OUT_F32 ? 4 : 2;
   const int64_t kb = K / 32;
-  uint8_t *sfa = h->ws.ptr;
-  uint8_t *sfb = h->ws.ptr + off_sfb;
+  // scale chunks: repacked into the workspace, or the caller's packed scales
+  const uint8_t *sfa = packed ? static_cast<const uint8_t *>(A_scale) : h->ws.ptr;
+  const uint8_t *sfb = packed ? static_cast<const uint8_t *>(B_scale) : h->ws.ptr + off_sfb;
+  if (packed) {
+    a_chunks = cdiv(M, 128) * k_steps;  // the packed area (a pair's second block may lie past it)
+    b_chunks = n_tiles * k_steps * 2;
+  }
   const void *bsrc = pad_b ? static_cast<const void *>(h->ws.ptr + off_b) : B;
   const int64_t bpitch = pad_b ? npad : N;
   const void *asrc = a_bits < 8 ? static_cast<const void *>(h->ws.ptr + z.off_a) : A;
-  pl->ra = mxg::RepackArgs{static_cast<const uint8_t *>(A_scale), reinterpret_cast<uint32_t *>(sfa),
+  pl->ra = mxg::RepackArgs{static_cast<const uint8_t *>(A_scale), reinterpret_cast<uint32_t *>(h->ws.ptr),
                            M, static_cast<int>(kb), static_cast<int>(k_steps), 1,
                            static_cast<int>(m_tiles * CG), static_cast<int>(cdiv(k_steps, 16))};
-  pl->rb = mxg::RepackArgs{static_cast<const uint8_t *>(B_scale), reinterpret_cast<uint32_t *>(sfb),
+  pl->rb = mxg::RepackArgs{static_cast<const uint8_t *>(B_scale),
+                           reinterpret_cast<uint32_t *>(h->ws.ptr + off_sfb),
                            N, static_cast<int>(kb), static_cast<int>(k_steps), 2,
                            static_cast<int>(n_tiles * 2), static_cast<int>(cdiv(k_steps, 16))};
   pl->blocks_a = pl->ra.row_blocks * pl->ra.kgroups;
@@ -374,11 +382,11 @@ int build_plan(mxgemm_ctx *h, Plan *pl, int64_t M, int64_t N, int64_t K, const v
   // are multiples of 16 bytes.
   std::memset(&pl->tSA, 0, sizeof(pl->tSA));
   std::memset(&pl->tSB, 0, sizeof(pl->tSB));
-  pl->repack = !fused;
+  pl->repack = !fused && !packed;
   const bool scale_tma = fused && kb % 16 == 0 &&
                          reinterpret_cast<uintptr_t>(A_scale) % 16 == 0 &&
                          reinterpret_cast<uintptr_t>(B_scale) % 16 == 0;
-  if (pl->repack &&
+  if (!fused &&
       (encode_2d(h, &pl->tSA, u8, sfa, 128, a_chunks * 4, 128, 128, 4, CU_TENSOR_MAP_SWIZZLE_NONE) ||
        encode_2d(h, &pl->tSB, u8, sfb, 128, b_chunks * 4, 128, 128, 8, CU_TENSOR_MAP_SWIZZLE_NONE)))
     return MXGEMM_ERR_CUDA;
@@ -441,6 +449,7 @@ int build_plan(mxgemm_ctx *h, Plan *pl, int64_t M, int64_t N, int64_t K, const v
   pl->stall = h->stall_producer; pl->sched = h->scheduler; pl->sk = h->stream_k;
   pl->timeout_ns = h->timeout_ns;
   pl->fmts = h->a_fmt * 8 + h->b_fmt;
+  pl->layout = packed ? MXGEMM_SCALES_PACKED : MXGEMM_SCALES_ROW_MAJOR;
   pl->ws = h->ws.ptr;
   pl->valid = true;
   return MXGEMM_OK;
@@ -552,6 +561,11 @@ int mxgemm_set_option(mxgemm_handle_t h, int option, int64_t value) {
       if (value < MXGEMM_FMT_E4M3 || value > MXGEMM_FMT_E2M1) return MXGEMM_ERR_INVALID_VALUE;
       (option == MXGEMM_OPT_A_FORMAT ? h->a_fmt : h->b_fmt) = static_cast<int>(value);
       return MXGEMM_OK;
+    case MXGEMM_OPT_SCALE_LAYOUT:
+      if (value != MXGEMM_SCALES_ROW_MAJOR && value != MXGEMM_SCALES_PACKED)
+        return MXGEMM_ERR_INVALID_VALUE;
+      h->scale_layout = static_cast<int>(value);
+      return MXGEMM_OK;
     default:
       return MXGEMM_ERR_INVALID_VALUE;
   }
@@ -602,9 +616,14 @@ int mxgemm_run(mxgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A
   // 512-byte chunks.  On full tiles the in-kernel build measured slower: its
   // 16-byte row segments cost TMA and shared-memory transactions that the
   // mainloop needs (1-CTA square 4096: 64.1 us against 58.0 with the prepass).
-  const bool fused = CG == 1 && M <= 128;
-  const int64_t a_chunks = fused ? 0 : m_tiles * CG * k_steps;
-  const int64_t b_chunks = fused ? 0 : n_tiles * k_steps * 2;  // 2 per 256 columns
+  // Caller-packed scales (MXGEMM_OPT_SCALE_LAYOUT) are loaded as they are:
+  // neither a prepass nor the scale loader.
+  const bool packed = h->scale_layout == MXGEMM_SCALES_PACKED;
+  if (packed && (reinterpret_cast<uintptr_t>(A_scale) % 16 || reinterpret_cast<uintptr_t>(B_scale) % 16))
+    return MXGEMM_ERR_MISALIGNED;
+  const bool fused = !packed && CG == 1 && M <= 128;
+  const int64_t a_chunks = fused || packed ? 0 : m_tiles * CG * k_steps;
+  const int64_t b_chunks = fused || packed ? 0 : n_tiles * k_steps * 2;  // 2 per 256 columns
   // 6- and 4-bit formats are packed 16 elements per 16-byte group first
   const int a_bits = h->a_fmt == MXGEMM_FMT_E2M1 ? 4 : h->a_fmt >= MXGEMM_FMT_E2M3 ? 6 : 8;
   const int b_bits = h->b_fmt == MXGEMM_FMT_E2M1 ? 4 : h->b_fmt >= MXGEMM_FMT_E2M3 ? 6 : 8;
@@ -625,7 +644,7 @@ int mxgemm_run(mxgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A
   for (Plan &pl : h->plans)
     if (pl.matches(M, N, K, A, A_scale, B, B_scale, C, use_acc, out_dtype, h->mode,
                    h->stall_producer, h->scheduler, h->stream_k, h->timeout_ns, h->ws.ptr,
-                   h->a_fmt * 8 + h->b_fmt) &&
+                   h->a_fmt * 8 + h->b_fmt, h->scale_layout) &&
         h->ws.bytes >= ws_bytes) {
       plan = &pl;
       break;
@@ -641,7 +660,7 @@ int mxgemm_run(mxgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A
     plan->valid = false;
     st = build_plan(h, plan, M, N, K, A, A_scale, B, B_scale, C, use_acc, out_dtype, CG, m_tiles,
                     n_tiles, k_steps, num_tiles, a_chunks, b_chunks, pad_b, npad, sp, z, a_bits,
-                    b_bits, fused);
+                    b_bits, fused, packed);
     if (st != MXGEMM_OK) return st;
   }
 
@@ -730,7 +749,7 @@ namespace {
 
 template <typename T, bool SR>
 void launch_quantize(const T *x, int64_t R, int64_t C, int along_cols, const uint32_t *rbits,
-                     uint8_t *cd, uint8_t *sc, int sms, cudaStream_t stream) {
+                     uint8_t *cd, uint8_t *sc, int64_t S, int sms, cudaStream_t stream) {
   // grid: a few resident blocks per SM, grid-stride loops over the work
   const int threads = 256;
   if (!along_cols) {
@@ -738,7 +757,8 @@ void launch_quantize(const T *x, int64_t R, int64_t C, int along_cols, const uin
     const int64_t warps_needed = (nblocks + 7) / 8;  // a warp takes 8 blocks
     int grid = static_cast<int>(std::min<int64_t>(cdiv(warps_needed, threads / 32), int64_t(sms) * 8));
     if (grid < 1) grid = 1;
-    mxg::mx_quantize_rows_kernel<T, SR><<<grid, threads, 0, stream>>>(x, nblocks, rbits, cd, sc);
+    mxg::mx_quantize_rows_kernel<T, SR><<<grid, threads, 0, stream>>>(x, nblocks, rbits, cd, sc,
+                                                                      C / 32, S);
   } else {
     // two adjacent columns per thread when C is even (wider loads and
     // stores); one with stochastic rounding, whose random words take as many
@@ -751,25 +771,39 @@ void launch_quantize(const T *x, int64_t R, int64_t C, int along_cols, const uin
     if (grid < 1) grid = 1;
     if constexpr (kPairsOk) {
       if (pairs) {
-        mxg::mx_quantize_cols_kernel<T, 2, SR><<<grid, threads, 0, stream>>>(x, R, C, rbits, cd, sc);
+        mxg::mx_quantize_cols_kernel<T, 2, SR><<<grid, threads, 0, stream>>>(x, R, C, rbits, cd, sc, S);
         return;
       }
     }
-    mxg::mx_quantize_cols_kernel<T, 1, SR><<<grid, threads, 0, stream>>>(x, R, C, rbits, cd, sc);
+    mxg::mx_quantize_cols_kernel<T, 1, SR><<<grid, threads, 0, stream>>>(x, R, C, rbits, cd, sc, S);
   }
 }
 
+// Bytes of the scales of an R x C matrix quantized along the rows (A: M = R,
+// K = C) or down the columns (B: K = R, N = C), in the given layout; -1 for
+// an invalid layout.
+int64_t scale_bytes(int64_t R, int64_t C, int along_cols, int layout) {
+  if (layout == MXGEMM_SCALES_ROW_MAJOR) return along_cols ? C * (R / 32) : R * (C / 32);
+  if (layout != MXGEMM_SCALES_PACKED) return -1;
+  const int64_t K = along_cols ? R : C, S = cdiv(K, 128);
+  return along_cols ? cdiv(C, 256) * S * 1024 : cdiv(R, 128) * S * 512;
+}
+
 int quantize_impl(const void *X, int x_dtype, int64_t R, int64_t C, int along_cols,
-                  const void *rand_bits, bool sr, void *codes, void *scales, mxgemm_stream_t stream_) {
+                  const void *rand_bits, bool sr, int layout, void *codes, void *scales,
+                  mxgemm_stream_t stream_) {
   const int64_t lim = int64_t(1) << 31;
   if (R < 0 || C < 0 || R >= lim || C >= lim) return MXGEMM_ERR_INVALID_VALUE;
+  if (layout != MXGEMM_SCALES_ROW_MAJOR && layout != MXGEMM_SCALES_PACKED)
+    return MXGEMM_ERR_INVALID_VALUE;
+  const bool packed = layout == MXGEMM_SCALES_PACKED;
   if (x_dtype != MXGEMM_IN_F32 && x_dtype != MXGEMM_IN_BF16) return MXGEMM_ERR_INVALID_VALUE;
   if (along_cols != 0 && along_cols != 1) return MXGEMM_ERR_INVALID_VALUE;
   if ((along_cols ? R % 32 : C % 32) != 0) return MXGEMM_ERR_INVALID_VALUE;
   if (R == 0 || C == 0) return MXGEMM_OK;
   if (!X || !codes || !scales || (sr && !rand_bits)) return MXGEMM_ERR_INVALID_VALUE;
   if (reinterpret_cast<uintptr_t>(X) % 16 || reinterpret_cast<uintptr_t>(codes) % 16 ||
-      reinterpret_cast<uintptr_t>(rand_bits) % 16)
+      reinterpret_cast<uintptr_t>(rand_bits) % 16 || (packed && reinterpret_cast<uintptr_t>(scales) % 16))
     return MXGEMM_ERR_MISALIGNED;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) {
@@ -787,14 +821,22 @@ int quantize_impl(const void *X, int x_dtype, int64_t R, int64_t C, int along_co
   cudaStream_t stream = static_cast<cudaStream_t>(stream_);
   uint8_t *cd = static_cast<uint8_t *>(codes), *sc = static_cast<uint8_t *>(scales);
   const uint32_t *rb = static_cast<const uint32_t *>(rand_bits);
+  // packed: the padding entries (rows or columns past the matrix, K blocks
+  // past the last) hold 127, the kernel then writes every real scale
+  const int64_t S = packed ? cdiv(along_cols ? R : C, 128) : 0;
+  if (packed && cudaMemsetAsync(sc, 127, static_cast<size_t>(scale_bytes(R, C, along_cols, layout)),
+                                stream) != cudaSuccess) {
+    cudaGetLastError();
+    return MXGEMM_ERR_CUDA;
+  }
   if (x_dtype == MXGEMM_IN_F32) {
     const float *x = static_cast<const float *>(X);
-    if (sr) launch_quantize<float, true>(x, R, C, along_cols, rb, cd, sc, sms, stream);
-    else launch_quantize<float, false>(x, R, C, along_cols, nullptr, cd, sc, sms, stream);
+    if (sr) launch_quantize<float, true>(x, R, C, along_cols, rb, cd, sc, S, sms, stream);
+    else launch_quantize<float, false>(x, R, C, along_cols, nullptr, cd, sc, S, sms, stream);
   } else {
     const __nv_bfloat16 *x = static_cast<const __nv_bfloat16 *>(X);
-    if (sr) launch_quantize<__nv_bfloat16, true>(x, R, C, along_cols, rb, cd, sc, sms, stream);
-    else launch_quantize<__nv_bfloat16, false>(x, R, C, along_cols, nullptr, cd, sc, sms, stream);
+    if (sr) launch_quantize<__nv_bfloat16, true>(x, R, C, along_cols, rb, cd, sc, S, sms, stream);
+    else launch_quantize<__nv_bfloat16, false>(x, R, C, along_cols, nullptr, cd, sc, S, sms, stream);
   }
   if (cudaGetLastError() != cudaSuccess) return MXGEMM_ERR_CUDA;
   return MXGEMM_OK;
@@ -804,13 +846,32 @@ int quantize_impl(const void *X, int x_dtype, int64_t R, int64_t C, int along_co
 
 extern "C" int mxgemm_quantize(const void *X, int x_dtype, int64_t R, int64_t C, int along_cols,
                                void *codes, void *scales, mxgemm_stream_t stream) {
-  return quantize_impl(X, x_dtype, R, C, along_cols, nullptr, false, codes, scales, stream);
+  return quantize_impl(X, x_dtype, R, C, along_cols, nullptr, false, MXGEMM_SCALES_ROW_MAJOR, codes,
+                       scales, stream);
 }
 
 extern "C" int mxgemm_quantize_sr(const void *X, int x_dtype, int64_t R, int64_t C,
                                   int along_cols, const void *rand_bits, void *codes,
                                   void *scales, mxgemm_stream_t stream) {
-  return quantize_impl(X, x_dtype, R, C, along_cols, rand_bits, true, codes, scales, stream);
+  return quantize_impl(X, x_dtype, R, C, along_cols, rand_bits, true, MXGEMM_SCALES_ROW_MAJOR, codes,
+                       scales, stream);
+}
+
+extern "C" int mxgemm_quantize_ex(const void *X, int x_dtype, int64_t R, int64_t C, int along_cols,
+                                  const void *rand_bits, int scale_layout, void *codes,
+                                  void *scales, mxgemm_stream_t stream) {
+  return quantize_impl(X, x_dtype, R, C, along_cols, rand_bits, rand_bits != nullptr, scale_layout,
+                       codes, scales, stream);
+}
+
+extern "C" int mxgemm_scale_bytes(int64_t R, int64_t C, int along_cols, int scale_layout,
+                                  int64_t *bytes_out) {
+  if (!bytes_out || R < 0 || C < 0 || (along_cols != 0 && along_cols != 1))
+    return MXGEMM_ERR_INVALID_VALUE;
+  const int64_t b = scale_bytes(R, C, along_cols, scale_layout);
+  if (b < 0) return MXGEMM_ERR_INVALID_VALUE;
+  *bytes_out = b;
+  return MXGEMM_OK;
 }
 
 // ===========================================================================
@@ -930,8 +991,16 @@ extern "C" int mxgemm_run_host(mxgemm_handle_t h, int64_t M, int64_t N, int64_t 
   if (ms < 256) ms = 256;
   if (ms > M) ms = M;
   const int64_t nslab = cdiv(M, ms);
-  const size_t b_bytes = static_cast<size_t>(K) * N, bs_bytes = static_cast<size_t>(N) * kb;
-  const size_t a_bytes = static_cast<size_t>(ms) * K, as_bytes = static_cast<size_t>(ms) * kb;
+  // scales: row-major, or packed (slabs are whole 128-row blocks: ms is a
+  // multiple of 256, and only the last slab may end short of one)
+  const bool packed = h->scale_layout == MXGEMM_SCALES_PACKED;
+  const int64_t S = cdiv(K, 128);
+  auto as_slab_bytes = [&](int64_t rows) -> size_t {
+    return packed ? static_cast<size_t>(cdiv(rows, 128) * S * 512) : static_cast<size_t>(rows) * kb;
+  };
+  const size_t b_bytes = static_cast<size_t>(K) * N;
+  const size_t bs_bytes = packed ? static_cast<size_t>(cdiv(N, 256) * S * 1024) : static_cast<size_t>(N) * kb;
+  const size_t a_bytes = static_cast<size_t>(ms) * K, as_bytes = as_slab_bytes(ms);
   const size_t c_bytes = static_cast<size_t>(ms) * N * esz;
   // staging: two B slots (consecutive calls alternate, so that one call's
   // B copy overlaps the previous call's last slabs), then two row slots
@@ -978,7 +1047,8 @@ extern "C" int mxgemm_run_host(mxgemm_handle_t h, int64_t M, int64_t N, int64_t 
     if (!wait_event(hp.h2d, hp.gemm_done[s]) || (use_acc && !wait_event(hp.h2d, hp.out_done[s])))
       return MXGEMM_ERR_CUDA;
     if (!copy_async(dA, hA + m0 * K, static_cast<size_t>(mj) * K, cudaMemcpyHostToDevice, hp.h2d) ||
-        !copy_async(dAs, hAs + m0 * kb, static_cast<size_t>(mj) * kb, cudaMemcpyHostToDevice, hp.h2d) ||
+        !copy_async(dAs, hAs + (packed ? (m0 / 128) * S * 512 : m0 * kb), as_slab_bytes(mj),
+                    cudaMemcpyHostToDevice, hp.h2d) ||
         (use_acc && !copy_async(dC, hC + m0 * crow, mj * crow, cudaMemcpyHostToDevice, hp.h2d)) ||
         !record_event(hp.in_ready[s], hp.h2d))
       return MXGEMM_ERR_CUDA;
@@ -1156,7 +1226,7 @@ extern "C" int mxgemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A
   Plan plan;
   st = build_plan(&ctx, &plan, M, N, K, A, A_scale, B, B_scale, C, use_acc, out_dtype, CG, m_tiles,
                   n_tiles, k_steps, num_tiles, a_chunks, b_chunks, pad_b, npad, sp, z, 8, 8,
-                  true);
+                  true, false);
   if (st != MXGEMM_OK) return st;
   // the status word must start each call at zero
   if (cudaMemsetAsync(nd->status, 0, 2 * sizeof(int), stream) != cudaSuccess) {

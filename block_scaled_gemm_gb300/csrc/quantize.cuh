@@ -91,6 +91,20 @@ __device__ __forceinline__ uint32_t mx_e4m3_sr(float y, uint32_t r) {
   return sign | (n + (up ? 1u : 0u));  // 8 is the code of 2^-6 too
 }
 
+// Packed scale layout (the order the GEMM's tensor cores read): byte of the
+// scale of row r (A, blocks along rows) or column c (B, blocks down
+// columns) for K block kb, with S K steps of 128.  A: chunk (r / 128, kb / 4)
+// at (r / 128 * S + kb / 4) * 512; B: chunk (c / 128, kb / 4) at
+// ((c / 256 * S + kb / 4) * 2 + c / 128 % 2) * 512; inside a chunk, byte
+// (r % 32) * 16 + (r / 32 % 4) * 4 + kb % 4.
+__device__ __forceinline__ int64_t packed_row_scale_at(int64_t r, int64_t kb, int64_t S) {
+  return ((r >> 7) * S + (kb >> 2)) * 512 + (r & 31) * 16 + ((r >> 5) & 3) * 4 + (kb & 3);
+}
+__device__ __forceinline__ int64_t packed_col_scale_at(int64_t c, int64_t kb, int64_t S) {
+  return (((c >> 8) * S + (kb >> 2)) * 2 + ((c >> 7) & 1)) * 512 + (c & 31) * 16 +
+         ((c >> 5) & 3) * 4 + (kb & 3);
+}
+
 template <typename T>
 __device__ __forceinline__ float mx_to_float(T v);
 template <>
@@ -104,10 +118,13 @@ __device__ __forceinline__ float mx_to_float<__nv_bfloat16>(__nv_bfloat16 v) {
 // blocks are contiguous in memory, block b = elements [32b, 32b + 32).
 // Four lanes share a block, eight values each; a warp covers eight blocks.
 // SR: rbits holds one random word per element, at the element's index.
+// S > 0: the scales go to the packed layout with S K steps (a row has kbn
+// blocks); S = 0: row-major, scale b for block b.
 template <typename T, bool SR>
 __global__ void mx_quantize_rows_kernel(const T *__restrict__ X, int64_t nblocks,
                                         const uint32_t *__restrict__ rbits,
-                                        uint8_t *__restrict__ codes, uint8_t *__restrict__ scales) {
+                                        uint8_t *__restrict__ codes, uint8_t *__restrict__ scales,
+                                        int64_t kbn, int64_t S) {
   const int lane = threadIdx.x & 31;
   const int sub = lane & 3;  // lane within the block's four
   const int64_t groups = (nblocks + 7) / 8;
@@ -166,7 +183,10 @@ __global__ void mx_quantize_rows_kernel(const T *__restrict__ X, int64_t nblocks
     }
     if (live) {
       *reinterpret_cast<uint2 *>(codes + b * 32 + sub * 8) = make_uint2(w0, w1);
-      if (sub == 0) scales[b] = static_cast<uint8_t>(s);
+      if (sub == 0) {
+        const int64_t at = S ? packed_row_scale_at(b / kbn, b % kbn, S) : b;
+        scales[at] = static_cast<uint8_t>(s);
+      }
     }
   }
 }
@@ -179,10 +199,13 @@ __global__ void mx_quantize_rows_kernel(const T *__restrict__ X, int64_t nblocks
 // stores NC codes per row.  NC = 2 needs C even.  SR (NC = 1): rbits holds
 // one random word per element, at the element's index; they are loaded with
 // the values.
+// S > 0: the scales go to the packed layout with S K steps; S = 0:
+// C x R/32, row j for column j.
 template <typename T, int NC, bool SR>
 __global__ void mx_quantize_cols_kernel(const T *__restrict__ X, int64_t R, int64_t C,
                                         const uint32_t *__restrict__ rbits,
-                                        uint8_t *__restrict__ codes, uint8_t *__restrict__ scales) {
+                                        uint8_t *__restrict__ codes, uint8_t *__restrict__ scales,
+                                        int64_t S) {
   static_assert(NC == 1 || NC == 2, "one or two columns per thread");
   constexpr int kWordBytes = NC * static_cast<int>(sizeof(T));
   using Word = typename std::conditional<
@@ -235,7 +258,8 @@ __global__ void mx_quantize_cols_kernel(const T *__restrict__ X, int64_t R, int6
       }
     }
 #pragma unroll
-    for (int c = 0; c < NC; ++c) scales[(j + c) * rblocks + rb] = static_cast<uint8_t>(s[c]);
+    for (int c = 0; c < NC; ++c)
+      scales[S ? packed_col_scale_at(j + c, rb, S) : (j + c) * rblocks + rb] = static_cast<uint8_t>(s[c]);
   }
 }
 

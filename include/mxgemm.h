@@ -106,8 +106,29 @@ typedef enum {
    * the A_format / B_format strings of async_dot_scaled).  A and B may
    * differ. */
   MXGEMM_OPT_A_FORMAT = 6,
-  MXGEMM_OPT_B_FORMAT = 7
+  MXGEMM_OPT_B_FORMAT = 7,
+  /* Layout of A_scale and B_scale, an mxgemm_scale_layout_t; default
+   * MXGEMM_SCALES_ROW_MAJOR.  With MXGEMM_SCALES_PACKED the run takes the
+   * scales in the order the tensor cores read them (as mxgemm_quantize_ex
+   * writes them) and runs no scale repack before the kernel. */
+  MXGEMM_OPT_SCALE_LAYOUT = 8
 } mxgemm_option_t;
+
+/* Scale layouts.
+ *   MXGEMM_SCALES_ROW_MAJOR : A_scale M x (K/32), B_scale N x (K/32), dense.
+ *   MXGEMM_SCALES_PACKED    : 512-byte chunks, one per 128 rows of A (or 128
+ *     columns of B) and 128-deep K step (4 scales per row).  Byte
+ *     (r % 32) * 16 + (r / 32) * 4 + j of a chunk holds the scale of its row
+ *     (column) r, r < 128, for K block 4 ks + j.  With S = ceil(K / 128):
+ *       A_scale: chunk (b, ks) of rows 128 b .. 128 b + 127 at byte
+ *                (b * S + ks) * 512;           ceil(M / 128) * S * 512 bytes
+ *       B_scale: chunk (c, ks) of columns 128 c .. 128 c + 127 at byte
+ *                ((c / 2 * S + ks) * 2 + c % 2) * 512;
+ *                                              ceil(N / 256) * S * 1024 bytes
+ *     Entries for rows (columns) past M (N) and K blocks past K/32 must hold
+ *     a finite scale (mxgemm_quantize_ex writes 127 there).  Device pointers
+ *     16-byte aligned (MXGEMM_ERR_MISALIGNED). */
+typedef enum { MXGEMM_SCALES_ROW_MAJOR = 0, MXGEMM_SCALES_PACKED = 1 } mxgemm_scale_layout_t;
 
 /* Element formats (OCP Microscaling Formats v1.0).  Every element occupies
  * one byte in A and B, also for the 6- and 4-bit formats, whose code sits
@@ -203,6 +224,26 @@ int mxgemm_quantize(const void *X, int x_dtype, int64_t R, int64_t C, int along_
 int mxgemm_quantize_sr(const void *X, int x_dtype, int64_t R, int64_t C, int along_cols,
                        const void *rand_bits, void *codes, void *scales,
                        mxgemm_stream_t stream);
+
+/* mxgemm_quantize with both choices: rand_bits NULL rounds to nearest
+ * (mxgemm_quantize), else stochastically (mxgemm_quantize_sr);
+ * scale_layout (an mxgemm_scale_layout_t) is the layout of `scales`.
+ * MXGEMM_SCALES_PACKED writes the order a run with MXGEMM_OPT_SCALE_LAYOUT
+ * = MXGEMM_SCALES_PACKED reads: along_cols = 0 gives A_scale of an M x K
+ * matrix X (M = R, K = C), along_cols = 1 gives B_scale of a K x N matrix X
+ * (K = R, N = C).  The whole packed area (mxgemm_scale_bytes) is written,
+ * the padding entries as 127; `scales` then needs 16-byte alignment
+ * (MXGEMM_ERR_MISALIGNED).  Other arguments and errors as for the two
+ * entry points above. */
+int mxgemm_quantize_ex(const void *X, int x_dtype, int64_t R, int64_t C, int along_cols,
+                       const void *rand_bits, int scale_layout, void *codes, void *scales,
+                       mxgemm_stream_t stream);
+
+/* Bytes of the scales that mxgemm_quantize_ex writes for an R x C matrix
+ * (and a run reads): row-major R * (C/32) or C * (R/32); packed as above.
+ * Host-only, no device work. */
+int mxgemm_scale_bytes(int64_t R, int64_t C, int along_cols, int scale_layout,
+                       int64_t *bytes_out);
 
 /* Set an option (mxgemm_option_t) on the handle; applies to later runs. */
 int mxgemm_set_option(mxgemm_handle_t h, int option, int64_t value);

@@ -282,3 +282,30 @@ WORKLOADS = {
     "skinny_64x8192x8192": lambda seed=0: skinny(64, seed),
     "skinny_128x8192x8192": lambda seed=0: skinny(128, seed),
 }
+
+
+def pack_scales(S, along_cols: bool = False):
+    """Rearrange row-major scales into the packed layout of mxgemm.h
+    (MXGEMM_SCALES_PACKED): S is n x K/32 uint8, rows of A (along_cols
+    False) or columns of B (along_cols True).  Returns the packed bytes (a
+    flat uint8 tensor), padding entries 127.  A layout change only: no value
+    is computed."""
+    import numpy as np
+    s = np.ascontiguousarray(S.cpu().numpy() if hasattr(S, "numpy") else S, dtype=np.uint8)
+    n, kbn = s.shape
+    steps = -(-kbn // 4)
+    if along_cols:
+        size = -(-n // 256) * steps * 1024
+    else:
+        size = -(-n // 128) * steps * 512
+    out = np.full(size, 127, dtype=np.uint8)
+    r = np.arange(n)[:, None]
+    kb = np.arange(kbn)[None, :]
+    inner = (r % 32) * 16 + ((r // 32) % 4) * 4 + kb % 4
+    if along_cols:
+        at = (((r // 256) * steps + kb // 4) * 2 + (r // 128) % 2) * 512 + inner
+    else:
+        at = ((r // 128) * steps + kb // 4) * 512 + inner
+    out[at] = s
+    return torch.from_numpy(out)
+

@@ -116,3 +116,24 @@ def test_header_is_plain_c_and_links(lib, tmp_path):
     r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=120)
     assert r.returncode == 0, (r.returncode, r.stdout, r.stderr)
     assert r.stdout.split()[0] in ("gpu", "nogpu")
+
+
+def test_scale_bytes_host_only():
+    # sizes of the scales in either layout, worked by hand from the layout
+    # definition in mxgemm.h (no device involved)
+    import block_scaled_gemm_gb300 as mx
+    lib = mx.library()
+    cases = [
+        # R, C, along_cols, layout, bytes
+        (300, 416, 0, 0, 300 * 13),               # A row-major: M x K/32
+        (300, 416, 0, 1, 3 * 4 * 512),            # ceil(300/128)=3 blocks, ceil(416/128)=4 steps
+        (416, 300, 1, 0, 300 * 13),               # B row-major: N x K/32
+        (416, 300, 1, 1, 2 * 4 * 1024),           # ceil(300/256)=2 tiles, 4 steps
+        (4096, 4096, 1, 1, 16 * 32 * 1024),
+        (1, 32, 0, 1, 1 * 1 * 512),
+    ]
+    for R, C, ac, lay, want in cases:
+        assert mx.mxgemm_scale_bytes(R, C, ac, lay) == want, (R, C, ac, lay)
+    out = ctypes.c_int64(0)
+    assert lib.mxgemm_scale_bytes(16, 32, 0, 2, ctypes.byref(out)) == mx.ERR_INVALID_VALUE
+    assert lib.mxgemm_scale_bytes(16, 32, 0, 0, None) == mx.ERR_INVALID_VALUE
