@@ -251,7 +251,13 @@ int mxgemm_set_option(mxgemm_handle_t h, int option, int64_t value);
 /* Synchronize `stream`, then read and clear the handle's device status word.
  * *status_out receives MXGEMM_OK or MXGEMM_ERR_TIMEOUT; *detail_out (may be
  * NULL) receives where the first failing wait was (role | stage << 8 |
- * tile << 16), 0 when none. */
+ * tile << 16), 0 when none.  Roles: 0x01 producer (free stage), 0x02 MMA
+ * issuer (free accumulator), 0x03 MMA issuer (full stage), 0x04 MMA issuer
+ * (final commit), 0x05 epilogue (full accumulator), 0x06 epilogue (stream-K
+ * partials), 0x07 / 0x08 cluster-launch-control response / free slot,
+ * 0x09 scale loader (free stage), 0x0A scale loader (staged scale rows),
+ * 0x0B scale loader (staging load at exit), 0x0C producer (scale loader's
+ * first staging load), 0x11 producer (drain at exit). */
 int mxgemm_get_device_status(mxgemm_handle_t h, mxgemm_stream_t stream,
                              int *status_out, int *detail_out);
 
