@@ -1165,14 +1165,24 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
           __threadfence();
           const float4 *slot = reinterpret_cast<const float4 *>(p.partials) +
                                static_cast<int64_t>(c * CG + (int)rank) * (128 * 256 / 4) + ew * (32 * 32) + lane;
+          // the row test outside the loop, and eight loads issued before their
+          // adds: with the test inside, the loads went out one after another
+          // (about 2.4 us per contributor at M = 16)
+          if (row_ok) {
 #pragma unroll
-          for (int c4 = 0; c4 < 128; c4 += 4) {
-            if (!row_ok) break;
-            const float4 o = __ldcg(slot + (c4 / 4) * 32);
-            v[c4 >> 5][(c4 & 31) + 0] = __float_as_uint(__uint_as_float(v[c4 >> 5][(c4 & 31) + 0]) + o.x);
-            v[c4 >> 5][(c4 & 31) + 1] = __float_as_uint(__uint_as_float(v[c4 >> 5][(c4 & 31) + 1]) + o.y);
-            v[c4 >> 5][(c4 & 31) + 2] = __float_as_uint(__uint_as_float(v[c4 >> 5][(c4 & 31) + 2]) + o.z);
-            v[c4 >> 5][(c4 & 31) + 3] = __float_as_uint(__uint_as_float(v[c4 >> 5][(c4 & 31) + 3]) + o.w);
+            for (int g8 = 0; g8 < 4; ++g8) {
+              float4 o[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) o[i] = __ldcg(slot + (g8 * 8 + i) * 32);
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const int c4 = (g8 * 8 + i) * 4;
+                v[c4 >> 5][(c4 & 31) + 0] = __float_as_uint(__uint_as_float(v[c4 >> 5][(c4 & 31) + 0]) + o[i].x);
+                v[c4 >> 5][(c4 & 31) + 1] = __float_as_uint(__uint_as_float(v[c4 >> 5][(c4 & 31) + 1]) + o[i].y);
+                v[c4 >> 5][(c4 & 31) + 2] = __float_as_uint(__uint_as_float(v[c4 >> 5][(c4 & 31) + 2]) + o[i].z);
+                v[c4 >> 5][(c4 & 31) + 3] = __float_as_uint(__uint_as_float(v[c4 >> 5][(c4 & 31) + 3]) + o[i].w);
+              }
+            }
           }
         }
         if (!got) break;
