@@ -377,14 +377,16 @@ def test_plan_cache_churn_and_workspace_growth(h):
         assert res["ok"], f"{p.name}: {res}"
 
 
-@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("mode,M", [(1, 300), (2, 300), (0, 100)])
 @pytest.mark.parametrize("K", [1024, 384, 160])
-def test_scales_at_unaligned_addresses(h, mode, K):
+def test_scales_at_unaligned_addresses(h, mode, M, K):
     # A_scale and B_scale one byte past a 16-byte boundary: the scale chunks
-    # are built from byte loads instead of 16-byte ones (single CTAs in the
-    # kernel, pairs in the repack); the result is the same, bit for bit
+    # are built from byte loads instead of 16-byte ones (M = 300: the repack,
+    # for single CTAs and pairs; M = 100: the kernel's scale loader, whose
+    # rows are also read byte by byte when K % 512 != 0); the result is the
+    # same, bit for bit
     _mode(h, mode)
-    p = mi.random_problem(300, 520, K, seed=K + mode, kind="normal")
+    p = mi.random_problem(M, 520, K, seed=K + mode + M, kind="normal")
     ref_c = gu.run_gpu(h, p).cpu()
     dev = gu.DEV
 
