@@ -1,4 +1,5 @@
-"""Randomized parity sweep: seeded random shapes, tile modes, output types,
+"""Randomized parity sweep: seeded random shapes, tile modes, output types, scale
+layouts (row-major, row-major at unaligned addresses, packed),
 use_acc, element formats and schedulers, each checked against the oracle on
 whole rows (including the first and last row and a row from every 256-row
 band touched), so that interior tiles, ragged edges and the tail-balancing
@@ -79,3 +80,49 @@ def test_random_configuration(h, i):
         mx.mxgemm_set_option(h, mx.OPT_SCHEDULER, 0)
     res = oracle.accept(gu.to_numpy_out(C, out_dtype)[rows], ref, bound, out_dtype)
     assert res["ok"], f"case {i} {(M, N, K, mode, out_dtype, use_acc, fa, fb, sched)}: {res}"
+
+
+def _shifted(t):
+    # the same bytes one past a 16-byte boundary
+    buf = torch.empty(t.numel() + 16, dtype=torch.uint8, device="cuda")
+    v = buf[1:1 + t.numel()].view(t.shape)
+    v.copy_(t)
+    return v
+
+
+@pytest.mark.parametrize("i", range(24))
+def test_random_scale_layouts(h, i):
+    # the same random problem with aligned row-major scales, row-major scales
+    # at unaligned addresses and packed scales: identical C, bit for bit, and
+    # the oracle on sampled rows
+    M, N, K, mode, out_dtype, use_acc, _, _, _ = _case(100 + i)
+    p = mi.random_problem(M, N, K, seed=6000 + i, kind="normal", out_dtype=out_dtype)
+    cin = mi.c_init(M, N, 7000 + i, out_dtype) if use_acc else None
+    tdt = torch.float32 if out_dtype == "f32" else torch.bfloat16
+    A, B = p.A.cuda(), p.B.cuda()
+    variants = [(p.As.cuda(), p.Bs.cuda(), mx.SCALES_ROW_MAJOR),
+                (_shifted(p.As.cuda()), _shifted(p.Bs.cuda()), mx.SCALES_ROW_MAJOR),
+                (mi.pack_scales(p.As).cuda(), mi.pack_scales(p.Bs, along_cols=True).cuda(), mx.SCALES_PACKED)]
+    outs = []
+    mx.mxgemm_set_option(h, mx.OPT_MODE, mode)
+    try:
+        for As, Bs, layout in variants:
+            mx.mxgemm_set_option(h, mx.OPT_SCALE_LAYOUT, layout)
+            C = (cin.to(tdt).cuda().clone() if cin is not None
+                 else torch.full((M, N), float("nan"), dtype=tdt, device="cuda"))
+            mx.mxgemm_run(h, M, N, K, A, As, B, Bs, C, int(use_acc), gu.out_code(out_dtype))
+            torch.cuda.synchronize()
+            st, det = mx.mxgemm_get_device_status(h)
+            assert st == 0, (st, det)
+            outs.append(C.cpu())
+    finally:
+        mx.mxgemm_set_option(h, mx.OPT_SCALE_LAYOUT, mx.SCALES_ROW_MAJOR)
+        mx.mxgemm_set_option(h, mx.OPT_MODE, 0)
+    iv = torch.int16 if out_dtype == "bf16" else torch.int32
+    assert torch.equal(outs[0].view(iv), outs[1].view(iv)), "unaligned scales differ"
+    assert torch.equal(outs[0].view(iv), outs[2].view(iv)), "packed scales differ"
+    rows = np.unique(np.array([0, M - 1, M // 2, min(M - 1, 129)], dtype=np.int64))
+    ref, bound = oracle.rows(p.A, p.As, p.B, p.Bs, rows=rows,
+                             c_in=None if cin is None else cin.to(torch.float64).numpy()[rows])
+    res = oracle.accept(gu.to_numpy_out(outs[0], out_dtype)[rows], ref, bound, out_dtype)
+    assert res["ok"], (M, N, K, mode, res)
