@@ -866,7 +866,8 @@ extern "C" int mxgemm_quantize_ex(const void *X, int x_dtype, int64_t R, int64_t
 
 extern "C" int mxgemm_scale_bytes(int64_t R, int64_t C, int along_cols, int scale_layout,
                                   int64_t *bytes_out) {
-  if (!bytes_out || R < 0 || C < 0 || (along_cols != 0 && along_cols != 1))
+  if (!bytes_out || R < 0 || C < 0 || (along_cols != 0 && along_cols != 1) ||
+      (along_cols ? R % 32 : C % 32) != 0)
     return MXGEMM_ERR_INVALID_VALUE;
   const int64_t b = scale_bytes(R, C, along_cols, scale_layout);
   if (b < 0) return MXGEMM_ERR_INVALID_VALUE;

@@ -241,7 +241,8 @@ int mxgemm_quantize_ex(const void *X, int x_dtype, int64_t R, int64_t C, int alo
 
 /* Bytes of the scales that mxgemm_quantize_ex writes for an R x C matrix
  * (and a run reads): row-major R * (C/32) or C * (R/32); packed as above.
- * Host-only, no device work. */
+ * The block dimension (C, or R with along_cols) must be a multiple of 32
+ * (MXGEMM_ERR_INVALID_VALUE).  Host-only, no device work. */
 int mxgemm_scale_bytes(int64_t R, int64_t C, int along_cols, int scale_layout,
                        int64_t *bytes_out);
 

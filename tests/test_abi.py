@@ -137,3 +137,5 @@ def test_scale_bytes_host_only():
     out = ctypes.c_int64(0)
     assert lib.mxgemm_scale_bytes(16, 32, 0, 2, ctypes.byref(out)) == mx.ERR_INVALID_VALUE
     assert lib.mxgemm_scale_bytes(16, 32, 0, 0, None) == mx.ERR_INVALID_VALUE
+    assert lib.mxgemm_scale_bytes(16, 48, 0, 0, ctypes.byref(out)) == mx.ERR_INVALID_VALUE  # C % 32
+    assert lib.mxgemm_scale_bytes(48, 16, 1, 1, ctypes.byref(out)) == mx.ERR_INVALID_VALUE  # R % 32
