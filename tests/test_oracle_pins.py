@@ -523,3 +523,35 @@ def test_stochastic_quantizer_keeps_scales_and_brackets_codes():
     ct, st = oracle.quantize_e4m3(xt.t().contiguous(), rand_bits=np.ascontiguousarray(rb[:, :64].T))
     assert np.array_equal(c2, ct.T) and np.array_equal(s2, st)
 
+
+
+def test_stochastic_rounding_against_exact_rationals():
+    # the definition again, in exact rationals (no floating point): the E4M3
+    # magnitude below |y| on the grid, the fraction of the step above it, and
+    # the comparison of r with 2^32 times that fraction; codes come from the
+    # decoder's table of the 127 finite magnitudes
+    from fractions import Fraction
+    table = {Fraction(oracle.e4m3(c)): c for c in range(0x7F)}
+    rng = np.random.default_rng(67)
+    ys = np.concatenate([rng.standard_normal(300) * 100, rng.standard_normal(300) * 0.01,
+                         rng.standard_normal(100) * 1e-35,
+                         rng.integers(-3584, 3585, 200) / 8.0]).astype(np.float32)
+    rs = rng.integers(0, 2 ** 32, ys.size, dtype=np.uint64)
+    rs[::5] = 0
+    rs[1::7] = 2 ** 32 - 1
+    for yv, r in zip(ys, rs):
+        y = Fraction(float(yv))
+        a = min(abs(y), Fraction(448))
+        sign = 0x80 if float(yv) < 0 or (float(yv) == 0 and np.signbit(yv)) else 0
+        if a == 0:
+            want = sign
+        else:
+            e = a.numerator.bit_length() - a.denominator.bit_length()
+            if Fraction(2) ** e > a:
+                e -= 1                      # now 2^e <= a < 2^(e+1)
+            q = Fraction(2) ** (max(e, -6) - 3)
+            n = a // q
+            frac = a / q - n
+            mag = (n + 1) * q if int(r) < frac * 2 ** 32 else n * q
+            want = sign | table[mag]
+        assert oracle.e4m3_sr(float(yv), int(r)) == want, (float(yv), int(r))
