@@ -152,7 +152,10 @@ int mxgemm_create(mxgemm_handle_t *out, int device);
  *               M == 0 or N == 0 is a no-op; K == 0 sets C to 0 (use_acc=0)
  *               or leaves it unchanged (use_acc=1).
  *   A, B, C   : device pointers, 16-byte aligned (MXGEMM_ERR_MISALIGNED).
- *   A_scale, B_scale : device pointers, any alignment.
+ *   A_scale, B_scale : device pointers, any alignment (row-major layout,
+ *               the default); with MXGEMM_OPT_SCALE_LAYOUT =
+ *               MXGEMM_SCALES_PACKED the packed chunks of
+ *               mxgemm_scale_layout_t, 16-byte aligned.
  *   use_acc   : 0 or 1 (see above).
  *   out_dtype : MXGEMM_OUT_F32 or MXGEMM_OUT_BF16.
  * C must not overlap A, B or the scales.  The call returns after enqueueing;
