@@ -28,7 +28,8 @@ __all__ = [
     "mxgemm_destroy", "mxgemm_set_option", "mxgemm_get_device_status", "mxgemm_status_string",
     "mxgemm_set_profile_events", "mxgemm_get_launch_count", "mxgemm_run_noalloc", "mxgemm_run_host",
     "mxgemm_quantize", "IN_F32", "IN_BF16", "EXPORTED_SYMBOLS", "Gemm", "OPT_SCALE_LAYOUT",
-    "SCALES_ROW_MAJOR", "SCALES_PACKED", "mxgemm_scale_bytes",
+    "SCALES_ROW_MAJOR", "SCALES_PACKED", "mxgemm_scale_bytes", "mxgemm_noalloc_get_status",
+    "mxgemm_noalloc_set_option",
 ]
 
 OUT_F32 = 0
@@ -68,7 +69,8 @@ EXPORTED_SYMBOLS = (
     "mxgemm_create", "mxgemm_run", "mxgemm_destroy", "mxgemm_set_option",
     "mxgemm_get_device_status", "mxgemm_status_string", "mxgemm_set_profile_events",
     "mxgemm_get_launch_count", "mxgemm_run_noalloc", "mxgemm_run_host", "mxgemm_quantize",
-    "mxgemm_quantize_sr", "mxgemm_quantize_ex", "mxgemm_scale_bytes",
+    "mxgemm_quantize_sr", "mxgemm_quantize_ex", "mxgemm_scale_bytes", "mxgemm_noalloc_get_status",
+    "mxgemm_noalloc_set_option",
 )
 
 _lib = None
@@ -121,6 +123,10 @@ def library():
         lib.mxgemm_run_host.restype = i32
         lib.mxgemm_run_noalloc.argtypes = [i64, i64, i64, vp, vp, vp, vp, vp, i32, i32, vp]
         lib.mxgemm_run_noalloc.restype = i32
+        lib.mxgemm_noalloc_get_status.argtypes = [vp, ctypes.POINTER(i32), ctypes.POINTER(i32)]
+        lib.mxgemm_noalloc_get_status.restype = i32
+        lib.mxgemm_noalloc_set_option.argtypes = [i32, i64]
+        lib.mxgemm_noalloc_set_option.restype = i32
         lib.mxgemm_status_string.argtypes = [i32]
         lib.mxgemm_status_string.restype = ctypes.c_char_p
         _lib = lib
@@ -236,6 +242,22 @@ def mxgemm_run_noalloc(M, N, K, A, A_scale, B, B_scale, C, use_acc=0, out_dtype=
     if check:
         _check(st, "mxgemm_run_noalloc")
     return st
+
+
+def mxgemm_noalloc_get_status(stream=None):
+    """Synchronize `stream`, then read and clear the current device's status
+    word of mxgemm_run_noalloc: (status, detail), the first failure since the
+    last read."""
+    st, det = ctypes.c_int(), ctypes.c_int()
+    _check(library().mxgemm_noalloc_get_status(_stream(stream), ctypes.byref(st), ctypes.byref(det)),
+           "mxgemm_noalloc_get_status")
+    return st.value, det.value
+
+
+def mxgemm_noalloc_set_option(option: int, value: int) -> None:
+    """Process-wide option of mxgemm_run_noalloc (OPT_WAIT_TIMEOUT_NS or
+    OPT_TEST_STALL_PRODUCER)."""
+    _check(library().mxgemm_noalloc_set_option(int(option), int(value)), "mxgemm_noalloc_set_option")
 
 
 def mxgemm_set_option(h, option: int, value: int) -> None:

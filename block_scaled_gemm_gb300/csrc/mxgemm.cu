@@ -13,6 +13,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <new>
 
@@ -1079,8 +1080,7 @@ extern "C" int mxgemm_run_host(mxgemm_handle_t h, int64_t M, int64_t N, int64_t 
 //
 // Callers that cannot allocate device memory where they call the GEMM (a
 // plug-in whose host framework owns all device memory, code that must not
-// allocate after start-up, a stream that is being captured) use this entry
-// point.  The kernel builds the scale chunks itself (fused scales), so its
+// allocate after start-up) use this entry point.  The kernel builds the scale chunks itself (fused scales), so its
 // only scratch is B re-pitched when N % 16 != 0.  That lives in the
 // file-scope array below, which the CUDA runtime places when it loads this
 // library's device code: every GPU that loads the library holds these
@@ -1108,6 +1108,9 @@ constexpr int kNoAllocMaxDevices = 64;
 NoAllocDevice g_noalloc_dev[kNoAllocMaxDevices];
 std::mutex g_noalloc_mu;
 PFN_cuTensorMapEncodeTiled_v12000 g_noalloc_encode = nullptr;
+// process-wide options of the no-allocation path (mxgemm_noalloc_set_option)
+std::atomic<long long> g_noalloc_timeout_ns{2000000000LL};
+std::atomic<int> g_noalloc_stall{0};
 
 // Once per device, with that device current: check it, and look up the
 // device addresses of the scratch arrays (in host code their names are
@@ -1219,6 +1222,8 @@ extern "C" int mxgemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A
   ctx.ws.ptr = nd->scratch;
   ctx.ws.bytes = kNoAllocScratchBytes;
   ctx.encode = g_noalloc_encode;
+  ctx.timeout_ns = g_noalloc_timeout_ns.load();
+  ctx.stall_producer = g_noalloc_stall.load();
   {
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
     for (int i = 0; i < 3; ++i)
@@ -1229,11 +1234,9 @@ extern "C" int mxgemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A
                   n_tiles, k_steps, num_tiles, a_chunks, b_chunks, pad_b, npad, sp, z, 8, 8,
                   true, false);
   if (st != MXGEMM_OK) return st;
-  // the status word must start each call at zero
-  if (cudaMemsetAsync(nd->status, 0, 2 * sizeof(int), stream) != cudaSuccess) {
-    cudaGetLastError();
-    return MXGEMM_ERR_CUDA;
-  }
+  // The status word is not cleared here: it keeps the first failure since
+  // mxgemm_noalloc_get_status last read (and cleared) it, so that one read
+  // after many calls still sees a failure in any of them.
   if (pad_b)
     mxg::pad_rows_kernel<<<launch_blocks(K * (npad / 16), 256), 256, 0, stream>>>(
         static_cast<const uint8_t *>(B), K, N, npad, nd->scratch + off_b, 8);
@@ -1248,4 +1251,44 @@ extern "C" int mxgemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A
       for (int j = 0; j < 8; ++j) nd->attr_set[i][j] = nd->attr_set[i][j] || ctx.attr_set[i][j];
   }
   return st;
+}
+
+extern "C" int mxgemm_noalloc_set_option(int option, int64_t value) {
+  switch (option) {
+    case MXGEMM_OPT_WAIT_TIMEOUT_NS:
+      if (value <= 0) return MXGEMM_ERR_INVALID_VALUE;
+      g_noalloc_timeout_ns.store(static_cast<long long>(value));
+      return MXGEMM_OK;
+    case MXGEMM_OPT_TEST_STALL_PRODUCER:
+      if (value < 0 || value > 1) return MXGEMM_ERR_INVALID_VALUE;
+      g_noalloc_stall.store(static_cast<int>(value));
+      return MXGEMM_OK;
+    default:
+      return MXGEMM_ERR_INVALID_VALUE;
+  }
+}
+
+extern "C" int mxgemm_noalloc_get_status(mxgemm_stream_t stream_, int *status_out, int *detail_out) {
+  if (!status_out) return MXGEMM_ERR_INVALID_VALUE;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return MXGEMM_ERR_CUDA;
+  }
+  NoAllocDevice *nd = nullptr;
+  int st = noalloc_setup(dev, &nd);
+  if (st != MXGEMM_OK) return st;
+  cudaStream_t stream = static_cast<cudaStream_t>(stream_);
+  // a plain synchronous copy into the caller's host ints: no pinned staging
+  // buffer is allocated
+  int hostv[2] = {0, 0};
+  if (cudaStreamSynchronize(stream) != cudaSuccess ||
+      cudaMemcpy(hostv, nd->status, sizeof(hostv), cudaMemcpyDeviceToHost) != cudaSuccess ||
+      cudaMemset(nd->status, 0, sizeof(hostv)) != cudaSuccess) {
+    cudaGetLastError();
+    return MXGEMM_ERR_CUDA;
+  }
+  *status_out = hostv[0];
+  if (detail_out) *detail_out = hostv[1];
+  return MXGEMM_OK;
 }

@@ -38,7 +38,8 @@
  *
  * Entry points: mxgemm_run (device operands), mxgemm_run_host (host
  * operands, copies pipelined with the GEMM), mxgemm_run_noalloc (no device
- * allocation, fixed scratch), mxgemm_quantize and mxgemm_quantize_sr
+ * allocation, fixed scratch; with mxgemm_noalloc_get_status and
+ * mxgemm_noalloc_set_option), mxgemm_quantize and mxgemm_quantize_sr
  * (FP32/BF16 -> E4M3 codes and E8M0 scales on the GPU, rounding to nearest
  * or stochastically), plus handle, option, status and timing helpers.
  */
@@ -141,13 +142,20 @@ typedef enum {
   MXGEMM_FMT_E2M1 = 4  /* FP4, max 6 */
 } mxgemm_format_t;
 
-/* Create a handle bound to CUDA device `device`.  Fails with
+/* Create a handle bound to CUDA device `device`.  The handle carries the
+ * state that mxgemm_run needs between calls (workspace, plan cache, status
+ * word); the scaled product itself is `async_dot_scaled` of "TLX API Quick
+ * Reference", section "Matrix Multiply (MMA)", whose operands mxgemm_run
+ * takes in the same order.  Fails with
  * MXGEMM_ERR_UNSUPPORTED_DEVICE unless the device is compute capability 10.3
  * (sm_103, GB300).  Allocates the handle's device status word and its
  * partial-sum flag slots. */
 int mxgemm_create(mxgemm_handle_t *out, int device);
 
-/* Enqueue C (+)= A.B on `stream` (NULL = the legacy default stream).
+/* Enqueue C (+)= A.B on `stream` (NULL = the legacy default stream): the
+ * scaled product D = (A*scale_A) @ (B*scale_B) (+ D) of "TLX API Quick
+ * Reference", section "Matrix Multiply (MMA)" (`async_dot_scaled` with
+ * A_format = B_format = "e4m3" and use_acc), over the whole of M, N, K.
  *   M, N, K   : sizes, each in [0, 2^31); K must be a multiple of 32.
  *               M == 0 or N == 0 is a no-op; K == 0 sets C to 0 (use_acc=0)
  *               or leaves it unchanged (use_acc=1).
@@ -277,15 +285,19 @@ int mxgemm_set_profile_events(mxgemm_handle_t h, void *ev_before, void *ev_after
  * prepasses), in *count_out. */
 int mxgemm_get_launch_count(mxgemm_handle_t h, int64_t *count_out);
 
-/* Free the handle's device memory (synchronizes its device) and the handle. */
+/* Free the handle's device memory (synchronizes its device) and the handle
+ * (the counterpart of mxgemm_create; the product is that of "TLX API Quick
+ * Reference", section "Matrix Multiply (MMA)"). */
 int mxgemm_destroy(mxgemm_handle_t h);
 
 /* The same product as mxgemm_run, for callers that cannot allocate device
  * memory where they call it: a plug-in whose host framework owns all device
- * memory, code that must not allocate after start-up, or a stream that is
- * being captured.  It takes no handle, allocates nothing (no cudaMalloc,
- * cudaFree or allocating library call) and runs on the current device and
- * the given stream.  The paper has no counterpart to this entry point.
+ * memory (and hands the plug-in only its inputs and outputs), or code that
+ * must not allocate after start-up (an allocation there can fail, block on
+ * other streams or fragment the caller's pool).  It takes no handle,
+ * allocates nothing (no cudaMalloc, cudaFree or allocating library call) and
+ * runs on the current device and the given stream.  Neither the paper nor
+ * the pages it draws on have a counterpart to this entry point.
  *
  * Scratch: B re-pitched to a 16-byte row pitch when N % 16 != 0 goes to one
  * file-scope device array of 16 MiB, which every GPU that loads this library
@@ -301,13 +313,29 @@ int mxgemm_destroy(mxgemm_handle_t h);
  * check and lookup of the array's device address); make that first call
  * before starting any stream capture.  Arguments, layouts and use_acc are as
  * for mxgemm_run; it always uses single-CTA 128x256 tiles computed whole.  A
- * device-side wait that runs out
- * is recorded in an internal status word that this entry point cannot report:
- * C is then incomplete. */
+ * device-side wait that runs out records MXGEMM_ERR_TIMEOUT in a status word
+ * of the current device (C is then incomplete); the word keeps the first
+ * failure until mxgemm_noalloc_get_status reads and clears it. */
 int mxgemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A,
                        const void *A_scale, const void *B, const void *B_scale,
                        void *C, int use_acc, int out_dtype,
                        mxgemm_stream_t stream);
+
+/* Synchronize `stream`, then read and clear the current device's status
+ * word of mxgemm_run_noalloc: *status_out receives MXGEMM_OK or
+ * MXGEMM_ERR_TIMEOUT (the first failure of any call since the last read),
+ * *detail_out (may be NULL) where the wait was, with the codes of
+ * mxgemm_get_device_status.  Allocates nothing: the word is copied into the
+ * caller's host ints.  The first use on a device does the same one-time
+ * set-up as mxgemm_run_noalloc.  No counterpart on the pages, as for
+ * mxgemm_run_noalloc. */
+int mxgemm_noalloc_get_status(mxgemm_stream_t stream, int *status_out, int *detail_out);
+
+/* Options of mxgemm_run_noalloc, for the whole process (it has no handle):
+ * MXGEMM_OPT_WAIT_TIMEOUT_NS (default 2e9) and the test hook
+ * MXGEMM_OPT_TEST_STALL_PRODUCER (default 0), as for mxgemm_set_option;
+ * other options are MXGEMM_ERR_INVALID_VALUE.  Applies to later calls. */
+int mxgemm_noalloc_set_option(int option, int64_t value);
 
 /* Static description of a status code. */
 const char *mxgemm_status_string(int status);

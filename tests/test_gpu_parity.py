@@ -132,17 +132,27 @@ def test_bf16_out_and_ragged_n(h, mode):
             gu.check_full(h, p)
 
 
-def test_one_vs_two_cta_identical(h):
-    p = mi.random_problem(512, 768, 1024, seed=11, kind="normal")
-    _mode(h, 1)
-    c1 = gu.run_gpu(h, p).cpu()
-    _mode(h, 2)
-    c2 = gu.run_gpu(h, p).cpu()
-    # same tile order of K accumulation within an output element; allow the
-    # tolerance anyway but report exact agreement
+@pytest.mark.parametrize("out_dtype", ["f32", "bf16"])
+def test_one_vs_two_cta_identical(h, out_dtype):
+    # Whole tiles in both modes (no tail splitting): every output element is
+    # the same sequence of K = 32 block-scaled MMAs, accumulated in FP32 in
+    # the same order, whether its 128 rows belong to a single-CTA MMA
+    # (M = 128) or to one half of a pair's MMA (M = 256).  The two results
+    # must agree bit for bit, and each with the oracle.
+    p = mi.random_problem(512, 768, 1024, seed=11, kind="normal", out_dtype=out_dtype)
+    mx.mxgemm_set_option(h, mx.OPT_STREAM_K, 0)
+    try:
+        _mode(h, 1)
+        c1 = gu.run_gpu(h, p).cpu()
+        _mode(h, 2)
+        c2 = gu.run_gpu(h, p).cpu()
+    finally:
+        mx.mxgemm_set_option(h, mx.OPT_STREAM_K, 1)
     ref, bound = oracle.rows(p.A, p.As, p.B, p.Bs)
-    assert oracle.accept(c1.numpy(), ref, bound, "f32")["ok"]
-    assert oracle.accept(c2.numpy(), ref, bound, "f32")["ok"]
+    assert oracle.accept(gu.to_numpy_out(c1, out_dtype), ref, bound, out_dtype)["ok"]
+    assert oracle.accept(gu.to_numpy_out(c2, out_dtype), ref, bound, out_dtype)["ok"]
+    bits = (lambda c: c.view(torch.int16)) if out_dtype == "bf16" else (lambda c: c.view(torch.int32))
+    assert torch.equal(bits(c1), bits(c2))
 
 
 def test_repeat_determinism(h):
