@@ -3,20 +3,26 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl mx|reference]
 
-One step = one C = A.B call through the C interface (scale repack prepasses +
-the tcgen05 GEMM kernel) on the square 4096 x 4096 x 4096 MXFP8 workload
-(E4M3 operands quantized per 32-element K block from N(0,1), E8M0 scale bytes
-replaced by uniform integers in [123, 131], FP32 output), inputs resident in
-HBM.  The operands plus C (97 MB) fit in the 126 MB L2, so a 256 MiB buffer
-is written between timed steps (L2 flushed) and each step is timed with its
-own CUDA events on the launching stream; the flush is outside the events.
+One step = one C = A.B call through the C interface (scale repack prepass +
+the tcgen05 GEMM kernel) on the LLM MLP up-projection workload: M = 8192
+tokens, N = 28672, K = 8192, A from N(0,1) activations with 0.1 % outliers
+x50, B from N(0, 0.02) weights, both quantized per 32-element K block to E4M3
+with E8M0 scales, BF16 output, CTA-pair (cta_group::2) tiles; inputs resident
+in HBM.  The operands (311 MB) exceed the 126 MB L2; a buffer of twice the
+L2 size is written between timed steps all the same, outside the CUDA events
+that time each step on the launching stream.
 
-Prints one JSON line: metric TFLOP/s = 2MNK / t (whole job), the roofline of
-the GEMM kernel (timed alone by events the library records around its
-launch) against the MXFP8 tensor peak, end-to-end TFLOP/s through the C
-interface with pinned host buffers (H2D of A, B and scales + D2H of C inside
-the timed region), SM clocks sampled during the timed region, and the CPU
-oracle timed on a bounded sample of the same workload.
+Prints one JSON line: metric TFLOP/s = 2MNK / t (whole job; t the sum of the
+per-step event times), per-step medians (flushed and hot L2), the roofline
+of the GEMM kernel (timed alone by events the library records around its
+launch) against the MXFP8 tensor peak, a sustained rate (the same step back
+to back for a few seconds), the other workloads of the suite in a
+"workloads" object (square 4096, long K, ragged, square 256, the skinny
+decode shapes with their HBM GB/s), each with its own spot parity,
+end-to-end TFLOP/s through the host-buffer entry point with pinned host
+buffers (H2D of A, B and scales + D2H of C inside the timed region), SM
+clocks sampled during the timed region, and the CPU oracle timed on a bounded
+sample of the same workload.
 
 ``--impl reference`` times the CPU oracle (the plain FP64 definition) on the
 same workload, a bounded sample of rows per step, on the host cores.
@@ -44,14 +50,18 @@ if str(ROOT) not in sys.path:
 
 METRIC = "MXFP8 GEMM TFLOP/s (2MNK/t) and % of GB300 dense MXFP8 peak, 1 GPU"
 UNIT = "TFLOP/s"
-WORKLOAD = "square_4096"
+WORKLOAD = "mlp_up_8192x28672x8192"
+# the other workloads measured in the same run (the "workloads" object)
+WORKLOAD_TABLE = ["square_4096", "longk_2048_65536", "ragged_5000x7000x8192", "square_256",
+                  "skinny_1x8192x8192", "skinny_16x8192x8192", "skinny_64x8192x8192",
+                  "skinny_128x8192x8192"]
 FP8_OVER_BF16 = 2.0  # nominal dense MXFP8 / BF16 tensor rate (4.5 / 2.25 PFLOP/s)
 FALLBACK_BF16_BURST = 1900.0  # TFLOP/s, used only when MEASURED_PEAKS.json is absent
 FORMATS = ["e4m3", "e5m2", "e2m3", "e3m2", "e2m1"]  # C interface order (mxgemm_format_t)
 FALLBACK_HBM_GBS = 6800.0     # GB/s, used only when MEASURED_PEAKS.json is absent
 KERNEL_SOURCES = ["block_scaled_gemm_gb300/csrc/mxgemm_kernel.cuh",
                   "block_scaled_gemm_gb300/csrc/ptx.cuh"]
-PROFILE_SUMMARY = ROOT / "profiles" / "mxgemm_kernel_square_4096.md"
+PROFILES = ROOT / "profiles"
 
 
 # ----------------------------------------------------------------------------- ranks
@@ -240,11 +250,12 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def profiled_traffic():
-    """DRAM bytes per launch of the GEMM kernel from the committed ncu summary,
-    if it was taken on the current kernel source; else None."""
+def profiled_traffic(workload: str):
+    """DRAM bytes per launch of the GEMM kernel from the committed ncu summary
+    of this workload, if it was taken on the current kernel source; else
+    None."""
     try:
-        text = PROFILE_SUMMARY.read_text()
+        text = (PROFILES / f"mxgemm_kernel_{workload}.md").read_text()
     except OSError:
         return None
     vals = {}
@@ -410,6 +421,132 @@ def run_quantize(args, world, rank, local):
     return 0
 
 
+class GemmSteps:
+    """The calls of one step of a workload through the C interface (one
+    mxgemm_run, or the chained use_acc calls of a K-split workload), with
+    device operands prepared once."""
+
+    def __init__(self, mx, h, prob, dev, packed: bool, stream):
+        import torch
+        import mx_inputs
+        self.mx, self.h, self.prob, self.stream = mx, h, prob, stream
+        self.out_code = mx.OUT_F32 if prob.out_dtype == "f32" else mx.OUT_BF16
+        tdt = torch.float32 if prob.out_dtype == "f32" else torch.bfloat16
+        self.C = torch.zeros((prob.M, prob.N), dtype=tdt, device=dev)
+        self.calls = []
+        chunks = [prob.chunk(c) for c in range(prob.k_chunks)] if prob.k_chunks > 1 else \
+            [(prob.A, prob.As, prob.B, prob.Bs, prob.K)]
+        self.keep = []
+        for c, (A, As, B, Bs, K) in enumerate(chunks):
+            if packed:
+                As = mx_inputs.pack_scales(As)
+                Bs = mx_inputs.pack_scales(Bs, along_cols=True)
+            t = [x.to(dev) for x in (A, As, B, Bs)]
+            self.keep.append(t)
+            # a K-split workload accumulates every call into C (use_acc)
+            ua = 1 if (prob.use_acc or c > 0) else 0
+            self.calls.append((prob.M, prob.N, K, *t, self.C, ua, self.out_code))
+        self.flops = 2.0 * prob.M * prob.N * prob.K
+
+    def run(self, k_events=None):
+        mx = self.mx
+        for i, (M, N, K, A, As, B, Bs, C, ua, oc) in enumerate(self.calls):
+            if k_events is not None:
+                mx.mxgemm_set_profile_events(self.h, k_events[i][0], k_events[i][1])
+            mx.mxgemm_run(self.h, M, N, K, A, As, B, Bs, C, ua, oc, self.stream)
+        if k_events is not None:
+            mx.mxgemm_set_profile_events(self.h, None, None)
+
+    def alg_bytes(self) -> int:
+        """Algorithmic HBM bytes of one step: operands, scales, C written
+        (and read by every use_acc call)."""
+        ob = 4 if self.prob.out_dtype == "f32" else 2
+        total = 0
+        for (M, N, K, *_rest, ua, _oc) in self.calls:
+            total += M * K + K * N + (M + N) * K // 32 + M * N * ob * (2 if ua else 1)
+        return total
+
+
+def _events(torch, n):
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    return ev
+
+
+def _prime_events(torch, stream, evs):
+    # torch creates the CUDA events lazily, at their first record
+    for a, b in evs:
+        a.record(stream)
+        b.record(stream)
+
+
+def time_workload(torch, ws: GemmSteps, steps: int, warmup: int, flush, dev):
+    """Per-step CUDA-event times (ms) of `steps` steps with L2 flushed
+    between steps (outside the events), per-step GEMM-kernel times (the
+    library's events around each kernel launch, a second loop), and per-step
+    times of back-to-back steps with no flush (hot L2)."""
+    stream = ws.stream
+    for _ in range(warmup):
+        if flush is not None:
+            flush.zero_()
+        ws.run()
+    s_ev = _events(torch, steps)
+    k_ev = [_events(torch, len(ws.calls)) for _ in range(steps)]
+    h_ev = _events(torch, steps)
+    _prime_events(torch, stream, s_ev + h_ev + [e for k in k_ev for e in k])
+    torch.cuda.synchronize(dev)
+    for i in range(steps):
+        if flush is not None:
+            flush.zero_()
+        s_ev[i][0].record(stream)
+        ws.run()
+        s_ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    for i in range(steps):
+        if flush is not None:
+            flush.zero_()
+        ws.run(k_events=k_ev[i])
+    for i in range(steps):
+        h_ev[i][0].record(stream)
+        ws.run()
+        h_ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    step = [a.elapsed_time(b) for a, b in s_ev]
+    kern = [sum(a.elapsed_time(b) for a, b in k) for k in k_ev]
+    hot = [a.elapsed_time(b) for a, b in h_ev]
+    return step, kern, hot
+
+
+def roofline_of(ws: GemmSteps, kern_ms: float, peak, peak_src, hbm, hbm_src):
+    """Tensor-bound when the arithmetic intensity is above the ridge (peak
+    FLOP/s / HBM bytes/s), else HBM-bound; achieved from the kernel time."""
+    ab = ws.alg_bytes()
+    if ws.flops / ab >= peak * 1e12 / (hbm * 1e9):
+        a = ws.flops / (kern_ms * 1e-3) / 1e12
+        return {"bound": "tensor", "achieved": a, "peak": peak, "unit": UNIT, "frac": a / peak,
+                "peak_source": peak_src, "algorithmic_bytes": ab}
+    gbs = ab / (kern_ms * 1e-3) / 1e9
+    return {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm,
+            "peak_source": hbm_src, "algorithmic_bytes": ab,
+            "tflops": ws.flops / (kern_ms * 1e-3) / 1e12}
+
+
+def spot_parity(torch, ws: GemmSteps, a_fmt, b_fmt, n=256, seed=1):
+    """Run one fresh step (C zeroed first: a use_acc chain then holds exactly
+    the product) and compare n seeded points with the oracle."""
+    import numpy as np
+    import oracle
+    p = ws.prob
+    ws.C.zero_()
+    ws.run()
+    torch.cuda.synchronize()
+    g = np.random.default_rng(seed)
+    I, J = g.integers(0, p.M, n), g.integers(0, p.N, n)
+    ref, bound = oracle.points(p.A, p.As, p.B, p.Bs, I, J, a_fmt=a_fmt, b_fmt=b_fmt)
+    got = ws.C.float().cpu().numpy()[I, J]
+    acc = oracle.accept(got, ref, bound, "f32" if p.out_dtype == "f32" else "bf16")
+    return {"points": int(I.size), "ok": acc["ok"], "max_err_over_bound": acc["max_err_over_bound"]}
+
+
 def run_mx(args, world, rank, local):
     import numpy as np
     import torch
@@ -429,21 +566,13 @@ def run_mx(args, world, rank, local):
     if (args.a_format, args.b_format) != ("e4m3", "e4m3"):
         prob = mx_inputs.with_formats(prob, args.a_format, args.b_format)
     M, N, K = prob.M, prob.N, prob.K
-    out_code = mx.OUT_F32 if prob.out_dtype == "f32" else mx.OUT_BF16
-    tdt = torch.float32 if prob.out_dtype == "f32" else torch.bfloat16
-    flops = 2.0 * M * N * K
-
-    # scales as the run takes them: row-major (the default), or already in
-    # the packed order the tensor cores read (no repack prepass)
     packed = args.scale_layout == "packed"
-    sA = mx_inputs.pack_scales(prob.As) if packed else prob.As
-    sB = mx_inputs.pack_scales(prob.Bs, along_cols=True) if packed else prob.Bs
-    A, As, B, Bs = (t.to(dev) for t in (prob.A, sA, prob.B, sB))
-    C = torch.empty((M, N), dtype=tdt, device=dev)
     props = torch.cuda.get_device_properties(dev)
     l2 = getattr(props, "L2_cache_size", 126 << 20)
     flush = torch.empty(max(2 * l2, 256 << 20), dtype=torch.uint8, device=dev) if not args.no_flush else None
     stream = torch.cuda.current_stream(dev)
+    peak, peak_src = measured_peak()
+    hbm, hbm_src = measured_hbm()
 
     h = mx.mxgemm_create(local)
     if args.mode is not None:
@@ -452,25 +581,22 @@ def run_mx(args, world, rank, local):
     mx.mxgemm_set_option(h, mx.OPT_B_FORMAT, FORMATS.index(args.b_format))
     if packed:
         mx.mxgemm_set_option(h, mx.OPT_SCALE_LAYOUT, mx.SCALES_PACKED)
-
-    def step():
-        if flush is not None:
-            flush.zero_()
-        mx.mxgemm_run(h, M, N, K, A, As, B, Bs, C, 0, out_code, stream)
+    ws = GemmSteps(mx, h, prob, dev, packed, stream)
+    flops = ws.flops
 
     for _ in range(args.warmup):
-        step()
+        if flush is not None:
+            flush.zero_()
+        ws.run()
     torch.cuda.synchronize(dev)
     st, det = mx.mxgemm_get_device_status(h)
     if st != 0:
         raise SystemExit(f"device status {st} detail {det:#x}")
 
-    mk = lambda: torch.cuda.Event(enable_timing=True)
-    s_ev = [(mk(), mk()) for _ in range(args.steps)]
-    k_ev = [(mk(), mk()) for _ in range(args.steps)]
-    for a, b in s_ev + k_ev:  # create the CUDA events (torch creates them lazily)
-        a.record(stream)
-        b.record(stream)
+    s_ev = _events(torch, args.steps)
+    k_ev = [_events(torch, len(ws.calls)) for _ in range(args.steps)]
+    h_ev = _events(torch, args.steps)
+    _prime_events(torch, stream, s_ev + h_ev + [e for k in k_ev for e in k])
     torch.cuda.synchronize(dev)
 
     uuid = None
@@ -481,6 +607,7 @@ def run_mx(args, world, rank, local):
     sampler = ClockSampler(uuid).start()
     launches0 = mx.mxgemm_get_launch_count(h)
 
+    # ---- the timed region: exactly args.steps steps, L2 flushed between them
     barrier(dist)
     torch.cuda.synchronize(dev)
     t_begin = time.perf_counter()
@@ -488,76 +615,135 @@ def run_mx(args, world, rank, local):
         if flush is not None:
             flush.zero_()
         s_ev[i][0].record(stream)
-        mx.mxgemm_run(h, M, N, K, A, As, B, Bs, C, 0, out_code, stream)
+        ws.run()
         s_ev[i][1].record(stream)
     torch.cuda.synchronize(dev)
     barrier(dist)
     t_end = time.perf_counter()
     launches = mx.mxgemm_get_launch_count(h) - launches0
-    sampler.stop()
     st, det = mx.mxgemm_get_device_status(h)
     if st != 0:
         raise SystemExit(f"device status {st} detail {det:#x}")
+    clocks = sampler.summary(t_begin, t_end)
 
     # the GEMM kernel alone, for its roofline: the library records events
-    # around the kernel launch (a second loop, so that the events between the
-    # prepass and the kernel do not disturb the timed steps above)
+    # around each kernel launch (a second loop, so that events between a
+    # prepass and the kernel do not disturb the timed steps above); then the
+    # same steps back to back with no flush (hot L2)
     for i in range(args.steps):
         if flush is not None:
             flush.zero_()
-        mx.mxgemm_set_profile_events(h, k_ev[i][0], k_ev[i][1])
-        mx.mxgemm_run(h, M, N, K, A, As, B, Bs, C, 0, out_code, stream)
+        ws.run(k_events=k_ev[i])
+    for i in range(args.steps):
+        h_ev[i][0].record(stream)
+        ws.run()
+        h_ev[i][1].record(stream)
     torch.cuda.synchronize(dev)
-    mx.mxgemm_set_profile_events(h, None, None)
 
-    step_ms = sum(a.elapsed_time(b) for a, b in s_ev)
-    kern_ms = sum(a.elapsed_time(b) for a, b in k_ev)
-    step_ms_max = max_over_ranks(step_ms, dist, dev)
+    step_list = [a.elapsed_time(b) for a, b in s_ev]
+    kern_list = [sum(a.elapsed_time(b) for a, b in k) for k in k_ev]
+    hot_list = [a.elapsed_time(b) for a, b in h_ev]
+    step_ms_max = max_over_ranks(sum(step_list), dist, dev)
     value = flops * world * args.steps / (step_ms_max * 1e-3) / 1e12
-    kern_avg_ms = kern_ms / args.steps
-    achieved = flops / (kern_avg_ms * 1e-3) / 1e12
-    peak, peak_src = measured_peak()
-    clocks = sampler.summary(t_begin, t_end)
+    kern_avg_ms = sum(kern_list) / len(kern_list)
 
-    # spot parity of the timed result against the oracle (rank 0)
+    # ---- sustained: the same step back to back for a few seconds (the
+    # power-capped rate of a long run; also what a clock sampler needs)
+    sustained = None
+    if args.sustain_s > 0:
+        per = max(statistics.median(hot_list), 1e-3)
+        n_sus = int(max(args.steps, min(200000, args.sustain_s * 1e3 / per)))
+        e0, e1 = _events(torch, 1)[0]
+        torch.cuda.synchronize(dev)
+        ts0 = time.perf_counter()
+        e0.record(stream)
+        for _ in range(n_sus):
+            ws.run()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        ts1 = time.perf_counter()
+        sus_ms = e0.elapsed_time(e1)
+        sustained = {"steps": n_sus, "seconds": sus_ms * 1e-3, "l2": "not flushed (back to back)",
+                     "value": flops * n_sus / (sus_ms * 1e-3) / 1e12, "unit": UNIT,
+                     "frac_of_peak": flops * n_sus / (sus_ms * 1e-3) / 1e12 / peak,
+                     "clocks": sampler.summary(ts0, ts1)}
+        st, det = mx.mxgemm_get_device_status(h)
+        if st != 0:
+            raise SystemExit(f"device status {st} detail {det:#x}")
+
+    # ---- the other workloads: step, kernel and hot-L2 medians, roofline,
+    # spot parity (each workload's own inputs, generated here)
+    table = None
+    if args.workloads != "none" and rank == 0:
+        table = {}
+        names = [n for n in WORKLOAD_TABLE if n != args.workload]
+        for name in names:
+            pw = mx_inputs.WORKLOADS[name]()
+            hw = mx.mxgemm_create(local)
+            try:
+                wsw = GemmSteps(mx, hw, pw, dev, packed, stream)
+                n_steps = max(args.steps, 50) if pw.M * pw.N * pw.K <= (1 << 36) else args.steps
+                step_w, kern_w, hot_w = time_workload(torch, wsw, n_steps, max(args.warmup, 5),
+                                                      flush, dev)
+                st, det = mx.mxgemm_get_device_status(hw)
+                km = statistics.median(kern_w)
+                row = {"M": pw.M, "N": pw.N, "K": pw.K, "calls_per_step": len(wsw.calls),
+                       "out": pw.out_dtype, "steps": n_steps,
+                       "step_us_median": statistics.median(step_w) * 1e3,
+                       "kernel_us_median": km * 1e3,
+                       "hot_l2_step_us_median": statistics.median(hot_w) * 1e3,
+                       "tflops_step": wsw.flops / (statistics.median(step_w) * 1e-3) / 1e12,
+                       "roofline": roofline_of(wsw, km, peak, peak_src, hbm, hbm_src),
+                       "status": st}
+                if not args.no_cpu:
+                    row["parity"] = spot_parity(torch, wsw, args.a_format, args.b_format)
+                table[name] = row
+                del wsw
+            finally:
+                mx.mxgemm_destroy(hw)
+            del pw
+            torch.cuda.empty_cache()
+
+    # spot parity of the headline result against the oracle (rank 0)
     parity = None
     if rank == 0 and not args.no_cpu:
-        import oracle
-        g = np.random.default_rng(1)
-        I, J = g.integers(0, M, 256), g.integers(0, N, 256)
-        ref, bound = oracle.points(prob.A, prob.As, prob.B, prob.Bs, I, J,
-                                   a_fmt=args.a_format, b_fmt=args.b_format)
-        got = C.float().cpu().numpy()[I, J]
-        acc = oracle.accept(got, ref, bound, "f32" if prob.out_dtype == "f32" else "bf16")
-        parity = {"points": int(I.size), "ok": acc["ok"],
-                  "max_err_over_bound": acc["max_err_over_bound"]}
+        parity = spot_parity(torch, ws, args.a_format, args.b_format)
 
-    # end to end through the C interface: pinned host operands in, C out
-    e2e_steps = max(1, min(args.steps, args.e2e_steps))
-    hA, hAs, hB, hBs = (t.contiguous().pin_memory() for t in (prob.A, sA, prob.B, sB))
-    hC = torch.empty((M, N), dtype=tdt).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (hA, hAs, hB, hBs))
-    d2h = hC.numel() * hC.element_size()
-
-    # the host-buffer entry point: B in, then A rows in / C rows out in
-    # slabs overlapped with the slabs' GEMMs; the copies are in the timed
-    # region of every step
-    def e2e_step():
-        mx.mxgemm_run_host(h, M, N, K, hA, hAs, hB, hBs, hC, 0, out_code, stream)
-
-    for _ in range(2):
-        e2e_step()
-    torch.cuda.synchronize(dev)
-    barrier(dist)
-    e0, e1 = mk(), mk()
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
-    e2e_value = flops * world * e2e_steps / (e2e_ms * 1e-3) / 1e12
+    # ---- end to end through the C interface: pinned host operands in, C out
+    e2e = None
+    if args.e2e_steps > 0:
+        e2e_steps = max(1, min(args.steps, args.e2e_steps))
+        sA = mx_inputs.pack_scales(prob.As) if packed else prob.As
+        sB = mx_inputs.pack_scales(prob.Bs, along_cols=True) if packed else prob.Bs
+        hA, hAs, hB, hBs = (t.contiguous().pin_memory() for t in (prob.A, sA, prob.B, sB))
+        hC = torch.empty((M, N), dtype=ws.C.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in (hA, hAs, hB, hBs))
+        d2h = hC.numel() * hC.element_size()
+        ua0 = 1 if prob.use_acc else 0
+        # the host-buffer entry point: B in, then A rows in / C rows out in
+        # slabs overlapped with the slabs' GEMMs; the copies are in the
+        # timed region of every step (one call over the whole K)
+        def e2e_step():
+            mx.mxgemm_run_host(h, M, N, K, hA, hAs, hB, hBs, hC, ua0, ws.out_code, stream)
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        barrier(dist)
+        e0, e1 = _events(torch, 1)[0]
+        e0.record(stream)
+        for _ in range(e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        e2e_ms = max_over_ranks(e0.elapsed_time(e1), dist, dev)
+        if prob.use_acc:
+            h2d += hC.numel() * hC.element_size()  # use_acc: C is copied in as well
+        e2e = {"value": flops * world * e2e_steps / (e2e_ms * 1e-3) / 1e12, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+               "entry_point": "mxgemm_run_host"}
+        del hA, hAs, hB, hBs, hC
     mx.mxgemm_destroy(h)
+    sampler.stop()
 
     cpu = None
     if rank == 0 and not args.no_cpu:
@@ -566,20 +752,8 @@ def run_mx(args, world, rank, local):
                "sample": f"first {rows} of {M} output rows (all {N} columns, K={K}), {dt:.1f} s"}
 
     if rank == 0:
-        # Tensor-bound when the arithmetic intensity is above the ridge
-        # (peak FLOP/s / HBM bytes/s), else HBM-bound: achieved = algorithmic
-        # bytes per launch / kernel time.
-        alg_bytes = M * K + K * N + (M + N) * K // 32 + M * N * (4 if prob.out_dtype == "f32" else 2)
-        hbm, hbm_src = measured_hbm()
-        if 2.0 * M * N * K / alg_bytes >= peak * 1e12 / (hbm * 1e9):
-            roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": UNIT,
-                        "frac": achieved / peak, "peak_source": peak_src}
-        else:
-            gbs = alg_bytes / (kern_avg_ms * 1e-3) / 1e9
-            roofline = {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s",
-                        "frac": gbs / hbm, "peak_source": hbm_src}
-        roofline.update({"traffic": profiled_traffic() if args.workload == WORKLOAD else None,
-                         "algorithmic_bytes": alg_bytes, "kernel": "mxgemm_kernel",
+        roofline = roofline_of(ws, kern_avg_ms, peak, peak_src, hbm, hbm_src)
+        roofline.update({"traffic": profiled_traffic(args.workload), "kernel": "mxgemm_kernel",
                          "kernel_avg_us": kern_avg_ms * 1e3})
         line = {
             "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
@@ -589,19 +763,28 @@ def run_mx(args, world, rank, local):
             "config": {"workload": args.workload, "M": M, "N": N, "K": K,
                        "a": f"{args.a_format.upper()} M x K (K-major), scales E8M0 per 32 K",
                        "b": f"{args.b_format.upper()} K x N (N-major), scales E8M0 per 32 K",
-                       "out": prob.out_dtype, "use_acc": 0, "accumulate": "fp32",
-                       "l2": ("flushed between timed steps (256 MiB write, outside the events)"
+                       "out": prob.out_dtype, "use_acc": int(prob.use_acc),
+                       "calls_per_step": len(ws.calls), "accumulate": "fp32",
+                       "l2": ("flushed between timed steps (write of 2x L2, outside the events)"
                               if flush is not None else "not flushed"),
                        "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
                        "tile_mode": args.mode if args.mode is not None else "auto",
                        "a_format": args.a_format, "b_format": args.b_format,
                        "scale_layout": args.scale_layout},
+            "timing": {"step_us_median": statistics.median(step_list) * 1e3,
+                       "step_us_mean": sum(step_list) / len(step_list) * 1e3,
+                       "kernel_us_median": statistics.median(kern_list) * 1e3,
+                       "kernel_us_mean": kern_avg_ms * 1e3,
+                       "hot_l2_step_us_median": statistics.median(hot_list) * 1e3,
+                       "tflops_step_median": flops / (statistics.median(step_list) * 1e-3) / 1e12,
+                       "tflops_hot_l2_median": flops / (statistics.median(hot_list) * 1e-3) / 1e12},
             "roofline": roofline,
             "cpu_baseline": cpu,
-            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+            "e2e": e2e,
             "gpu_launches": launches,
             "clocks": clocks,
+            "sustained": sustained,
+            "workloads": table,
             "parity": parity,
             "kernel_source_sha": kernel_source_hash(),
         }
@@ -637,6 +820,10 @@ def main(argv=None):
     ap.add_argument("--no-flush", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle baseline and spot parity")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--workloads", default="all", choices=["all", "none"],
+                    help="also measure the other workloads (the 'workloads' object)")
+    ap.add_argument("--sustain-s", type=float, default=3.0,
+                    help="seconds of back-to-back steps for the sustained rate (0: skip)")
     ap.add_argument("--cpu-budget", type=float, default=12.0, help="seconds of oracle work")
     ap.add_argument("--ref-budget", type=float, default=90.0,
                     help="seconds of oracle work for --impl reference")
