@@ -1,4 +1,5 @@
-"""Build step for the CUDA library: one nvcc invocation, sm_103a only.
+"""Build step for the CUDA library: sm_103a only, one nvcc compile per
+translation unit (run in parallel), then one link.
 
     python -m block_scaled_gemm_gb300._build        # (re)build libmxgemm.so
 
@@ -16,14 +17,17 @@ from pathlib import Path
 PKG = Path(__file__).resolve().parent
 ROOT = PKG.parent
 SRC_DIR = PKG / "csrc"
-MAIN_SRC = SRC_DIR / "mxgemm.cu"
+# translation units: the C interface with the tiled kernel, and the
+# skinny-problem kernel
+UNITS = [SRC_DIR / "mxgemm.cu", SRC_DIR / "swapab.cu"]
+OBJ_DIR = PKG / "_build"
 HEADER = ROOT / "include" / "mxgemm.h"
 LIB = PKG / "libmxgemm.so"
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
     "-std=c++17", "-O3", "-lineinfo",
-    "-Xcompiler", "-fPIC", "-shared",
+    "-Xcompiler", "-fPIC",
 ]
 
 
@@ -51,12 +55,26 @@ def needs_build() -> bool:
 def build(force: bool = False, verbose: bool = False) -> Path:
     if not force and not needs_build():
         return LIB
-    tmp = LIB.with_name(f"libmxgemm.so.tmp{os.getpid()}")
-    cmd = [nvcc_path(), *NVCC_FLAGS, "-I", str(ROOT / "include"), "-o", str(tmp), str(MAIN_SRC)]
-    if verbose:
-        cmd.insert(1, "-Xptxas=-v")
-        print(" ".join(cmd), file=sys.stderr)
-    subprocess.run(cmd, check=True)
+    nvcc = nvcc_path()
+    OBJ_DIR.mkdir(exist_ok=True)
+    tag = os.getpid()
+    objs, procs = [], []
+    for src in UNITS:
+        obj = OBJ_DIR / f"{src.stem}.{tag}.o"
+        cmd = [nvcc, *NVCC_FLAGS, "-I", str(ROOT / "include"), "-c", "-o", str(obj), str(src)]
+        if verbose:
+            cmd.insert(1, "-Xptxas=-v")
+            print(" ".join(cmd), file=sys.stderr)
+        objs.append(obj)
+        procs.append((cmd, subprocess.Popen(cmd)))
+    failed = [cmd for cmd, pr in procs if pr.wait() != 0]
+    if failed:
+        raise subprocess.CalledProcessError(1, failed[0])
+    tmp = LIB.with_name(f"libmxgemm.so.tmp{tag}")
+    subprocess.run([nvcc, "-shared", "-Xcompiler", "-fPIC", "-o", str(tmp), *map(str, objs)],
+                   check=True)
+    for obj in objs:
+        obj.unlink()
     os.replace(tmp, LIB)
     return LIB
 

@@ -21,6 +21,8 @@
 #include "mxgemm_kernel.cuh"
 #include "prepass.cuh"
 #include "quantize.cuh"
+#include "swapab.h"
+#include "swapab_kernel.cuh"
 
 namespace {
 
@@ -56,6 +58,11 @@ struct Plan {
   int blocks_a = 0, blocks_b = 0;
   int units = 0;     // persistent CTAs (pairs) of the GEMM grid
   bool repack = false;  // pairs: the scale chunks come from the repack prepass
+  // skinny problems (M <= 128) computed transposed by mxgemm_swapab_kernel
+  bool swap = false;
+  CUtensorMap tAt, tSBs, tSAs;  // A rows (MMA B operand), scale staging maps
+  mxg::SwapParams swp;
+  int swap_grid = 0;
 
   bool matches(int64_t M_, int64_t N_, int64_t K_, const void *A_, const void *As_, const void *B_,
                const void *Bs_, void *C_, int ua, int od, int md, int sl, int sc, int sk_,
@@ -103,6 +110,7 @@ struct mxgemm_ctx {
   int a_fmt = 0, b_fmt = 0;  // element formats (mxgemm_format_t)
   int scale_layout = MXGEMM_SCALES_ROW_MAJOR;
   bool attr_set[3][8] = {};
+  bool swap_attr[4][4] = {};
   cudaEvent_t prof_before = nullptr;
   cudaEvent_t prof_after = nullptr;
   int64_t launches = 0;
@@ -456,6 +464,135 @@ int build_plan(mxgemm_ctx *h, Plan *pl, int64_t M, int64_t N, int64_t K, const v
   return MXGEMM_OK;
 }
 
+// Skinny problems (M <= 128, 8-bit element formats): C^T = B^T x A^T on
+// mxgemm_swapab_kernel, one CTA per (128-column block of N, K split), the
+// K splits of a block reduced inside their cluster.  The only workspace is a
+// re-pitched B when N % 16 != 0.
+int run_swapab(mxgemm_ctx *h, int64_t M, int64_t N, int64_t K, const void *A, const void *A_scale,
+               const void *B, const void *B_scale, void *C, int use_acc, int out_dtype,
+               bool packed, cudaStream_t stream) {
+  const int64_t k_steps = cdiv(K, 128);
+  const int64_t nblk = cdiv(N, 128);
+  const bool pad_b = (N % 16) != 0;
+  const int64_t npad = round_up(static_cast<size_t>(N), 16);
+  const size_t ws_bytes = pad_b ? round_up(static_cast<size_t>(K) * npad, 1024) : 0;
+
+  Plan *plan = nullptr;
+  for (Plan &pl : h->plans)
+    if (pl.matches(M, N, K, A, A_scale, B, B_scale, C, use_acc, out_dtype, h->mode,
+                   h->stall_producer, h->scheduler, h->stream_k, h->timeout_ns, h->ws.ptr,
+                   h->a_fmt * 8 + h->b_fmt, h->scale_layout) &&
+        pl.swap && h->ws.bytes >= ws_bytes) {
+      plan = &pl;
+      break;
+    }
+  if (!plan) {
+    if (!on_device(C, h->device) || !on_device(A, h->device) || !on_device(B, h->device) ||
+        !on_device(A_scale, h->device) || !on_device(B_scale, h->device))
+      return MXGEMM_ERR_INVALID_VALUE;
+    int st = ensure_workspace(h, ws_bytes, stream);
+    if (st != MXGEMM_OK) return st;
+    plan = &h->plans[h->next_plan];
+    h->next_plan = (h->next_plan + 1) % kPlanCache;
+    Plan &pl = *plan;
+    pl.valid = false;
+    const int nt = mxg::swapab_class(static_cast<int>(M));
+    const int nm = static_cast<int>(round_up(static_cast<size_t>(M), 16));
+    // K splits: enough CTAs per column block to cover the SMs when the
+    // blocks alone do not, within one cluster (at most 8, and what the
+    // first CTA's shared memory can receive), at least 4 K steps each
+    int64_t splits = 1;
+    if (nblk < h->sm_count) {
+      splits = h->sm_count / nblk;
+      splits = std::min<int64_t>(splits, mxg::swapab_max_splits(nt));
+      splits = std::min<int64_t>(splits, std::max<int64_t>(1, k_steps / 4));
+      splits = std::max<int64_t>(splits, 1);
+    }
+    const int64_t kb = K / 32;
+    const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
+    const void *bsrc = pad_b ? static_cast<const void *>(h->ws.ptr) : B;
+    const int64_t bpitch = pad_b ? npad : N;
+    const bool scale_tma = !packed && kb % 16 == 0 &&
+                           reinterpret_cast<uintptr_t>(A_scale) % 16 == 0 &&
+                           reinterpret_cast<uintptr_t>(B_scale) % 16 == 0;
+    std::memset(&pl.tSBs, 0, sizeof(pl.tSBs));
+    std::memset(&pl.tSAs, 0, sizeof(pl.tSAs));
+    // B: 128 columns x 128 K rows per box (the MMA's A operand, M-major);
+    // A: 128 K bytes x nm rows (the MMA's B operand, K-major), rows past M
+    // filled with zero
+    if (encode_2d(h, &pl.tB, u8, bsrc, N, K, bpitch, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        encode_2d(h, &pl.tAt, u8, A, K, M, K, 128, static_cast<uint32_t>(nm),
+                  CU_TENSOR_MAP_SWIZZLE_128B))
+      return MXGEMM_ERR_CUDA;
+    // 16-byte row segments (four K steps) of the block's 128 B_scale rows and
+    // of the nm A_scale rows
+    if (scale_tma &&
+        (encode_2d(h, &pl.tSBs, u8, B_scale, kb, N, kb, 16, 128, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+         encode_2d(h, &pl.tSAs, u8, A_scale, kb, M, kb, 16, static_cast<uint32_t>(nm),
+                   CU_TENSOR_MAP_SWIZZLE_NONE)))
+      return MXGEMM_ERR_CUDA;
+    mxg::SwapParams &p = pl.swp;
+    std::memset(&p, 0, sizeof(p));
+    p.M = static_cast<int>(M);
+    p.N = static_cast<int>(N);
+    p.K = static_cast<int>(K);
+    p.nm = nm;
+    p.k_steps = static_cast<int>(k_steps);
+    p.splits = static_cast<int>(splits);
+    p.C = C;
+    p.use_acc = use_acc;
+    p.status = h->d_status;
+    p.timeout_ns = static_cast<unsigned long long>(h->timeout_ns);
+    p.stall_producer = h->stall_producer;
+    // the MMA's A operand is B and its B operand is A: their formats swap
+    p.idesc_fmt = (mxg::mma_format_code(h->b_fmt) << 7) | (mxg::mma_format_code(h->a_fmt) << 10);
+    p.a_scale = static_cast<const uint8_t *>(A_scale);
+    p.b_scale = static_cast<const uint8_t *>(B_scale);
+    p.kb_count = static_cast<int>(kb);
+    p.scale_tma = scale_tma ? 1 : 0;
+    p.packed = packed ? 1 : 0;
+    p.a_chunks = static_cast<const uint8_t *>(A_scale);
+    p.b_chunks = static_cast<const uint8_t *>(B_scale);
+    pl.swap = true;
+    pl.swap_grid = static_cast<int>(nblk * splits);
+    pl.CG = 1;
+    pl.pad_b = pad_b;
+    pl.npad = npad;
+    pl.a_bits = 8;
+    pl.b_bits = 8;
+    pl.repack = false;
+    pl.M = M; pl.N = N; pl.K = K;
+    pl.A = A; pl.As = A_scale; pl.B = B; pl.Bs = B_scale; pl.C = C;
+    pl.use_acc = use_acc; pl.out_dtype = out_dtype; pl.mode = h->mode;
+    pl.stall = h->stall_producer; pl.sched = h->scheduler; pl.sk = h->stream_k;
+    pl.timeout_ns = h->timeout_ns;
+    pl.fmts = h->a_fmt * 8 + h->b_fmt;
+    pl.layout = packed ? MXGEMM_SCALES_PACKED : MXGEMM_SCALES_ROW_MAJOR;
+    pl.ws = h->ws.ptr;
+    pl.valid = true;
+  }
+  if (plan->pad_b) {
+    mxg::pad_rows_kernel<<<launch_blocks(K * (plan->npad / 16), 256), 256, 0, stream>>>(
+        static_cast<const uint8_t *>(B), K, N, plan->npad, h->ws.ptr, 8);
+    ++h->launches;
+    if (cudaGetLastError() != cudaSuccess) return MXGEMM_ERR_CUDA;
+  }
+  if (h->prof_before && cudaEventRecord(h->prof_before, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return MXGEMM_ERR_CUDA;
+  }
+  const int st = mxg::swapab_launch(plan->tB, plan->tAt, plan->tSBs, plan->tSAs, plan->swp,
+                                    out_dtype == MXGEMM_OUT_BF16, plan->swap_grid, stream,
+                                    h->swap_attr);
+  if (st != MXGEMM_OK) return st;
+  ++h->launches;
+  if (h->prof_after && cudaEventRecord(h->prof_after, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return MXGEMM_ERR_CUDA;
+  }
+  return MXGEMM_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -538,7 +675,7 @@ int mxgemm_set_option(mxgemm_handle_t h, int option, int64_t value) {
   if (!h) return MXGEMM_ERR_INVALID_VALUE;
   switch (option) {
     case MXGEMM_OPT_MODE:
-      if (value < 0 || value > 2) return MXGEMM_ERR_INVALID_VALUE;
+      if (value < 0 || value > 3) return MXGEMM_ERR_INVALID_VALUE;
       h->mode = static_cast<int>(value);
       return MXGEMM_OK;
     case MXGEMM_OPT_WAIT_TIMEOUT_NS:
@@ -600,6 +737,20 @@ int mxgemm_run(mxgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A
   if (reinterpret_cast<uintptr_t>(A) % 16 || reinterpret_cast<uintptr_t>(B) % 16)
     return MXGEMM_ERR_MISALIGNED;
 
+  // Skinny problems: the transposed kernel, automatically for M <= 128 with
+  // 8-bit element formats, or on request (MXGEMM_OPT_MODE = 3)
+  {
+    const bool sub_byte = h->a_fmt >= MXGEMM_FMT_E2M3 || h->b_fmt >= MXGEMM_FMT_E2M3;
+    const bool swap_ok = M <= 128 && !sub_byte;
+    if (h->mode == 3 && !swap_ok) return MXGEMM_ERR_INVALID_VALUE;
+    if (h->mode == 3 || (h->mode == 0 && swap_ok)) {
+      const bool pk = h->scale_layout == MXGEMM_SCALES_PACKED;
+      if (pk && (reinterpret_cast<uintptr_t>(A_scale) % 16 || reinterpret_cast<uintptr_t>(B_scale) % 16))
+        return MXGEMM_ERR_MISALIGNED;
+      return run_swapab(h, M, N, K, A, A_scale, B, B_scale, C, use_acc, out_dtype, pk, stream);
+    }
+  }
+
   // workspace size depends only on the shape and mode
   int CG = 1;
   if (h->mode == 2) CG = 2;
@@ -646,7 +797,7 @@ int mxgemm_run(mxgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A
     if (pl.matches(M, N, K, A, A_scale, B, B_scale, C, use_acc, out_dtype, h->mode,
                    h->stall_producer, h->scheduler, h->stream_k, h->timeout_ns, h->ws.ptr,
                    h->a_fmt * 8 + h->b_fmt, h->scale_layout) &&
-        h->ws.bytes >= ws_bytes) {
+        !pl.swap && h->ws.bytes >= ws_bytes) {
       plan = &pl;
       break;
     }
@@ -659,6 +810,7 @@ int mxgemm_run(mxgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A
     plan = &h->plans[h->next_plan];
     h->next_plan = (h->next_plan + 1) % kPlanCache;
     plan->valid = false;
+    plan->swap = false;
     st = build_plan(h, plan, M, N, K, A, A_scale, B, B_scale, C, use_acc, out_dtype, CG, m_tiles,
                     n_tiles, k_steps, num_tiles, a_chunks, b_chunks, pad_b, npad, sp, z, a_bits,
                     b_bits, fused, packed);

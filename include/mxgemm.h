@@ -75,9 +75,16 @@ typedef enum {
 
 /* Options for mxgemm_set_option. */
 typedef enum {
-  /* Tile mode: 0 = automatic (CTA pair when M > 128, else one CTA), 1 = one
-   * CTA per 128x256 tile, 2 = CTA pair (cta_group::2) per 256x256 tile.
-   * Default 0. */
+  /* Tile mode: 0 = automatic (the transposed kernel of mode 3 when M <= 128
+   * and both element formats are 8-bit, else a CTA pair when M > 128, else
+   * one CTA), 1 = one CTA per 128x256 tile, 2 = CTA pair (cta_group::2) per
+   * 256x256 tile, 3 = the transposed kernel for few rows: C^T = B^T x A^T
+   * with 128 columns of B on the tensor cores' 128-row side and the M rows
+   * of A as the MMA's N (M rounded up to 16), K split over a cluster of up
+   * to 8 CTAs whose partials are added in shared memory in a fixed order;
+   * needs M <= 128 and E4M3 / E5M2 operands (else a run returns
+   * MXGEMM_ERR_INVALID_VALUE); the options SCHEDULER and STREAM_K do not
+   * apply to it.  Default 0. */
   MXGEMM_OPT_MODE = 1,
   /* Device-side wait limit in nanoseconds (default 2e9).  A wait that runs
    * out sets MXGEMM_ERR_TIMEOUT and the kernel drains and returns. */
@@ -296,8 +303,8 @@ int mxgemm_destroy(mxgemm_handle_t h);
  * must not allocate after start-up (an allocation there can fail, block on
  * other streams or fragment the caller's pool).  It takes no handle,
  * allocates nothing (no cudaMalloc, cudaFree or allocating library call) and
- * runs on the current device and the given stream.  Neither the paper nor
- * the pages it draws on have a counterpart to this entry point.
+ * runs on the current device and the given stream.  The pages have no
+ * counterpart to this entry point.
  *
  * Scratch: B re-pitched to a 16-byte row pitch when N % 16 != 0 goes to one
  * file-scope device array of 16 MiB, which every GPU that loads this library

@@ -341,10 +341,12 @@ def test_clc_scheduler_full_check(h, mode):
 @pytest.mark.parametrize("M", [1, 16, 100, 128])
 @pytest.mark.parametrize("out_dtype,use_acc", [("f32", False), ("bf16", True)])
 def test_skinny_split_k(h, M, out_dtype, use_acc):
-    # At most 128 rows and fewer tiles than CTAs: every tile's K steps are
-    # split over all CTAs, with partial sums of the valid rows only.  Full
-    # check against the oracle, and against whole tiles (tail balancing off).
-    _mode(h, 0)
+    # The tiled single-CTA path (mode 1; automatic mode takes the transposed
+    # kernel for these shapes) with at most 128 rows and fewer tiles than
+    # CTAs: every tile's K steps are split over all CTAs, with partial sums
+    # of the valid rows only.  Full check against the oracle, and against
+    # whole tiles (tail balancing off).
+    _mode(h, 1)
     p = mi.random_problem(M, 2304, 2048, seed=101 + M, kind="normal", out_dtype=out_dtype)
     cin = mi.c_init(M, p.N, 101, out_dtype) if use_acc else None
     ref, bound = oracle.rows(p.A, p.As, p.B, p.Bs,
@@ -387,14 +389,15 @@ def test_plan_cache_churn_and_workspace_growth(h):
         assert res["ok"], f"{p.name}: {res}"
 
 
-@pytest.mark.parametrize("mode,M", [(1, 300), (2, 300), (0, 100)])
+@pytest.mark.parametrize("mode,M", [(1, 300), (2, 300), (1, 100), (0, 100)])
 @pytest.mark.parametrize("K", [1024, 384, 160])
 def test_scales_at_unaligned_addresses(h, mode, M, K):
     # A_scale and B_scale one byte past a 16-byte boundary: the scale chunks
     # are built from byte loads instead of 16-byte ones (M = 300: the repack,
-    # for single CTAs and pairs; M = 100: the kernel's scale loader, whose
-    # rows are also read byte by byte when K % 512 != 0); the result is the
-    # same, bit for bit
+    # for single CTAs and pairs; M = 100, mode 1: the tiled kernel's scale
+    # loader, mode 0: the transposed kernel's scale builder, both reading
+    # rows byte by byte also when K % 512 != 0); the result is the same, bit
+    # for bit
     _mode(h, mode)
     p = mi.random_problem(M, 520, K, seed=K + mode + M, kind="normal")
     ref_c = gu.run_gpu(h, p).cpu()
