@@ -58,6 +58,7 @@ struct Plan {
   int blocks_a = 0, blocks_b = 0;
   int units = 0;     // persistent CTAs (pairs) of the GEMM grid
   bool repack = false;  // pairs: the scale chunks come from the repack prepass
+  bool repack_lite = false;  // ... by repack_scales_lite_kernel
   // skinny problems (M <= 128) computed transposed by mxgemm_swapab_kernel
   bool swap = false;
   CUtensorMap tAt, tSBs, tSAs;  // A rows (MMA B operand), scale staging maps
@@ -445,6 +446,12 @@ int build_plan(mxgemm_ctx *h, Plan *pl, int64_t M, int64_t N, int64_t K, const v
   kp.kb_count = static_cast<int>(kb);
   kp.fused_scales = fused ? 1 : 0;
   kp.scale_tma = scale_tma ? 1 : 0;
+  // The light repack (beside the GEMM's CTAs) needs 16-byte scale rows;
+  // its GEMM then sends its first A and B loads before waiting for it.
+  pl->repack_lite = pl->repack && kb % 16 == 0 &&
+                    reinterpret_cast<uintptr_t>(A_scale) % 16 == 0 &&
+                    reinterpret_cast<uintptr_t>(B_scale) % 16 == 0;
+  kp.early_ab = pl->repack_lite ? 1 : 0;
   pl->units = sp.units;
   pl->CG = CG;
   pl->pad_b = pad_b;
@@ -828,7 +835,14 @@ int mxgemm_run(mxgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A
         static_cast<const uint8_t *>(A), M, K, K, h->ws.ptr + plan->off_a, plan->a_bits);
     ++h->launches;
   }
-  if (plan->repack) {
+  if (plan->repack_lite) {
+    // one CTA per SM at most, so that each fits beside a GEMM CTA
+    const int units = plan->blocks_a + plan->blocks_b;
+    const int grid = std::max(1, std::min((units + 1) / 2, h->sm_count));
+    mxg::repack_scales_lite_kernel<<<grid, mxg::kRepackLiteThreads, 0, stream>>>(plan->ra, plan->rb,
+                                                                               plan->blocks_a, units);
+    h->launches += 1;
+  } else if (plan->repack) {
     mxg::repack_scales_kernel<<<plan->blocks_a + plan->blocks_b, mxg::kRepackThreads, 0, stream>>>(
         plan->ra, plan->rb, plan->blocks_a);
     h->launches += 1;

@@ -150,6 +150,12 @@ struct KParams {
   // scales (16-byte row pitch and base) and the scale loader stages its rows
   // by TMA; else it loads them with per-lane loads
   int scale_tma;
+  // The launch before this one is the library's scale repack, which waited
+  // for all earlier work on the stream: A and B are complete, and only the
+  // scale chunks depend on that launch.  The producers of CTA pairs then send
+  // the first ring round's A and B loads before the programmatic-dependent-
+  // launch wait, and its chunk loads after it.
+  int early_ab;
 };
 
 // Instruction descriptor of tcgen05.mma.kind::mxf8f6f4.block_scale:
@@ -502,8 +508,9 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
   // The set-up above overlaps the tail of the prepass before the kernel, if
   // any (the scale repack, the B re-pitch; programmatic dependent
   // launch); nothing below reads or writes global memory before that grid
-  // has finished.
-  griddep_wait();
+  // has finished, except the producer's early A and B loads (early_ab),
+  // whose warp waits for it itself.
+  if (!(p.early_ab && warp == 0)) griddep_wait();
 
   const WaitCtl wc{p.status, abort_flag, p.timeout_ns};
   // Barriers completed by TMA byte counts or tcgen05.commit arrivals are
@@ -583,12 +590,54 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
           tma_load_2d_pair(sSB, &tmSFB, 0, (nt * p.k_steps + ks) * 8, fbl);
         }
       };
+      // early_ab: the first ring round's A and B go out before the wait for
+      // the scale repack, its chunks after (pairs whose first item is a
+      // whole tile with more K steps than the ring has stages); otherwise the
+      // wait comes first.
+      int pre = 0;  // stages of the first ring round filled here
+      if (p.early_ab) {
+        if (CG == 2 && ok && w.ke - w.kb > C::STAGES) {
+          const int row0 = mt * (128 * CG) + 128 * (int)rank;
+          const int mblk = mt * CG + (int)rank;
+          for (int st = 0; st < C::STAGES; ++st) {
+            if (leader) {
+              const uint32_t fb = bar_full + 8 * st;
+              if (rank == 0) mbar_arrive_expect_tx(fb, C::STAGE_TX);
+              const uint32_t fbl = mapa_shared(fb, 0);
+              tma_load_2d_pair(base + C::OFF_A + st * C::A_BYTES, &tmA, (w.kb + st) * 128, row0, fbl);
+              tma_load_2d_pair(base + C::OFF_B + st * C::B_BYTES, &tmB, nt * 256 + 128 * (int)rank,
+                               (w.kb + st) * 128, fbl);
+            }
+            __syncwarp();
+          }
+          griddep_wait();
+          for (int st = 0; st < C::STAGES; ++st) {
+            if (leader) {
+              const uint32_t fbl = mapa_shared(bar_full + 8 * st, 0);
+              tma_load_2d_pair(base + C::OFF_SFA + st * C::SFA_BYTES, &tmSFA, 0,
+                               (mblk * p.k_steps + w.kb + st) * 4, fbl);
+              tma_load_2d_pair(base + C::OFF_SFB + st * C::SFB_BYTES, &tmSFB, 0,
+                               (nt * p.k_steps + w.kb + st) * 8, fbl);
+            }
+            __syncwarp();
+          }
+          pre = C::STAGES;
+          ks = w.kb + C::STAGES;
+        } else {
+          griddep_wait();
+        }
+      }
       if constexpr (CG == 2) {
         // Pairs: the unrolled loop holds only the per-step work; a stage
         // that is not free yet, or a tile boundary, is handled after it
         // (measured faster for pairs; slower for single CTAs, whose 4-stage
         // ring is refilled late by the extra exit and re-entry).
         int skip = 0;  // stages of the current ring round already filled
+        if (pre == C::STAGES) {  // the first ring round went out above
+          phase = 1u;
+          nst = 0;
+          nph = 1u;
+        }
         while (ok) {
           bool tile_end = false, must_wait = false;
 #pragma unroll

@@ -80,6 +80,50 @@ __global__ void __launch_bounds__(kRepackThreads)
   }
 }
 
+// The same repack by a light kernel that fits beside a GEMM CTA on one SM
+// (256 threads, at most 40 registers, no shared memory), so that the GEMM
+// launched after it with programmatic dependent launch becomes resident at
+// once and sends its first operand loads while this runs.  Units (a unit:
+// 128 rows x 16 K steps of one operand, the block of repack_scales_kernel;
+// units [0, units0) are A's) go two per round: thread t takes row t % 128 of
+// unit 2 * (round index) + t / 128, reads the row's 16 K steps (16-byte
+// loads, 127 for rows past the matrix) and writes each step's 4 bytes to
+// word (r % 32) * 4 + r / 32 of that step's chunk.  Needs 16-byte aligned
+// scale rows (K % 512 == 0, aligned bases).
+constexpr int kRepackLiteThreads = 256;
+
+__global__ void __launch_bounds__(kRepackLiteThreads, 6)
+    repack_scales_lite_kernel(RepackArgs a0, RepackArgs a1, int units0, int units) {
+  griddep_launch_dependents();
+  const int t = threadIdx.x;
+  const int r = t & 127;
+  const int word = (r & 31) * 4 + (r >> 5);
+  for (int u = 2 * static_cast<int>(blockIdx.x) + (t >> 7); u < units; u += 2 * static_cast<int>(gridDim.x)) {
+    const bool second = u >= units0;
+    const RepackArgs &a = second ? a1 : a0;
+    const int b = second ? u - units0 : u;
+    const int rb = b / a.kgroups, kg = b - rb * a.kgroups;
+    const int64_t row = static_cast<int64_t>(rb) * 128 + r;
+    const int n = min(16, a.k_steps - kg * 16);
+    const uint4 *src = reinterpret_cast<const uint4 *>(a.S + row * a.kb_count + kg * 64);
+    uint4 seg[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q)
+      seg[q] = (4 * q < n && row < a.rows) ? __ldg(src + q)
+                                           : make_uint4(0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu, 0x7F7F7F7Fu);
+    const int tile_idx = rb / a.atoms, at = rb - tile_idx * a.atoms;
+    uint32_t *out = a.out + ((static_cast<int64_t>(tile_idx) * a.k_steps + kg * 16) * a.atoms + at) * 128 + word;
+    const int64_t stride = static_cast<int64_t>(a.atoms) * 128;
+#pragma unroll
+    for (int k = 0; k < 16; ++k) {
+      if (k < n) {
+        const uint4 &x = seg[k >> 2];
+        out[k * stride] = (k & 3) == 0 ? x.x : (k & 3) == 1 ? x.y : (k & 3) == 2 ? x.z : x.w;
+      }
+    }
+  }
+}
+
 // Re-pitch the rows of an operand into the workspace: `rows` rows of `N`
 // one-byte elements become rows of `Npad` bytes (a multiple of 16, for the
 // 16-byte stride rule of tensor-map loads; the pad columns are zero).  With
