@@ -426,7 +426,7 @@ class GemmSteps:
     mxgemm_run, or the chained use_acc calls of a K-split workload), with
     device operands prepared once."""
 
-    def __init__(self, mx, h, prob, dev, packed: bool, stream):
+    def __init__(self, mx, h, prob, dev, packed: bool, stream, elems_packed: bool = False):
         import torch
         import mx_inputs
         self.mx, self.h, self.prob, self.stream = mx, h, prob, stream
@@ -441,6 +441,14 @@ class GemmSteps:
             if packed:
                 As = mx_inputs.pack_scales(As)
                 Bs = mx_inputs.pack_scales(Bs, along_cols=True)
+            if elems_packed:
+                # 6- and 4-bit operands handed over in the tensor cores'
+                # packed form (a host-side layout change, outside the step)
+                fa, fb = prob.meta.get("formats", ("e4m3", "e4m3"))
+                if mx_inputs.FORMAT_BITS[fa] < 8:
+                    A = mx_inputs.pack_elements(A, mx_inputs.FORMAT_BITS[fa])
+                if mx_inputs.FORMAT_BITS[fb] < 8:
+                    B = mx_inputs.pack_elements(B, mx_inputs.FORMAT_BITS[fb])
             t = [x.to(dev) for x in (A, As, B, Bs)]
             self.keep.append(t)
             # a K-split workload accumulates every call into C (use_acc)
@@ -579,9 +587,12 @@ def run_mx(args, world, rank, local):
         mx.mxgemm_set_option(h, mx.OPT_MODE, args.mode)
     mx.mxgemm_set_option(h, mx.OPT_A_FORMAT, FORMATS.index(args.a_format))
     mx.mxgemm_set_option(h, mx.OPT_B_FORMAT, FORMATS.index(args.b_format))
+    elems_packed = args.element_layout == "packed"
+    if elems_packed:
+        mx.mxgemm_set_option(h, mx.OPT_ELEMENT_LAYOUT, mx.ELEMS_PACKED)
     if packed:
         mx.mxgemm_set_option(h, mx.OPT_SCALE_LAYOUT, mx.SCALES_PACKED)
-    ws = GemmSteps(mx, h, prob, dev, packed, stream)
+    ws = GemmSteps(mx, h, prob, dev, packed, stream, elems_packed)
     flops = ws.flops
 
     for _ in range(args.warmup):
@@ -715,7 +726,13 @@ def run_mx(args, world, rank, local):
         e2e_steps = max(1, min(args.steps, args.e2e_steps))
         sA = mx_inputs.pack_scales(prob.As) if packed else prob.As
         sB = mx_inputs.pack_scales(prob.Bs, along_cols=True) if packed else prob.Bs
-        hA, hAs, hB, hBs = (t.contiguous().pin_memory() for t in (prob.A, sA, prob.B, sB))
+        eA, eB = prob.A, prob.B
+        if elems_packed:
+            if mx_inputs.FORMAT_BITS[args.a_format] < 8:
+                eA = mx_inputs.pack_elements(eA, mx_inputs.FORMAT_BITS[args.a_format])
+            if mx_inputs.FORMAT_BITS[args.b_format] < 8:
+                eB = mx_inputs.pack_elements(eB, mx_inputs.FORMAT_BITS[args.b_format])
+        hA, hAs, hB, hBs = (t.contiguous().pin_memory() for t in (eA, sA, eB, sB))
         hC = torch.empty((M, N), dtype=ws.C.dtype).pin_memory()
         h2d = sum(t.numel() * t.element_size() for t in (hA, hAs, hB, hBs))
         d2h = hC.numel() * hC.element_size()
@@ -770,7 +787,7 @@ def run_mx(args, world, rank, local):
                        "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
                        "tile_mode": args.mode if args.mode is not None else "auto",
                        "a_format": args.a_format, "b_format": args.b_format,
-                       "scale_layout": args.scale_layout},
+                       "scale_layout": args.scale_layout, "element_layout": args.element_layout},
             "timing": {"step_us_median": statistics.median(step_list) * 1e3,
                        "step_us_mean": sum(step_list) / len(step_list) * 1e3,
                        "kernel_us_median": statistics.median(kern_list) * 1e3,
@@ -817,6 +834,9 @@ def main(argv=None):
     ap.add_argument("--scale-layout", default="row-major", choices=["row-major", "packed"],
                     help="scales row-major (the workload's form; the run repacks them) or "
                          "pre-packed in the tensor cores' order (as mxgemm_quantize_ex writes them)")
+    ap.add_argument("--element-layout", default="byte", choices=["byte", "packed"],
+                    help="6- and 4-bit operands one code per byte (packed by the library each "
+                         "call) or already in the tensor cores' packed form")
     ap.add_argument("--no-flush", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle baseline and spot parity")
     ap.add_argument("--e2e-steps", type=int, default=20)

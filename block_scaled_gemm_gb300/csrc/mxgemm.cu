@@ -110,6 +110,7 @@ struct mxgemm_ctx {
   int stream_k = 1;
   int a_fmt = 0, b_fmt = 0;  // element formats (mxgemm_format_t)
   int scale_layout = MXGEMM_SCALES_ROW_MAJOR;
+  int elem_layout = MXGEMM_ELEMS_BYTE;
   bool attr_set[3][8] = {};
   bool swap_attr[4][4] = {};
   cudaEvent_t prof_before = nullptr;
@@ -464,7 +465,7 @@ int build_plan(mxgemm_ctx *h, Plan *pl, int64_t M, int64_t N, int64_t K, const v
   pl->use_acc = use_acc; pl->out_dtype = out_dtype; pl->mode = h->mode;
   pl->stall = h->stall_producer; pl->sched = h->scheduler; pl->sk = h->stream_k;
   pl->timeout_ns = h->timeout_ns;
-  pl->fmts = h->a_fmt * 8 + h->b_fmt;
+  pl->fmts = h->a_fmt * 8 + h->b_fmt + 64 * h->elem_layout;
   pl->layout = packed ? MXGEMM_SCALES_PACKED : MXGEMM_SCALES_ROW_MAJOR;
   pl->ws = h->ws.ptr;
   pl->valid = true;
@@ -488,7 +489,7 @@ int run_swapab(mxgemm_ctx *h, int64_t M, int64_t N, int64_t K, const void *A, co
   for (Plan &pl : h->plans)
     if (pl.matches(M, N, K, A, A_scale, B, B_scale, C, use_acc, out_dtype, h->mode,
                    h->stall_producer, h->scheduler, h->stream_k, h->timeout_ns, h->ws.ptr,
-                   h->a_fmt * 8 + h->b_fmt, h->scale_layout) &&
+                   h->a_fmt * 8 + h->b_fmt + 64 * h->elem_layout, h->scale_layout) &&
         pl.swap && h->ws.bytes >= ws_bytes) {
       plan = &pl;
       break;
@@ -573,7 +574,7 @@ int run_swapab(mxgemm_ctx *h, int64_t M, int64_t N, int64_t K, const void *A, co
     pl.use_acc = use_acc; pl.out_dtype = out_dtype; pl.mode = h->mode;
     pl.stall = h->stall_producer; pl.sched = h->scheduler; pl.sk = h->stream_k;
     pl.timeout_ns = h->timeout_ns;
-    pl.fmts = h->a_fmt * 8 + h->b_fmt;
+    pl.fmts = h->a_fmt * 8 + h->b_fmt + 64 * h->elem_layout;
     pl.layout = packed ? MXGEMM_SCALES_PACKED : MXGEMM_SCALES_ROW_MAJOR;
     pl.ws = h->ws.ptr;
     pl.valid = true;
@@ -711,6 +712,10 @@ int mxgemm_set_option(mxgemm_handle_t h, int option, int64_t value) {
         return MXGEMM_ERR_INVALID_VALUE;
       h->scale_layout = static_cast<int>(value);
       return MXGEMM_OK;
+    case MXGEMM_OPT_ELEMENT_LAYOUT:
+      if (value != MXGEMM_ELEMS_BYTE && value != MXGEMM_ELEMS_PACKED) return MXGEMM_ERR_INVALID_VALUE;
+      h->elem_layout = static_cast<int>(value);
+      return MXGEMM_OK;
     default:
       return MXGEMM_ERR_INVALID_VALUE;
   }
@@ -784,8 +789,12 @@ int mxgemm_run(mxgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A
   const int64_t a_chunks = fused || packed ? 0 : m_tiles * CG * k_steps;
   const int64_t b_chunks = fused || packed ? 0 : n_tiles * k_steps * 2;  // 2 per 256 columns
   // 6- and 4-bit formats are packed 16 elements per 16-byte group first
-  const int a_bits = h->a_fmt == MXGEMM_FMT_E2M1 ? 4 : h->a_fmt >= MXGEMM_FMT_E2M3 ? 6 : 8;
-  const int b_bits = h->b_fmt == MXGEMM_FMT_E2M1 ? 4 : h->b_fmt >= MXGEMM_FMT_E2M3 ? 6 : 8;
+  // (with MXGEMM_ELEMS_PACKED they arrive in that form and are read as
+  // they are: whole 16-element groups, so N % 16 == 0 for a sub-byte B)
+  const bool elems_packed = h->elem_layout == MXGEMM_ELEMS_PACKED;
+  if (elems_packed && h->b_fmt >= MXGEMM_FMT_E2M3 && N % 16 != 0) return MXGEMM_ERR_INVALID_VALUE;
+  const int a_bits = elems_packed ? 8 : h->a_fmt == MXGEMM_FMT_E2M1 ? 4 : h->a_fmt >= MXGEMM_FMT_E2M3 ? 6 : 8;
+  const int b_bits = elems_packed ? 8 : h->b_fmt == MXGEMM_FMT_E2M1 ? 4 : h->b_fmt >= MXGEMM_FMT_E2M3 ? 6 : 8;
   const bool pad_b = (N % 16) != 0 || b_bits < 8;
   const int64_t npad = round_up(static_cast<size_t>(N), 16);
   // Cluster launch control: one cluster per work item (whole tiles, then
@@ -803,7 +812,7 @@ int mxgemm_run(mxgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A
   for (Plan &pl : h->plans)
     if (pl.matches(M, N, K, A, A_scale, B, B_scale, C, use_acc, out_dtype, h->mode,
                    h->stall_producer, h->scheduler, h->stream_k, h->timeout_ns, h->ws.ptr,
-                   h->a_fmt * 8 + h->b_fmt, h->scale_layout) &&
+                   h->a_fmt * 8 + h->b_fmt + 64 * h->elem_layout, h->scale_layout) &&
         !pl.swap && h->ws.bytes >= ws_bytes) {
       plan = &pl;
       break;

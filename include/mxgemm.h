@@ -119,8 +119,26 @@ typedef enum {
    * MXGEMM_SCALES_ROW_MAJOR.  With MXGEMM_SCALES_PACKED the run takes the
    * scales in the order the tensor cores read them (as mxgemm_quantize_ex
    * writes them) and runs no scale repack before the kernel. */
-  MXGEMM_OPT_SCALE_LAYOUT = 8
+  MXGEMM_OPT_SCALE_LAYOUT = 8,
+  /* Layout of the 6- and 4-bit element codes in A and B, an
+   * mxgemm_element_layout_t; default MXGEMM_ELEMS_BYTE.  No effect on 8-bit
+   * formats. */
+  MXGEMM_OPT_ELEMENT_LAYOUT = 10
 } mxgemm_option_t;
+
+/* Element layouts of 6- and 4-bit operands (both take one byte per element
+ * of address space: A is M x K bytes, B is K x N bytes).
+ *   MXGEMM_ELEMS_BYTE   : one element per byte, the code in the low bits
+ *     (the upper bits are ignored).  Each run repacks A and B into the form
+ *     below before the GEMM (a pass over each operand).
+ *   MXGEMM_ELEMS_PACKED : the form the tensor cores read: each 16-byte group
+ *     of a row (16 consecutive K elements of a row of A, 16 consecutive N
+ *     elements of a row of B) holds its 16 elements as one little-endian
+ *     128-bit number, element i at bits [b*i, b*i + b) for b = 6 or 4, that
+ *     is in the group's first 12 or 8 bytes (the other bytes are ignored).
+ *     Read as it is, with no pass before the GEMM; a 6- or 4-bit B then needs
+ *     N % 16 == 0 (MXGEMM_ERR_INVALID_VALUE). */
+typedef enum { MXGEMM_ELEMS_BYTE = 0, MXGEMM_ELEMS_PACKED = 1 } mxgemm_element_layout_t;
 
 /* Scale layouts.
  *   MXGEMM_SCALES_ROW_MAJOR : A_scale M x (K/32), B_scale N x (K/32), dense.

@@ -309,3 +309,23 @@ def pack_scales(S, along_cols: bool = False):
     out[at] = s
     return torch.from_numpy(out)
 
+
+
+def pack_elements(codes, nbits: int):
+    """Rearrange sub-byte element codes (one per byte, code in the low nbits)
+    into the packed form of mxgemm.h (MXGEMM_ELEMS_PACKED): every 16
+    consecutive elements of a row become one little-endian 128-bit number,
+    element i at bits [nbits*i, nbits*i + nbits), stored in the 16 bytes the
+    group occupied (the bytes past 2*nbits are zero).  The rows must hold a
+    multiple of 16 elements.  A layout change only: no value is computed."""
+    import numpy as np
+    c = np.ascontiguousarray(codes.cpu().numpy() if hasattr(codes, "numpy") else codes, dtype=np.uint8)
+    rows, n = c.shape
+    if n % 16:
+        raise ValueError("rows of whole 16-element groups only")
+    g = (c.reshape(-1, 16) & ((1 << nbits) - 1)).astype(np.uint8)
+    bits = ((g[:, :, None] >> np.arange(nbits, dtype=np.uint8)) & 1).reshape(-1, 16 * nbits)
+    packed = np.packbits(bits, axis=1, bitorder="little")  # (groups, 2 * nbits) bytes
+    out = np.zeros((g.shape[0], 16), dtype=np.uint8)
+    out[:, :packed.shape[1]] = packed
+    return torch.from_numpy(out.reshape(rows, n))

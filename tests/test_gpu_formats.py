@@ -88,3 +88,64 @@ def test_format_option_rejects_unknown_values(h):
             mx.mxgemm_set_option(h, opt, 5)
         with pytest.raises(mx.MxgemmError):
             mx.mxgemm_set_option(h, opt, -1)
+
+
+SUB_PAIRS = [("e2m1", "e2m1"), ("e2m3", "e3m2"), ("e3m2", "e4m3"), ("e4m3", "e2m1"), ("e2m1", "e5m2")]
+
+
+@pytest.mark.parametrize("mode", [1, 2])
+@pytest.mark.parametrize("fa,fb", SUB_PAIRS)
+def test_packed_elements_match_byte_elements(h, mode, fa, fb):
+    # 6- and 4-bit operands given already in the tensor cores' packed form
+    # (MXGEMM_ELEMS_PACKED, read as they are) and one code per byte (packed
+    # by the library first): the same C bit for bit, and the oracle on every
+    # element
+    M, N, K = 300, 528, 1024
+    g = torch.Generator().manual_seed(FMT[fa] * 11 + FMT[fb] + mode)
+    A = _codes(fa, (M, K), g, junk_high_bits=True)
+    B = _codes(fb, (K, N), g, junk_high_bits=True)
+    As = torch.randint(118, 137, (M, K // 32), generator=g, dtype=torch.int32).to(torch.uint8)
+    Bs = torch.randint(118, 137, (N, K // 32), generator=g, dtype=torch.int32).to(torch.uint8)
+    Ap = mi.pack_elements(A, BITS[fa]) if fa in BITS else A
+    Bp = mi.pack_elements(B, BITS[fb]) if fb in BITS else B
+    mx.mxgemm_set_option(h, mx.OPT_MODE, mode)
+    mx.mxgemm_set_option(h, mx.OPT_A_FORMAT, FMT[fa])
+    mx.mxgemm_set_option(h, mx.OPT_B_FORMAT, FMT[fb])
+    outs = []
+    try:
+        for layout, a, b in ((mx.ELEMS_BYTE, A, B), (mx.ELEMS_PACKED, Ap, Bp)):
+            mx.mxgemm_set_option(h, mx.OPT_ELEMENT_LAYOUT, layout)
+            n0 = mx.mxgemm_get_launch_count(h)
+            p = mi.Problem(f"{fa}x{fb}", M, N, K, a, As, b, Bs, "f32", False)
+            outs.append((gu.run_gpu(h, p).cpu(), mx.mxgemm_get_launch_count(h) - n0))
+    finally:
+        mx.mxgemm_set_option(h, mx.OPT_ELEMENT_LAYOUT, mx.ELEMS_BYTE)
+        mx.mxgemm_set_option(h, mx.OPT_A_FORMAT, 0)
+        mx.mxgemm_set_option(h, mx.OPT_B_FORMAT, 0)
+        mx.mxgemm_set_option(h, mx.OPT_MODE, 0)
+    (c_byte, n_byte), (c_packed, n_packed) = outs
+    assert torch.equal(c_byte.view(torch.int32), c_packed.view(torch.int32))
+    # no packing pass over A or B for packed elements
+    assert n_packed == n_byte - (fa in BITS) - (fb in BITS), (n_byte, n_packed)
+    ref, bound = oracle.rows(A, As, B, Bs, a_fmt=fa, b_fmt=fb)
+    res = oracle.accept(c_packed.numpy(), ref, bound, "f32")
+    assert res["ok"], res
+
+
+def test_packed_elements_need_whole_groups_of_b(h):
+    mx.mxgemm_set_option(h, mx.OPT_B_FORMAT, FMT["e2m1"])
+    mx.mxgemm_set_option(h, mx.OPT_ELEMENT_LAYOUT, mx.ELEMS_PACKED)
+    try:
+        dev = gu.DEV
+        A = torch.zeros((256, 64), dtype=torch.uint8, device=dev)
+        S = torch.full((256, 2), 127, dtype=torch.uint8, device=dev)
+        B = torch.zeros((64, 40), dtype=torch.uint8, device=dev)
+        T = torch.full((40, 2), 127, dtype=torch.uint8, device=dev)
+        C = torch.full((256, 40), 5.0, device=dev)
+        st = mx.mxgemm_run(h, 256, 40, 64, A, S, B, T, C, 0, mx.OUT_F32, check=False)
+        assert st == mx.ERR_INVALID_VALUE
+        with pytest.raises(mx.MxgemmError):
+            mx.mxgemm_set_option(h, mx.OPT_ELEMENT_LAYOUT, 2)
+    finally:
+        mx.mxgemm_set_option(h, mx.OPT_ELEMENT_LAYOUT, mx.ELEMS_BYTE)
+        mx.mxgemm_set_option(h, mx.OPT_B_FORMAT, 0)

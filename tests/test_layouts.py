@@ -1,6 +1,7 @@
-"""The host-side scale packer of the input module (used by bench.py's
---scale-layout packed) against the packed scale layout that mxgemm.h
-defines, worked out per element.  CPU only."""
+"""The host-side packers of the input module (scales: bench.py's
+--scale-layout packed; sub-byte elements: --element-layout packed) against
+the packed layouts that mxgemm.h defines, worked out per element.  CPU
+only."""
 import numpy as np
 import torch
 
@@ -27,3 +28,19 @@ def test_pack_scales_places_every_scale_once():
                 assert packed[at] == int(s[r, kb])
                 seen[at] = True
         assert np.all(packed[~seen] == 127)
+
+
+def test_pack_elements_places_each_code_at_its_bits():
+    # element i of a 16-element group at bits [b*i, b*i + b) of the group's
+    # little-endian 128-bit number; the high bits of each input byte dropped
+    g = torch.Generator().manual_seed(5)
+    for nbits in (4, 6):
+        codes = torch.randint(0, 256, (3, 48), generator=g, dtype=torch.int32).to(torch.uint8)
+        packed = mi.pack_elements(codes, nbits).numpy()
+        c = codes.numpy()
+        for r in range(3):
+            for grp in range(3):
+                value = int.from_bytes(packed[r, 16 * grp:16 * grp + 16].tobytes(), "little")
+                for i in range(16):
+                    assert (value >> (nbits * i)) & ((1 << nbits) - 1) == c[r, 16 * grp + i] & ((1 << nbits) - 1)
+                assert value >> (16 * nbits) == 0
