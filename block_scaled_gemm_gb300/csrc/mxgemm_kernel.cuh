@@ -80,8 +80,9 @@ struct Cfg {
   static constexpr int CLC_SLOTS = 4;  // cluster-launch-control response ring
   // full[], empty[], acc_full, acc_empty, final, clc_full[], clc_empty[],
   // stg (the scale loader's staging buffer has landed), stg_go (the scale
-  // loader has issued its first staging load)
-  static constexpr int NUM_BARS = 2 * STAGES + 3 + 2 * CLC_SLOTS + 2;
+  // loader has issued its first staging load), cin[] (per epilogue warp:
+  // its C_in chunks of the CTA's last tile have landed)
+  static constexpr int NUM_BARS = 2 * STAGES + 3 + 2 * CLC_SLOTS + 2 + 8;
   static constexpr int OFF_CLC = (OFF_BAR + NUM_BARS * 8 + 15) / 16 * 16;  // 16-byte responses
   static constexpr int OFF_MISC = OFF_CLC + 16 * CLC_SLOTS;
   // epilogue staging: one 32-row x 64-byte buffer per epilogue warp
@@ -462,6 +463,7 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
   const uint32_t bar_clc_empty = bar_clc_full + 8 * C::CLC_SLOTS;
   const uint32_t bar_stg = bar_clc_empty + 8 * C::CLC_SLOTS;
   const uint32_t bar_stg_go = bar_stg + 8;
+  const uint32_t bar_cin = bar_stg_go + 8;  // EPI_WARPS barriers
   const bool fused = C::HAS_SCALE_WARP && p.fused_scales != 0;
   uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(sm + C::OFF_MISC);
   volatile int *abort_flag = reinterpret_cast<volatile int *>(sm + C::OFF_MISC + 4);
@@ -484,6 +486,7 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
     }
     mbar_init(bar_stg, 1);
     mbar_init(bar_stg_go, 1);
+    for (int i = 0; i < C::EPI_WARPS; ++i) mbar_init(bar_cin + 8 * i, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -1239,8 +1242,9 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
 
       const int row0w = mt * (128 * CG) + 128 * (int)rank + 32 * q;  // this warp's first row
       const int row = row0w + lane;
-      if (kAcc && row < p.M) {
-        // C_in: this lane's row, ncols columns (the prefetch above put them in L2)
+      if (kAcc && !kTma && row < p.M) {
+        // C_in of the direct-store path (rows not 16-byte aligned): this
+        // lane's row, ncols columns (the prefetch above put them in L2)
         if constexpr (!kBF16) {
           const float *cp = reinterpret_cast<const float *>(p.C) + static_cast<int64_t>(row) * p.N + colb;
 #pragma unroll
@@ -1287,7 +1291,91 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
         }
       }
 
-      if constexpr (kTma) {
+      // use_acc on the CTA's last tile: the operand ring is free (the tile's
+      // MMAs have read every stage), so all of this warp's C_in chunks are
+      // loaded into it by TMA at once (16 KB per warp, each chunk in the
+      // swizzled layout of a store box) and waited for once, instead of one
+      // load round trip per chunk at the end of the kernel; each chunk is
+      // then summed in place and stored from there.
+      bool cin_done = false;
+      if constexpr (kAcc && kTma) {
+        bool last = false;
+        if (!p.use_clc) {
+          WorkIter peek = wi.wi;
+          WorkItem nx;
+          last = !peek.next(nx);
+        }
+        if (last && whole) {
+          constexpr int CCOLS = kBF16 ? 64 : 32;  // columns per chunk: 128 bytes
+          const uint32_t region = base + ew * 16384;
+          const uint32_t cbar = bar_cin + 8 * ew;
+          int nchunk = 0;
+          for (int cc = 0; cc < 128 / CCOLS; ++cc)
+            for (int rh = 0; rh < 2; ++rh)
+              if (colb + cc * CCOLS < p.N && row0w + 16 * rh < p.M) ++nchunk;
+          if (lane == 0) {
+            mbar_arrive_expect_tx(cbar, 2048u * nchunk);
+            for (int cc = 0; cc < 128 / CCOLS; ++cc)
+              for (int rh = 0; rh < 2; ++rh)
+                if (colb + cc * CCOLS < p.N && row0w + 16 * rh < p.M)
+                  tma_load_2d(region + (2 * cc + rh) * 2048, &tmC, colb + cc * CCOLS, row0w + 16 * rh, cbar);
+          }
+          __syncwarp();
+          if (!__all_sync(0xFFFFFFFFu, wait_phase<false>(cbar, 0, wc, 0x0E | ((t & 0xFFFF) << 16)))) break;
+          const int r16 = lane & 15;
+          const uint32_t swz = r16 & 7;
+#pragma unroll
+          for (int cc = 0; cc < 128 / CCOLS; ++cc) {
+            const int c0 = colb + cc * CCOLS;
+            if (c0 >= p.N) break;
+#pragma unroll
+            for (int rh = 0; rh < 2; ++rh) {
+              const int r0 = row0w + 16 * rh;
+              if (r0 >= p.M) break;
+              const uint32_t chunk = region + (2 * cc + rh) * 2048;
+              const uint32_t rowaddr = chunk + r16 * 128;
+              if ((lane >> 4) == rh) {
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                  const uint4 o = ld_shared_v4(rowaddr + ((u ^ swz) << 4));
+                  if constexpr (!kBF16) {
+                    const int c = cc * 32 + 4 * u;
+                    const float s0 = __uint_as_float(v[c >> 5][(c & 31) + 0]) + __uint_as_float(o.x);
+                    const float s1 = __uint_as_float(v[c >> 5][(c & 31) + 1]) + __uint_as_float(o.y);
+                    const float s2 = __uint_as_float(v[c >> 5][(c & 31) + 2]) + __uint_as_float(o.z);
+                    const float s3 = __uint_as_float(v[c >> 5][(c & 31) + 3]) + __uint_as_float(o.w);
+                    st_shared_v4(rowaddr + ((u ^ swz) << 4), __float_as_uint(s0), __float_as_uint(s1),
+                                 __float_as_uint(s2), __float_as_uint(s3));
+                  } else {
+                    const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
+                    uint32_t w2[4];
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                      const int c = cc * 64 + 8 * u + 2 * e;
+                      const float lo = __uint_as_float(v[c >> 5][c & 31]) + __uint_as_float(ow[e] << 16);
+                      const float hi =
+                          __uint_as_float(v[c >> 5][(c & 31) + 1]) + __uint_as_float(ow[e] & 0xFFFF0000u);
+                      const __nv_bfloat162 b2 = __floats2bfloat162_rn(lo, hi);
+                      w2[e] = *reinterpret_cast<const uint32_t *>(&b2);
+                    }
+                    st_shared_v4(rowaddr + ((u ^ swz) << 4), w2[0], w2[1], w2[2], w2[3]);
+                  }
+                }
+              }
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_2d(&tmC, chunk, c0, r0);
+                bulk_commit_group();
+              }
+            }
+          }
+          cin_done = true;
+        }
+      }
+      if (cin_done) {
+        // (stored from the ring above)
+      } else if constexpr (kTma) {
         // Chunks of 16 rows x 128 bytes through this warp's 2 KB staging
         // buffer, so that every row of a TMA store is a whole 128-byte line
         // in C (64-byte-wide chunks wrote each line in two halves, from two
@@ -1311,11 +1399,40 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
             if (r0 >= p.M) break;
             if (lane == 0) bulk_wait_read_all();
             __syncwarp();
+            if constexpr (kAcc) {
+              // C_in of the chunk, 16 rows x 128 bytes, with coalesced
+              // 16-byte loads (8 lanes per row, 4 rows per instruction) into
+              // the staging buffer in its swizzled order; the lanes holding
+              // the rows then add it to their accumulator values below.
+              // (Loads of one row per lane, 32 rows per instruction, took
+              // 8x the L1 wavefronts and slowed the concurrent main loop.)
+              const int u = lane & 7;
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                const int rr = (lane >> 3) + 4 * j;  // row within the chunk
+                uint4 x = make_uint4(0u, 0u, 0u, 0u);
+                // C's rows are 16-byte multiples here, so a unit is wholly
+                // inside or wholly past column N
+                if (r0 + rr < p.M && (c0 + u * CCOLS / 8) < p.N)
+                  x = __ldcg(reinterpret_cast<const uint4 *>(
+                      reinterpret_cast<const uint8_t *>(p.C) +
+                      (static_cast<int64_t>(r0 + rr) * p.N + c0) * (kBF16 ? 2 : 4) + 16 * u));
+                st_shared_v4(buf + rr * 128 + ((u ^ (rr & 7)) << 4), x.x, x.y, x.z, x.w);
+              }
+              __syncwarp();
+            }
             if ((lane >> 4) == rh) {
               if constexpr (!kBF16) {
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
                   const int c = cc * 32 + 4 * u;
+                  if constexpr (kAcc) {
+                    const uint4 o = ld_shared_v4(rowaddr + ((u ^ swz) << 4));
+                    v[c >> 5][(c & 31) + 0] = __float_as_uint(__uint_as_float(v[c >> 5][(c & 31) + 0]) + __uint_as_float(o.x));
+                    v[c >> 5][(c & 31) + 1] = __float_as_uint(__uint_as_float(v[c >> 5][(c & 31) + 1]) + __uint_as_float(o.y));
+                    v[c >> 5][(c & 31) + 2] = __float_as_uint(__uint_as_float(v[c >> 5][(c & 31) + 2]) + __uint_as_float(o.z));
+                    v[c >> 5][(c & 31) + 3] = __float_as_uint(__uint_as_float(v[c >> 5][(c & 31) + 3]) + __uint_as_float(o.w));
+                  }
                   st_shared_v4(rowaddr + ((u ^ swz) << 4), v[c >> 5][c & 31], v[c >> 5][(c & 31) + 1],
                                v[c >> 5][(c & 31) + 2], v[c >> 5][(c & 31) + 3]);
                 }
@@ -1323,6 +1440,18 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
                   uint32_t w[4];
+                  if constexpr (kAcc) {
+                    const uint4 o = ld_shared_v4(rowaddr + ((u ^ swz) << 4));
+                    const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                      const int c = cc * 64 + 8 * u + 2 * e;
+                      v[c >> 5][c & 31] =
+                          __float_as_uint(__uint_as_float(v[c >> 5][c & 31]) + __uint_as_float(ow[e] << 16));
+                      v[c >> 5][(c & 31) + 1] = __float_as_uint(__uint_as_float(v[c >> 5][(c & 31) + 1]) +
+                                                                __uint_as_float(ow[e] & 0xFFFF0000u));
+                    }
+                  }
 #pragma unroll
                   for (int e = 0; e < 4; ++e) {
                     const int c = cc * 64 + 8 * u + 2 * e;
