@@ -117,6 +117,7 @@ struct SwapCfg {
   static constexpr int THREADS = 7 * 32;
   static_assert(TM_SF + 8 * STAGES <= (int)TM_COLS, "TMEM budget");
   static_assert(NT <= TM_SF, "accumulator columns");
+  static_assert(STAGES <= 32 && SD <= 32, "one lane per early load");
   static_assert(SMEM_BYTES <= 232448, "shared memory budget");
   static_assert(AT_BYTES % 1024 == 0 && OFF_AT % 1024 == 0, "operand alignment");
 };
@@ -225,25 +226,37 @@ __global__ void __launch_bounds__(SwapCfg<NT>::THREADS, 1)
     tma_load_2d(sb + S::STG_BT, &tmSA, 16 * g, 0, bar);
   };
 
-  if (threadIdx.x == 0) {
-    for (int s = 0; s < S::STAGES; ++s) {
-      // full: the producer's arrive with the bytes, plus the scale
-      // builder's arrive once the stage's chunks are written
-      mbar_init(bar_full + 8 * s, packed ? 1 : 2);
-      mbar_init(bar_empty + 8 * s, 1);
+  if (warp == 0) {
+    if (lane == 0) {
+      // the tensor-map descriptors, fetched while the barriers are set up
+      tma_prefetch_desc(&tmBt);
+      tma_prefetch_desc(&tmAt);
+      if (stg_tma) {
+        tma_prefetch_desc(&tmSB);
+        tma_prefetch_desc(&tmSA);
+      }
+      for (int s = 0; s < S::STAGES; ++s) {
+        // full: the producer's arrive with the bytes, plus the scale
+        // builder's arrive once the stage's chunks are written
+        mbar_init(bar_full + 8 * s, packed ? 1 : 2);
+        mbar_init(bar_empty + 8 * s, 1);
+      }
+      mbar_init(bar_acc, 1);
+      for (int i = 0; i < S::SD; ++i) mbar_init(bar_stg + 8 * i, 1);
+      mbar_init(bar_final, 1);
+      *abort_flag = 0;
+      *never = 0;
+      fence_mbar_init();
+      fence_proxy_async_smem();  // the initialized barriers, before TMA completes on them
     }
-    mbar_init(bar_acc, 1);
-    for (int i = 0; i < S::SD; ++i) mbar_init(bar_stg + 8 * i, 1);
-    mbar_init(bar_final, 1);
-    *abort_flag = 0;
-    *never = 0;
-    fence_mbar_init();
-    fence_proxy_async_smem();  // the initialized barriers, before TMA completes on them
+    __syncwarp();
     // a prepass before this kernel (B re-pitched for N % 16 != 0) may still
     // be finishing: no global access before it has
     griddep_wait();
-    for (int g = g_first; g < g_first + n_stg_early; ++g) load_stg(g);
-    for (int i = 0; i < n_early; ++i) load_step(i, kb + i);
+    // one lane per load: the staging loads first, then the operand stages
+    if (lane < n_stg_early) load_stg(g_first + lane);
+    __syncwarp();
+    if (lane < n_early) load_step(lane, kb + lane);
   }
   if (warp == 1) {
     tmem_alloc<1>(smem_u32(tmem_slot), S::TM_COLS);
