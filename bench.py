@@ -426,7 +426,8 @@ class GemmSteps:
     mxgemm_run, or the chained use_acc calls of a K-split workload), with
     device operands prepared once."""
 
-    def __init__(self, mx, h, prob, dev, packed: bool, stream, elems_packed: bool = False):
+    def __init__(self, mx, h, prob, dev, packed: bool, stream, elems_packed: bool = False,
+                 b_nk: bool = False):
         import torch
         import mx_inputs
         self.mx, self.h, self.prob, self.stream = mx, h, prob, stream
@@ -441,6 +442,8 @@ class GemmSteps:
             if packed:
                 As = mx_inputs.pack_scales(As)
                 Bs = mx_inputs.pack_scales(Bs, along_cols=True)
+            if b_nk:
+                B = B.t().contiguous()  # B handed over as N x K (outside the step)
             if elems_packed:
                 # 6- and 4-bit operands handed over in the tensor cores'
                 # packed form (a host-side layout change, outside the step)
@@ -590,9 +593,12 @@ def run_mx(args, world, rank, local):
     elems_packed = args.element_layout == "packed"
     if elems_packed:
         mx.mxgemm_set_option(h, mx.OPT_ELEMENT_LAYOUT, mx.ELEMS_PACKED)
+    b_nk = args.b_major == "nk"
+    if b_nk:
+        mx.mxgemm_set_option(h, mx.OPT_B_MAJOR, mx.B_N_BY_K)
     if packed:
         mx.mxgemm_set_option(h, mx.OPT_SCALE_LAYOUT, mx.SCALES_PACKED)
-    ws = GemmSteps(mx, h, prob, dev, packed, stream, elems_packed)
+    ws = GemmSteps(mx, h, prob, dev, packed, stream, elems_packed, b_nk)
     flops = ws.flops
 
     for _ in range(args.warmup):
@@ -726,7 +732,7 @@ def run_mx(args, world, rank, local):
         e2e_steps = max(1, min(args.steps, args.e2e_steps))
         sA = mx_inputs.pack_scales(prob.As) if packed else prob.As
         sB = mx_inputs.pack_scales(prob.Bs, along_cols=True) if packed else prob.Bs
-        eA, eB = prob.A, prob.B
+        eA, eB = prob.A, (prob.B.t().contiguous() if b_nk else prob.B)
         if elems_packed:
             if mx_inputs.FORMAT_BITS[args.a_format] < 8:
                 eA = mx_inputs.pack_elements(eA, mx_inputs.FORMAT_BITS[args.a_format])
@@ -787,7 +793,8 @@ def run_mx(args, world, rank, local):
                        "parallelism": f"replicas x{world}" if world > 1 else "1 GPU",
                        "tile_mode": args.mode if args.mode is not None else "auto",
                        "a_format": args.a_format, "b_format": args.b_format,
-                       "scale_layout": args.scale_layout, "element_layout": args.element_layout},
+                       "scale_layout": args.scale_layout, "element_layout": args.element_layout,
+                       "b_major": args.b_major},
             "timing": {"step_us_median": statistics.median(step_list) * 1e3,
                        "step_us_mean": sum(step_list) / len(step_list) * 1e3,
                        "kernel_us_median": statistics.median(kern_list) * 1e3,
@@ -837,6 +844,9 @@ def main(argv=None):
     ap.add_argument("--element-layout", default="byte", choices=["byte", "packed"],
                     help="6- and 4-bit operands one code per byte (packed by the library each "
                          "call) or already in the tensor cores' packed form")
+    ap.add_argument("--b-major", default="kn", choices=["kn", "nk"],
+                    help="B handed over K x N (N contiguous, the default) or N x K (K contiguous, "
+                         "a linear layer's weight)")
     ap.add_argument("--no-flush", action="store_true")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle baseline and spot parity")
     ap.add_argument("--e2e-steps", type=int, default=20)

@@ -27,7 +27,7 @@ __all__ = [
     "FMT_E2M3", "FMT_E3M2", "FMT_E2M1", "MxgemmError", "library", "library_path", "mxgemm_create", "mxgemm_run",
     "mxgemm_destroy", "mxgemm_set_option", "mxgemm_get_device_status", "mxgemm_status_string",
     "mxgemm_set_profile_events", "mxgemm_get_launch_count", "mxgemm_run_noalloc", "mxgemm_run_host",
-    "mxgemm_quantize", "IN_F32", "IN_BF16", "EXPORTED_SYMBOLS", "Gemm", "OPT_SCALE_LAYOUT", "OPT_ELEMENT_LAYOUT", "ELEMS_BYTE", "ELEMS_PACKED",
+    "mxgemm_quantize", "IN_F32", "IN_BF16", "EXPORTED_SYMBOLS", "Gemm", "OPT_SCALE_LAYOUT", "OPT_ELEMENT_LAYOUT", "OPT_B_MAJOR", "B_K_BY_N", "B_N_BY_K", "ELEMS_BYTE", "ELEMS_PACKED",
     "SCALES_ROW_MAJOR", "SCALES_PACKED", "mxgemm_scale_bytes", "mxgemm_noalloc_get_status",
     "mxgemm_noalloc_set_option",
 ]
@@ -44,6 +44,9 @@ OPT_A_FORMAT = 6
 OPT_B_FORMAT = 7
 OPT_SCALE_LAYOUT = 8
 OPT_ELEMENT_LAYOUT = 10
+OPT_B_MAJOR = 11
+B_K_BY_N = 0
+B_N_BY_K = 1
 ELEMS_BYTE = 0
 ELEMS_PACKED = 1
 

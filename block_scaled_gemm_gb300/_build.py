@@ -17,9 +17,9 @@ from pathlib import Path
 PKG = Path(__file__).resolve().parent
 ROOT = PKG.parent
 SRC_DIR = PKG / "csrc"
-# translation units: the C interface with the tiled kernel, and the
-# skinny-problem kernel
-UNITS = [SRC_DIR / "mxgemm.cu", SRC_DIR / "swapab.cu"]
+# translation units: the C interface with the tiled kernel (B given K x N),
+# the tiled kernel's variants for B given N x K, and the skinny-problem kernel
+UNITS = [SRC_DIR / "mxgemm.cu", SRC_DIR / "tiled_kmajor.cu", SRC_DIR / "swapab.cu"]
 OBJ_DIR = PKG / "_build"
 HEADER = ROOT / "include" / "mxgemm.h"
 LIB = PKG / "libmxgemm.so"

@@ -23,6 +23,7 @@
 #include "quantize.cuh"
 #include "swapab.h"
 #include "swapab_kernel.cuh"
+#include "tiled_launch.cuh"
 
 namespace {
 
@@ -49,6 +50,7 @@ struct Plan {
   // value
   int CG = 1;
   bool pad_b = false;
+  bool pack_bk = false;  // B given N x K with a sub-byte format: packed into the workspace
   int64_t npad = 0;
   int a_bits = 8, b_bits = 8;  // element bits; below 8 the operand is packed first
   size_t off_a = 0;
@@ -111,7 +113,8 @@ struct mxgemm_ctx {
   int a_fmt = 0, b_fmt = 0;  // element formats (mxgemm_format_t)
   int scale_layout = MXGEMM_SCALES_ROW_MAJOR;
   int elem_layout = MXGEMM_ELEMS_BYTE;
-  bool attr_set[3][8] = {};
+  int b_major = MXGEMM_B_K_BY_N;
+  bool attr_set[3][16] = {};
   bool swap_attr[4][4] = {};
   cudaEvent_t prof_before = nullptr;
   cudaEvent_t prof_after = nullptr;
@@ -183,76 +186,15 @@ int ensure_workspace(mxgemm_ctx *h, size_t bytes, cudaStream_t stream) {
   return MXGEMM_OK;
 }
 
-template <int CG, int EPI>
-int launch_gemm_epi(mxgemm_ctx *h, const CUtensorMap &tA, const CUtensorMap &tB,
-                    const CUtensorMap &tB64, const CUtensorMap &tSA, const CUtensorMap &tSB, const CUtensorMap &tC,
-                    const KParams &kp, int units, cudaStream_t stream) {
-  using C = Cfg<CG>;
-  auto kern = mxg::mxgemm_kernel<CG, EPI>;
-  if (!h->attr_set[CG][EPI]) {
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
-        cudaSuccess) {
-      cudaGetLastError();
-      return MXGEMM_ERR_CUDA;
-    }
-    h->attr_set[CG][EPI] = true;
-  }
-  const int clusters = units;
-  cudaLaunchConfig_t cfg;
-  std::memset(&cfg, 0, sizeof(cfg));
-  cfg.gridDim = dim3(static_cast<unsigned>(clusters * CG), 1, 1);
-  cfg.blockDim = dim3(C::THREADS, 1, 1);
-  cfg.dynamicSmemBytes = C::SMEM_BYTES;
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[2];
-  // the kernel may start while the scale prepass before it finishes; it
-  // waits (griddepcontrol.wait) before touching global memory
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  if (CG == 2) {
-    attr[1].id = cudaLaunchAttributeClusterDimension;
-    attr[1].val.clusterDim.x = 2;
-    attr[1].val.clusterDim.y = 1;
-    attr[1].val.clusterDim.z = 1;
-    cfg.numAttrs = 2;
-  }
-  if (h->prof_before && cudaEventRecord(h->prof_before, stream) != cudaSuccess) {
-    cudaGetLastError();
-    return MXGEMM_ERR_CUDA;
-  }
-  cudaError_t e = cudaLaunchKernelEx(&cfg, kern, tA, tB, tB64, tSA, tSB, tC, kp);
-  if (e != cudaSuccess) {
-    cudaGetLastError();
-    return MXGEMM_ERR_CUDA;
-  }
-  ++h->launches;
-  if (h->prof_after && cudaEventRecord(h->prof_after, stream) != cudaSuccess) {
-    cudaGetLastError();
-    return MXGEMM_ERR_CUDA;
-  }
-  return MXGEMM_OK;
-}
-
-// The kernel instantiation for this run's epilogue (output type, use_acc,
-// TMA or direct stores).
+// The tiled kernel for this run: its epilogue variant, and its B layout.
 template <int CG>
 int launch_gemm(mxgemm_ctx *h, const CUtensorMap &tA, const CUtensorMap &tB,
                 const CUtensorMap &tB64, const CUtensorMap &tSA, const CUtensorMap &tSB, const CUtensorMap &tC,
                 const KParams &kp, int units, cudaStream_t stream) {
-  const int epi = (kp.out_bf16 ? mxg::kEpiBF16 : 0) | (kp.use_acc ? mxg::kEpiAcc : 0) |
-                  (kp.tma_store ? mxg::kEpiTma : 0);
-  switch (epi) {
-    case 0: return launch_gemm_epi<CG, 0>(h, tA, tB, tB64, tSA, tSB, tC, kp, units, stream);
-    case 1: return launch_gemm_epi<CG, 1>(h, tA, tB, tB64, tSA, tSB, tC, kp, units, stream);
-    case 2: return launch_gemm_epi<CG, 2>(h, tA, tB, tB64, tSA, tSB, tC, kp, units, stream);
-    case 3: return launch_gemm_epi<CG, 3>(h, tA, tB, tB64, tSA, tSB, tC, kp, units, stream);
-    case 4: return launch_gemm_epi<CG, 4>(h, tA, tB, tB64, tSA, tSB, tC, kp, units, stream);
-    case 5: return launch_gemm_epi<CG, 5>(h, tA, tB, tB64, tSA, tSB, tC, kp, units, stream);
-    case 6: return launch_gemm_epi<CG, 6>(h, tA, tB, tB64, tSA, tSB, tC, kp, units, stream);
-    default: return launch_gemm_epi<CG, 7>(h, tA, tB, tB64, tSA, tSB, tC, kp, units, stream);
-  }
+  mxg::TiledLaunch L{h->attr_set[CG], h->prof_before, h->prof_after, &h->launches};
+  const mxg::TiledMaps m{&tA, &tB, &tB64, &tSA, &tSB, &tC};
+  if (kp.b_kmajor) return mxg::launch_tiled_kmajor(CG, L, m, kp, units, stream);
+  return mxg::launch_tiled_epi<CG, 0>(L, m, kp, units, stream);
 }
 
 int launch_blocks(int64_t work, int per_block) {
@@ -338,12 +280,12 @@ struct Sizes {
   size_t off_sfb, off_b, off_part, off_a, total;
 };
 
-Sizes plan_sizes(int64_t a_chunks, int64_t b_chunks, bool pad_b, int64_t K, int64_t npad,
+Sizes plan_sizes(int64_t a_chunks, int64_t b_chunks, size_t b_ws_bytes,
                  const Split &sp, int CG, size_t a_bytes) {
   Sizes z;
   z.off_sfb = round_up(static_cast<size_t>(a_chunks) * 512, 1024);
   z.off_b = round_up(z.off_sfb + static_cast<size_t>(b_chunks) * 512, 1024);
-  z.off_part = round_up(z.off_b + (pad_b ? static_cast<size_t>(K) * npad : 0), 1024);
+  z.off_part = round_up(z.off_b + b_ws_bytes, 1024);
   z.off_a = round_up(z.off_part + static_cast<size_t>(sp.sk_ctas) * CG * 128 * 256 * sizeof(float),
                      1024);
   z.total = round_up(z.off_a + a_bytes, 1024);
@@ -367,7 +309,9 @@ int build_plan(mxgemm_ctx *h, Plan *pl, int64_t M, int64_t N, int64_t K, const v
     a_chunks = cdiv(M, 128) * k_steps;  // the packed area (a pair's second block may lie past it)
     b_chunks = n_tiles * k_steps * 2;
   }
-  const void *bsrc = pad_b ? static_cast<const void *>(h->ws.ptr + off_b) : B;
+  const bool b_km = h->b_major == MXGEMM_B_N_BY_K;
+  const bool pack_bk = b_km && b_bits < 8;
+  const void *bsrc = pad_b || pack_bk ? static_cast<const void *>(h->ws.ptr + off_b) : B;
   const int64_t bpitch = pad_b ? npad : N;
   const void *asrc = a_bits < 8 ? static_cast<const void *>(h->ws.ptr + z.off_a) : A;
   pl->ra = mxg::RepackArgs{static_cast<const uint8_t *>(A_scale), reinterpret_cast<uint32_t *>(h->ws.ptr),
@@ -381,9 +325,11 @@ int build_plan(mxgemm_ctx *h, Plan *pl, int64_t M, int64_t N, int64_t K, const v
   pl->blocks_b = pl->rb.row_blocks * pl->rb.kgroups;
   const CUtensorMapDataType u8 = CU_TENSOR_MAP_DATA_TYPE_UINT8;
   if (encode_2d(h, &pl->tA, u8, asrc, K, M, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      encode_2d(h, &pl->tB, u8, bsrc, N, K, bpitch, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
-      // half-width tiles of CTA pairs: 64 columns per CTA
-      encode_2d(h, &pl->tB64, u8, bsrc, N, K, bpitch, 64, 128, CU_TENSOR_MAP_SWIZZLE_64B))
+      (b_km ? encode_2d(h, &pl->tB, u8, bsrc, K, N, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B)
+            : encode_2d(h, &pl->tB, u8, bsrc, N, K, bpitch, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B)) ||
+      // half-width tiles of CTA pairs: 64 columns (rows of an N x K B) per CTA
+      (b_km ? encode_2d(h, &pl->tB64, u8, bsrc, K, N, K, 128, 64, CU_TENSOR_MAP_SWIZZLE_128B)
+            : encode_2d(h, &pl->tB64, u8, bsrc, N, K, bpitch, 64, 128, CU_TENSOR_MAP_SWIZZLE_64B)))
     return MXGEMM_ERR_CUDA;
   // Repacked scale chunks are contiguous 512-byte blocks, fetched as rows of
   // 128 bytes (4 rows per chunk) so each chunk is a handful of TMA requests.
@@ -453,9 +399,11 @@ int build_plan(mxgemm_ctx *h, Plan *pl, int64_t M, int64_t N, int64_t K, const v
                     reinterpret_cast<uintptr_t>(A_scale) % 16 == 0 &&
                     reinterpret_cast<uintptr_t>(B_scale) % 16 == 0;
   kp.early_ab = pl->repack_lite ? 1 : 0;
+  kp.b_kmajor = b_km ? 1 : 0;
   pl->units = sp.units;
   pl->CG = CG;
   pl->pad_b = pad_b;
+  pl->pack_bk = pack_bk;
   pl->npad = npad;
   pl->a_bits = a_bits;
   pl->b_bits = b_bits;
@@ -465,7 +413,7 @@ int build_plan(mxgemm_ctx *h, Plan *pl, int64_t M, int64_t N, int64_t K, const v
   pl->use_acc = use_acc; pl->out_dtype = out_dtype; pl->mode = h->mode;
   pl->stall = h->stall_producer; pl->sched = h->scheduler; pl->sk = h->stream_k;
   pl->timeout_ns = h->timeout_ns;
-  pl->fmts = h->a_fmt * 8 + h->b_fmt + 64 * h->elem_layout;
+  pl->fmts = h->a_fmt * 8 + h->b_fmt + 64 * h->elem_layout + 128 * h->b_major;
   pl->layout = packed ? MXGEMM_SCALES_PACKED : MXGEMM_SCALES_ROW_MAJOR;
   pl->ws = h->ws.ptr;
   pl->valid = true;
@@ -481,7 +429,8 @@ int run_swapab(mxgemm_ctx *h, int64_t M, int64_t N, int64_t K, const void *A, co
                bool packed, cudaStream_t stream) {
   const int64_t k_steps = cdiv(K, 128);
   const int64_t nblk = cdiv(N, 128);
-  const bool pad_b = (N % 16) != 0;
+  const bool b_km = h->b_major == MXGEMM_B_N_BY_K;
+  const bool pad_b = !b_km && (N % 16) != 0;
   const int64_t npad = round_up(static_cast<size_t>(N), 16);
   const size_t ws_bytes = pad_b ? round_up(static_cast<size_t>(K) * npad, 1024) : 0;
 
@@ -489,7 +438,7 @@ int run_swapab(mxgemm_ctx *h, int64_t M, int64_t N, int64_t K, const void *A, co
   for (Plan &pl : h->plans)
     if (pl.matches(M, N, K, A, A_scale, B, B_scale, C, use_acc, out_dtype, h->mode,
                    h->stall_producer, h->scheduler, h->stream_k, h->timeout_ns, h->ws.ptr,
-                   h->a_fmt * 8 + h->b_fmt + 64 * h->elem_layout, h->scale_layout) &&
+                   h->a_fmt * 8 + h->b_fmt + 64 * h->elem_layout + 128 * h->b_major, h->scale_layout) &&
         pl.swap && h->ws.bytes >= ws_bytes) {
       plan = &pl;
       break;
@@ -528,7 +477,8 @@ int run_swapab(mxgemm_ctx *h, int64_t M, int64_t N, int64_t K, const void *A, co
     // B: 128 columns x 128 K rows per box (the MMA's A operand, M-major);
     // A: 128 K bytes x nm rows (the MMA's B operand, K-major), rows past M
     // filled with zero
-    if (encode_2d(h, &pl.tB, u8, bsrc, N, K, bpitch, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B) ||
+    if ((b_km ? encode_2d(h, &pl.tB, u8, B, K, N, K, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B)
+              : encode_2d(h, &pl.tB, u8, bsrc, N, K, bpitch, 128, 128, CU_TENSOR_MAP_SWIZZLE_128B)) ||
         encode_2d(h, &pl.tAt, u8, A, K, M, K, 128, static_cast<uint32_t>(nm),
                   CU_TENSOR_MAP_SWIZZLE_128B))
       return MXGEMM_ERR_CUDA;
@@ -559,12 +509,14 @@ int run_swapab(mxgemm_ctx *h, int64_t M, int64_t N, int64_t K, const void *A, co
     p.kb_count = static_cast<int>(kb);
     p.scale_tma = scale_tma ? 1 : 0;
     p.packed = packed ? 1 : 0;
+    p.b_kmajor = b_km ? 1 : 0;
     p.a_chunks = static_cast<const uint8_t *>(A_scale);
     p.b_chunks = static_cast<const uint8_t *>(B_scale);
     pl.swap = true;
     pl.swap_grid = static_cast<int>(nblk * splits);
     pl.CG = 1;
     pl.pad_b = pad_b;
+    pl.pack_bk = false;
     pl.npad = npad;
     pl.a_bits = 8;
     pl.b_bits = 8;
@@ -574,7 +526,7 @@ int run_swapab(mxgemm_ctx *h, int64_t M, int64_t N, int64_t K, const void *A, co
     pl.use_acc = use_acc; pl.out_dtype = out_dtype; pl.mode = h->mode;
     pl.stall = h->stall_producer; pl.sched = h->scheduler; pl.sk = h->stream_k;
     pl.timeout_ns = h->timeout_ns;
-    pl.fmts = h->a_fmt * 8 + h->b_fmt + 64 * h->elem_layout;
+    pl.fmts = h->a_fmt * 8 + h->b_fmt + 64 * h->elem_layout + 128 * h->b_major;
     pl.layout = packed ? MXGEMM_SCALES_PACKED : MXGEMM_SCALES_ROW_MAJOR;
     pl.ws = h->ws.ptr;
     pl.valid = true;
@@ -716,6 +668,10 @@ int mxgemm_set_option(mxgemm_handle_t h, int option, int64_t value) {
       if (value != MXGEMM_ELEMS_BYTE && value != MXGEMM_ELEMS_PACKED) return MXGEMM_ERR_INVALID_VALUE;
       h->elem_layout = static_cast<int>(value);
       return MXGEMM_OK;
+    case MXGEMM_OPT_B_MAJOR:
+      if (value != MXGEMM_B_K_BY_N && value != MXGEMM_B_N_BY_K) return MXGEMM_ERR_INVALID_VALUE;
+      h->b_major = static_cast<int>(value);
+      return MXGEMM_OK;
     default:
       return MXGEMM_ERR_INVALID_VALUE;
   }
@@ -791,11 +747,15 @@ int mxgemm_run(mxgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A
   // 6- and 4-bit formats are packed 16 elements per 16-byte group first
   // (with MXGEMM_ELEMS_PACKED they arrive in that form and are read as
   // they are: whole 16-element groups, so N % 16 == 0 for a sub-byte B)
+  // B given N x K (MXGEMM_B_N_BY_K) has rows of K bytes: never re-pitched
+  // (K % 32 == 0), and its sub-byte groups run along K
+  const bool b_km = h->b_major == MXGEMM_B_N_BY_K;
   const bool elems_packed = h->elem_layout == MXGEMM_ELEMS_PACKED;
-  if (elems_packed && h->b_fmt >= MXGEMM_FMT_E2M3 && N % 16 != 0) return MXGEMM_ERR_INVALID_VALUE;
+  if (elems_packed && h->b_fmt >= MXGEMM_FMT_E2M3 && !b_km && N % 16 != 0) return MXGEMM_ERR_INVALID_VALUE;
   const int a_bits = elems_packed ? 8 : h->a_fmt == MXGEMM_FMT_E2M1 ? 4 : h->a_fmt >= MXGEMM_FMT_E2M3 ? 6 : 8;
   const int b_bits = elems_packed ? 8 : h->b_fmt == MXGEMM_FMT_E2M1 ? 4 : h->b_fmt >= MXGEMM_FMT_E2M3 ? 6 : 8;
-  const bool pad_b = (N % 16) != 0 || b_bits < 8;
+  const bool pad_b = !b_km && ((N % 16) != 0 || b_bits < 8);
+  const bool pack_bk = b_km && b_bits < 8;  // sub-byte B, N x K: packed along K first
   const int64_t npad = round_up(static_cast<size_t>(N), 16);
   // Cluster launch control: one cluster per work item (whole tiles, then
   // half-width items), handed out by the hardware; no stream-K, whose
@@ -803,7 +763,9 @@ int mxgemm_run(mxgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A
   const bool clc = h->scheduler == 1;
   Split sp = plan_split(num_tiles, k_steps, h->sm_count / CG, h->stream_k != 0, !clc, M);
   if (clc) sp.units = sp.dp_tiles + sp.half_tiles;
-  const Sizes z = plan_sizes(a_chunks, b_chunks, pad_b, K, npad, sp, CG,
+  const Sizes z = plan_sizes(a_chunks, b_chunks,
+                             pad_b ? static_cast<size_t>(K) * npad
+                                   : pack_bk ? static_cast<size_t>(N) * K : 0, sp, CG,
                              a_bits < 8 ? static_cast<size_t>(M) * K : 0);
   const size_t off_b = z.off_b;
   const size_t ws_bytes = z.total;
@@ -812,7 +774,7 @@ int mxgemm_run(mxgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A
   for (Plan &pl : h->plans)
     if (pl.matches(M, N, K, A, A_scale, B, B_scale, C, use_acc, out_dtype, h->mode,
                    h->stall_producer, h->scheduler, h->stream_k, h->timeout_ns, h->ws.ptr,
-                   h->a_fmt * 8 + h->b_fmt + 64 * h->elem_layout, h->scale_layout) &&
+                   h->a_fmt * 8 + h->b_fmt + 64 * h->elem_layout + 128 * h->b_major, h->scale_layout) &&
         !pl.swap && h->ws.bytes >= ws_bytes) {
       plan = &pl;
       break;
@@ -837,6 +799,10 @@ int mxgemm_run(mxgemm_handle_t h, int64_t M, int64_t N, int64_t K, const void *A
   if (plan->pad_b) {
     mxg::pad_rows_kernel<<<launch_blocks(K * (plan->npad / 16), 256), 256, 0, stream>>>(
         static_cast<const uint8_t *>(B), K, N, plan->npad, h->ws.ptr + off_b, plan->b_bits);
+    ++h->launches;
+  } else if (plan->pack_bk) {
+    mxg::pad_rows_kernel<<<launch_blocks(N * (K / 16), 256), 256, 0, stream>>>(
+        static_cast<const uint8_t *>(B), N, K, K, h->ws.ptr + off_b, plan->b_bits);
     ++h->launches;
   }
   if (plan->a_bits < 8) {
@@ -1276,7 +1242,7 @@ struct NoAllocDevice {
   uint8_t *scratch = nullptr;  // this device's address of g_noalloc_scratch
   int *status = nullptr;       // this device's address of g_noalloc_status
   int sm_count = 0;
-  bool attr_set[3][8] = {};
+  bool attr_set[3][16] = {};
 };
 
 constexpr int kNoAllocMaxDevices = 64;
@@ -1380,7 +1346,7 @@ extern "C" int mxgemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A
   // no stream-K split here (no partial sums or flags): the scratch holds
   // only a re-pitched B
   const Split sp = plan_split(num_tiles, k_steps, nd->sm_count / CG, false, false, M);
-  const Sizes z = plan_sizes(a_chunks, b_chunks, pad_b, K, npad, sp, CG, 0);
+  const Sizes z = plan_sizes(a_chunks, b_chunks, pad_b ? static_cast<size_t>(K) * npad : 0, sp, CG, 0);
   const size_t off_b = z.off_b;
   const size_t ws_bytes = z.total;
   if (ws_bytes > kNoAllocScratchBytes) return MXGEMM_ERR_TOO_LARGE;
@@ -1402,7 +1368,7 @@ extern "C" int mxgemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A
   {
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
     for (int i = 0; i < 3; ++i)
-      for (int j = 0; j < 8; ++j) ctx.attr_set[i][j] = nd->attr_set[i][j];
+      for (int j = 0; j < 16; ++j) ctx.attr_set[i][j] = nd->attr_set[i][j];
   }
   Plan plan;
   st = build_plan(&ctx, &plan, M, N, K, A, A_scale, B, B_scale, C, use_acc, out_dtype, CG, m_tiles,
@@ -1423,7 +1389,7 @@ extern "C" int mxgemm_run_noalloc(int64_t M, int64_t N, int64_t K, const void *A
   {
     std::lock_guard<std::mutex> lock(g_noalloc_mu);
     for (int i = 0; i < 3; ++i)
-      for (int j = 0; j < 8; ++j) nd->attr_set[i][j] = nd->attr_set[i][j] || ctx.attr_set[i][j];
+      for (int j = 0; j < 16; ++j) nd->attr_set[i][j] = nd->attr_set[i][j] || ctx.attr_set[i][j];
   }
   return st;
 }

@@ -157,6 +157,8 @@ struct KParams {
   // the first ring round's A and B loads before the programmatic-dependent-
   // launch wait, and its chunk loads after it.
   int early_ab;
+  // B given N x K (K contiguous); the kernel variant is chosen by it
+  int b_kmajor;
 };
 
 // Instruction descriptor of tcgen05.mma.kind::mxf8f6f4.block_scale:
@@ -317,6 +319,9 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, const 
 constexpr int kEpiBF16 = 1;    // BF16 output (else FP32)
 constexpr int kEpiAcc = 2;     // use_acc: C_in is read and added
 constexpr int kEpiTma = 4;     // C's rows are 16-byte aligned: TMA stores
+// (not an epilogue choice, but compiled the same way) B given N x K, K
+// contiguous: its tiles are K-major in shared memory, like A's
+constexpr int kEpiBKMajor = 8;
 
 // Bounded wait (whole warp) until the n flag slots at `slots` (written by
 // other CTAs after a fence) all hold `epoch`; lane i < n polls slot i.
@@ -448,6 +453,12 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
   constexpr bool kBF16 = (EPI & kEpiBF16) != 0;
   constexpr bool kAcc = (EPI & kEpiAcc) != 0;
   constexpr bool kTma = (EPI & kEpiTma) != 0;
+  // B K-major: a B tile is [rows of B][128 K bytes], loaded by boxes of
+  // 128 K bytes x 128 (64 for pair half-width tiles) rows, and read by the
+  // MMA like A (no transpose bit, 32 bytes per K = 32); else B is N-major:
+  // [128-column chunk][128 K rows][128 B], 4 KB per K = 32
+  constexpr bool kBKM = (EPI & kEpiBKMajor) != 0;
+  constexpr uint32_t kBNoT = kBKM ? ~(1u << 16) : ~0u;  // clears the transpose-B bit
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -581,8 +592,13 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
           // (fused: the scale chunks come from the scale loader)
           mbar_arrive_expect_tx(fb, fused ? C::STAGE_TX - C::CHUNK_TX : C::STAGE_TX);
           tma_load_2d(sA, &tmA, k0, row0, fb);
-          tma_load_2d(sB, &tmB, col0, k0, fb);
-          tma_load_2d(sB + 16384, &tmB, col0 + 128, k0, fb);
+          if constexpr (kBKM) {
+            tma_load_2d(sB, &tmB, k0, col0, fb);
+            tma_load_2d(sB + 16384, &tmB, k0, col0 + 128, fb);
+          } else {
+            tma_load_2d(sB, &tmB, col0, k0, fb);
+            tma_load_2d(sB + 16384, &tmB, col0 + 128, k0, fb);
+          }
           if (!fused) {
             tma_load_2d(sSA, &tmSFA, 0, (mblk * p.k_steps + ks) * 4, fb);
             tma_load_2d(sSB, &tmSFB, 0, (nt * p.k_steps + ks) * 8, fb);
@@ -591,7 +607,8 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
           if (rank == 0) mbar_arrive_expect_tx(fb, C::STAGE_TX);
           const uint32_t fbl = mapa_shared(fb, 0);  // leader's barrier
           tma_load_2d_pair(sA, &tmA, k0, row0, fbl);
-          tma_load_2d_pair(sB, &tmB, col0 + 128 * (int)rank, k0, fbl);
+          if constexpr (kBKM) tma_load_2d_pair(sB, &tmB, k0, col0 + 128 * (int)rank, fbl);
+          else tma_load_2d_pair(sB, &tmB, col0 + 128 * (int)rank, k0, fbl);
           tma_load_2d_pair(sSA, &tmSFA, 0, (mblk * p.k_steps + ks) * 4, fbl);
           tma_load_2d_pair(sSB, &tmSFB, 0, (nt * p.k_steps + ks) * 8, fbl);
         }
@@ -611,8 +628,12 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
               if (rank == 0) mbar_arrive_expect_tx(fb, C::STAGE_TX);
               const uint32_t fbl = mapa_shared(fb, 0);
               tma_load_2d_pair(base + C::OFF_A + st * C::A_BYTES, &tmA, (w.kb + st) * 128, row0, fbl);
-              tma_load_2d_pair(base + C::OFF_B + st * C::B_BYTES, &tmB, nt * 256 + 128 * (int)rank,
-                               (w.kb + st) * 128, fbl);
+              if constexpr (kBKM)
+                tma_load_2d_pair(base + C::OFF_B + st * C::B_BYTES, &tmB, (w.kb + st) * 128,
+                                 nt * 256 + 128 * (int)rank, fbl);
+              else
+                tma_load_2d_pair(base + C::OFF_B + st * C::B_BYTES, &tmB, nt * 256 + 128 * (int)rank,
+                                 (w.kb + st) * 128, fbl);
             }
             __syncwarp();
           }
@@ -733,7 +754,8 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
           if constexpr (CG == 1) {
             mbar_arrive_expect_tx(fb, fused ? C::STAGE_TX_HALF - C::CHUNK_TX : C::STAGE_TX_HALF);
             tma_load_2d(sA, &tmA, k0, row0, fb);
-            tma_load_2d(sB, &tmB, col0, k0, fb);
+            if constexpr (kBKM) tma_load_2d(sB, &tmB, k0, col0, fb);
+            else tma_load_2d(sB, &tmB, col0, k0, fb);
             if (!fused) {
               tma_load_2d(sSA, &tmSFA, 0, (mblk * p.k_steps + ks) * 4, fb);
               tma_load_2d(sSB, &tmSFB, 0, (nt * p.k_steps + ks) * 8, fb);
@@ -742,8 +764,9 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
             if (rank == 0) mbar_arrive_expect_tx(fb, C::STAGE_TX_HALF);
             const uint32_t fbl = mapa_shared(fb, 0);
             tma_load_2d_pair(sA, &tmA, k0, row0, fbl);
-            // 64 columns per CTA, 64-byte swizzle
-            tma_load_2d_pair(sB, &tmB64, col0 + 64 * (int)rank, k0, fbl);
+            // 64 columns per CTA (N-major: 64-byte swizzle; K-major: 64 rows)
+            if constexpr (kBKM) tma_load_2d_pair(sB, &tmB64, k0, col0 + 64 * (int)rank, fbl);
+            else tma_load_2d_pair(sB, &tmB64, col0 + 64 * (int)rank, k0, fbl);
             tma_load_2d_pair(sSA, &tmSFA, 0, (mblk * p.k_steps + ks) * 4, fbl);
             tma_load_2d_pair(sSB, &tmSFB, 0, (nt * p.k_steps + ks) * 8, fbl);
           }
@@ -817,13 +840,15 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
         // A: K-major, 128-byte swizzle, 8-row groups 1024 B apart; 32 B per K=32.
         // B: N-major, 128-byte swizzle; 128-column chunks 16 KB apart,
         // 8-row K groups 1024 B apart; 32 rows (4 KB) per K=32.
-        mma_mxf8<CG>(tmem + C::TM_ACC, smem_desc(sA, 0, 1024, 2), smem_desc(sB, 16384, 1024, 2),
-                     idesc_mxf8(128 * CG, 256, 0, 0) | fmt, tSA, tSB, ks != w.kb);
+        mma_mxf8<CG>(tmem + C::TM_ACC, smem_desc(sA, 0, 1024, 2),
+                     kBKM ? smem_desc(sB, 0, 1024, 2) : smem_desc(sB, 16384, 1024, 2),
+                     (idesc_mxf8(128 * CG, 256, 0, 0) | fmt) & kBNoT, tSA, tSB, ks != w.kb);
         const uint32_t ready = mbar_test_wait(bar_full + 8 * nst, nph);
 #pragma unroll
         for (int k = 1; k < 4; ++k)
           mma_mxf8<CG>(tmem + C::TM_ACC, smem_desc(sA + 32 * k, 0, 1024, 2),
-                       smem_desc(sB + 4096 * k, 16384, 1024, 2), idesc_mxf8(128 * CG, 256, k, k) | fmt, tSA,
+                       kBKM ? smem_desc(sB + 32 * k, 0, 1024, 2) : smem_desc(sB + 4096 * k, 16384, 1024, 2),
+                       (idesc_mxf8(128 * CG, 256, k, k) | fmt) & kBNoT, tSA,
                        tSB, 1u);
         if constexpr (CG == 1) tc_commit(bar_empty + 8 * st);
         else tc_commit_pair(bar_empty + 8 * st, 0x3);
@@ -932,8 +957,10 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
       if (go_half) {
         int s = hst;
         uint32_t ph = hph;
-        const uint64_t bdesc = CG == 2 ? smem_desc(0, 8192, 512, 4) : smem_desc(0, 16384, 1024, 2);
-        const uint32_t bstep = CG == 2 ? 2048 : 4096;
+        const uint64_t bdesc = kBKM    ? smem_desc(0, 0, 1024, 2)
+                               : CG == 2 ? smem_desc(0, 8192, 512, 4)
+                                         : smem_desc(0, 16384, 1024, 2);
+        const uint32_t bstep = kBKM ? 32 : CG == 2 ? 2048 : 4096;
         bool run = true;
         while (run) {
           run = __all_sync(0xFFFFFFFFu, wait_phase<CL>(bar_acc_empty, acc_phase ^ 1u, wc,
@@ -961,7 +988,7 @@ __global__ void __launch_bounds__(Cfg<CG>::THREADS, 1)
 #pragma unroll
               for (int k = 0; k < 4; ++k)
                 mma_mxf8<CG>(tmem + C::TM_ACC, smem_desc(sA + 32 * k, 0, 1024, 2),
-                             bdesc | ((sB + bstep * k) >> 4), idesc_mxf8(128 * CG, 128, k, k) | fmt, tSA,
+                             bdesc | ((sB + bstep * k) >> 4), (idesc_mxf8(128 * CG, 128, k, k) | fmt) & kBNoT, tSA,
                              tSB, (k0 != w.kb || k != 0) ? 1u : 0u);
               if constexpr (CG == 1) tc_commit(bar_empty + 8 * s);
               else tc_commit_pair(bar_empty + 8 * s, 0x3);

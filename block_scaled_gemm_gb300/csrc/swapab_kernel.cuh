@@ -85,6 +85,9 @@ struct SwapParams {
   int packed;
   const uint8_t *a_chunks;  // A_scale chunks, row block 0: ks * 512
   const uint8_t *b_chunks;  // B_scale chunks: ((c / 2 * S + ks) * 2 + c % 2) * 512
+  // B given N x K (K contiguous): the MMA's A operand is then K-major (a box
+  // of 128 K bytes x 128 rows of B, no transpose bit)
+  int b_kmajor;
 };
 
 template <int NT>
@@ -206,7 +209,8 @@ __global__ void __launch_bounds__(SwapCfg<NT>::THREADS, 1)
   auto load_step = [&](int st, int ks) {
     const uint32_t fb = bar_full + 8 * st;
     mbar_arrive_expect_tx(fb, S::BT_BYTES + at_tx + (packed ? 2 * S::SF_BYTES : 0));
-    tma_load_2d(base + S::OFF_BT + st * S::BT_BYTES, &tmBt, n0, ks * 128, fb);
+    if (p.b_kmajor) tma_load_2d(base + S::OFF_BT + st * S::BT_BYTES, &tmBt, ks * 128, n0, fb);
+    else tma_load_2d(base + S::OFF_BT + st * S::BT_BYTES, &tmBt, n0, ks * 128, fb);
     tma_load_2d(base + S::OFF_AT + st * S::AT_BYTES, &tmAt, ks * 128, 0, fb);
     if (packed) {
       const int c = n0 / 128;
@@ -326,8 +330,11 @@ __global__ void __launch_bounds__(SwapCfg<NT>::THREADS, 1)
           // A op: M-major, 128-byte swizzle, one 128-byte-wide column chunk,
           // 8-row K groups 1 KB apart, 32 K rows (4 KB) per K = 32.
           // B op: K-major, 128-byte swizzle, 8-row groups 1 KB apart, 32 B per K = 32.
-          mma_mxf8<1>(tmem + S::TM_ACC, smem_desc(sBt + 4096 * k, 16384, 1024, 2),
-                      smem_desc(sAt + 32 * k, 0, 1024, 2), idesc_swap(nm, k) | p.idesc_fmt, tSA, tSB,
+          mma_mxf8<1>(tmem + S::TM_ACC,
+                      p.b_kmajor ? smem_desc(sBt + 32 * k, 0, 1024, 2)
+                                 : smem_desc(sBt + 4096 * k, 16384, 1024, 2),
+                      smem_desc(sAt + 32 * k, 0, 1024, 2),
+                      (idesc_swap(nm, k) | p.idesc_fmt) & (p.b_kmajor ? ~(1u << 15) : ~0u), tSA, tSB,
                       (ks != kb || k != 0) ? 1u : 0u);
         tc_commit(bar_empty + 8 * st);
       }

@@ -18,6 +18,7 @@
  *                        MXGEMM_OPT_A_FORMAT), K contiguous
  *   A_scale : M x (K/32) uint8 E8M0 codes
  *   B       : K x N      uint8 element codes (MXGEMM_OPT_B_FORMAT), N contiguous
+ *                        (or N x K, K contiguous: MXGEMM_OPT_B_MAJOR)
  *   B_scale : N x (K/32) uint8 E8M0 codes (row j holds column j's scales)
  *   C       : M x N      float (MXGEMM_OUT_F32) or bfloat16 (MXGEMM_OUT_BF16)
  *
@@ -123,8 +124,19 @@ typedef enum {
   /* Layout of the 6- and 4-bit element codes in A and B, an
    * mxgemm_element_layout_t; default MXGEMM_ELEMS_BYTE.  No effect on 8-bit
    * formats. */
-  MXGEMM_OPT_ELEMENT_LAYOUT = 10
+  MXGEMM_OPT_ELEMENT_LAYOUT = 10,
+  /* Layout of B, an mxgemm_b_major_t; default MXGEMM_B_K_BY_N. */
+  MXGEMM_OPT_B_MAJOR = 11
 } mxgemm_option_t;
+
+/* Layouts of B (B_scale is N x (K/32) either way).
+ *   MXGEMM_B_K_BY_N : B is K x N, N contiguous (row pitch N bytes), as the
+ *     product C = A.B is written.
+ *   MXGEMM_B_N_BY_K : B is stored transposed, N x K with K contiguous (row
+ *     pitch K bytes; row j holds column j of B) -- the layout of a linear
+ *     layer's weight [out features][in features].  Its rows need no
+ *     re-pitch for any N, and 6- and 4-bit groups of 16 run along K. */
+typedef enum { MXGEMM_B_K_BY_N = 0, MXGEMM_B_N_BY_K = 1 } mxgemm_b_major_t;
 
 /* Element layouts of 6- and 4-bit operands (both take one byte per element
  * of address space: A is M x K bytes, B is K x N bytes).
