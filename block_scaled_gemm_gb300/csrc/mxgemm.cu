@@ -85,9 +85,10 @@ struct HostPipe {
   cudaStream_t h2d = nullptr, d2h = nullptr;
   cudaEvent_t start = nullptr;      // the caller's stream reached the call
   cudaEvent_t b_ready = nullptr;    // B and its scales are on the device
-  cudaEvent_t in_ready[2] = {};     // slot s holds its slab's inputs
-  cudaEvent_t gemm_done[2] = {};    // slot s's GEMM has finished
-  cudaEvent_t out_done[2] = {};     // slot s's C rows are back on the host
+  static constexpr int kSlots = 3;   // device slots for the row slabs
+  cudaEvent_t in_ready[kSlots] = {};   // slot s holds its slab's inputs
+  cudaEvent_t gemm_done[kSlots] = {};  // slot s's GEMM has finished
+  cudaEvent_t out_done[kSlots] = {};   // slot s's C rows are back on the host
   cudaEvent_t b_used[2] = {};       // the last GEMM reading B slot b has finished
   int bslot = 0;                    // B slot of the next call
   Workspace stage;
@@ -870,9 +871,9 @@ int mxgemm_destroy(mxgemm_handle_t h) {
     if (h->flags) cudaFree(h->flags);
     HostPipe &hp = h->hp;
     if (hp.stage.ptr) cudaFree(hp.stage.ptr);
-    for (cudaEvent_t e : {hp.start, hp.b_ready, hp.in_ready[0], hp.in_ready[1], hp.gemm_done[0],
-                          hp.gemm_done[1], hp.out_done[0], hp.out_done[1], hp.b_used[0],
-                          hp.b_used[1]})
+    for (cudaEvent_t e : {hp.start, hp.b_ready, hp.in_ready[0], hp.in_ready[1], hp.in_ready[2],
+                          hp.gemm_done[0], hp.gemm_done[1], hp.gemm_done[2], hp.out_done[0],
+                          hp.out_done[1], hp.out_done[2], hp.b_used[0], hp.b_used[1]})
       if (e) cudaEventDestroy(e);
     if (hp.h2d) cudaStreamDestroy(hp.h2d);
     if (hp.d2h) cudaStreamDestroy(hp.d2h);
@@ -1021,8 +1022,8 @@ extern "C" int mxgemm_scale_bytes(int64_t R, int64_t C, int along_cols, int scal
 // mxgemm_run_host: operands and result in host memory.
 //
 // B and its scales go to the device first; then the rows of A (and of C)
-// move in slabs through two device slots, so that a slab's GEMM overlaps the
-// next slab's copy in and the previous slab's copy out.  The GEMM of a slab
+// move in slabs through three device slots, so that a slab's GEMM overlaps
+// the next slab's copy in and the copies out of the two before it.  The GEMM of a slab
 // is an ordinary mxgemm_run on the slot's buffers.
 // ===========================================================================
 
@@ -1037,9 +1038,10 @@ int host_pipe_init(mxgemm_ctx *h) {
     cudaGetLastError();
     return MXGEMM_ERR_CUDA;
   }
-  cudaEvent_t *evs[] = {&hp.start,        &hp.b_ready,      &hp.in_ready[0], &hp.in_ready[1],
-                        &hp.gemm_done[0], &hp.gemm_done[1], &hp.out_done[0], &hp.out_done[1],
-                        &hp.b_used[0],    &hp.b_used[1]};
+  cudaEvent_t *evs[] = {&hp.start,        &hp.b_ready,      &hp.in_ready[0],  &hp.in_ready[1],
+                        &hp.in_ready[2],  &hp.gemm_done[0], &hp.gemm_done[1], &hp.gemm_done[2],
+                        &hp.out_done[0],  &hp.out_done[1],  &hp.out_done[2],  &hp.b_used[0],
+                        &hp.b_used[1]};
   for (cudaEvent_t *e : evs)
     if (!*e && cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) {
       cudaGetLastError();
@@ -1146,7 +1148,7 @@ extern "C" int mxgemm_run_host(mxgemm_handle_t h, int64_t M, int64_t N, int64_t 
   const size_t a_bytes = static_cast<size_t>(ms) * K, as_bytes = as_slab_bytes(ms);
   const size_t c_bytes = static_cast<size_t>(ms) * N * esz;
   // staging: two B slots (consecutive calls alternate, so that one call's
-  // B copy overlaps the previous call's last slabs), then two row slots
+  // B copy overlaps the previous call's last slabs), then three row slots
   const size_t off_bs = round_up(b_bytes, 256);
   const size_t bslot_bytes = round_up(off_bs + bs_bytes, 256);
   const size_t off_slot = 2 * bslot_bytes;
@@ -1154,7 +1156,7 @@ extern "C" int mxgemm_run_host(mxgemm_handle_t h, int64_t M, int64_t N, int64_t 
   const size_t off_c = round_up(off_as + as_bytes, 256);
   const size_t slot_bytes = round_up(off_c + c_bytes, 256);
   bool grown = false;
-  st = ensure_stage(h, off_slot + 2 * slot_bytes, stream, &grown);
+  st = ensure_stage(h, off_slot + HostPipe::kSlots * slot_bytes, stream, &grown);
   if (st != MXGEMM_OK) return st;
   const uint8_t *hA = static_cast<const uint8_t *>(A), *hAs = static_cast<const uint8_t *>(A_scale);
   uint8_t *hC = static_cast<uint8_t *>(C);
@@ -1179,7 +1181,7 @@ extern "C" int mxgemm_run_host(mxgemm_handle_t h, int64_t M, int64_t N, int64_t 
       !record_event(hp.b_ready, hp.h2d))
     return MXGEMM_ERR_CUDA;
   for (int64_t j = 0; j < nslab; ++j) {
-    const int s = static_cast<int>(j & 1);
+    const int s = static_cast<int>(j % HostPipe::kSlots);
     const int64_t m0 = j * ms, mj = (M - m0 < ms) ? M - m0 : ms;
     uint8_t *dA = base + off_slot + s * slot_bytes;
     uint8_t *dAs = dA + off_as;
@@ -1210,9 +1212,9 @@ extern "C" int mxgemm_run_host(mxgemm_handle_t h, int64_t M, int64_t N, int64_t 
   }
   // B slot bs is free once this call's last GEMM is done; the caller's
   // stream completes once every slab is back
-  if (!record_event(hp.b_used[bs], stream) || !wait_event(stream, hp.out_done[0]) ||
-      (nslab > 1 && !wait_event(stream, hp.out_done[1])))
-    return MXGEMM_ERR_CUDA;
+  if (!record_event(hp.b_used[bs], stream)) return MXGEMM_ERR_CUDA;
+  for (int s = 0; s < HostPipe::kSlots && s < nslab; ++s)
+    if (!wait_event(stream, hp.out_done[s])) return MXGEMM_ERR_CUDA;
   return MXGEMM_OK;
 }
 

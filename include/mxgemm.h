@@ -215,17 +215,17 @@ int mxgemm_run(mxgemm_handle_t h, int64_t M, int64_t N, int64_t K,
  * Arguments as for mxgemm_run, except that A, A_scale, B, B_scale and C
  * are host pointers (any alignment).  The call copies B and B_scale to the
  * device, then pipelines the rows of A and C in slabs of at most
- * max(256, M/8 rounded up to 256) rows through two device slots: while one
- * slab's GEMM runs on `stream`, the next slab's A rows (and, with use_acc,
- * its C rows) are copied in on an internal stream and the previous slab's
- * C rows are copied out on another.  `stream` waits for the last copy, so
+ * max(256, M/8 rounded up to 256) rows through three device slots: while
+ * one slab's GEMM runs on `stream`, the next slab's A rows (and, with
+ * use_acc, its C rows) are copied in on an internal stream and the earlier
+ * slabs' C rows are copied out on another.  `stream` waits for the last copy, so
  * C on the host is complete once `stream` is: synchronize it before reading
  * C.  The host buffers must hold their values when the call is made and
  * stay unchanged until `stream` has completed it; consecutive calls on one
  * handle overlap (one call's copies in run while the previous call's
  * copies out finish).  Page-locked (pinned) host buffers let the copies
  * overlap; pageable ones work but the copies then block the calling thread.  The handle owns
- * the device staging buffers (B, B_scale and the two slots), which grow
+ * the device staging buffers (B, B_scale and the three slots), which grow
  * lazily in stream order on `stream`, and two internal streams.  Use one
  * stream per handle.  K == 0 synchronizes `stream` and then zeroes C (use_acc
  * = 0) or leaves it unchanged.  Errors as for mxgemm_run; MXGEMM_ERR_CUDA if
