@@ -373,8 +373,8 @@ void mxo_round_bf16_array(const double *x, uint16_t *out, int64_t n) {
 /* ---------------------------------------------------------------------- */
 /*
  * Per block of 32 consecutive values x_0..x_31 (along a row, or down a
- * column), the recipe of the benchmark spec (OCP MX v1.0 conversion with an
- * E4M3 maximum of 448):
+ * column), the block-scaling recipe of the inputs' generator, which is the
+ * OCP Microscaling Formats v1.0 conversion with an E4M3 maximum of 448:
  *   amax  = max |x_i|
  *   scale = clamp(127 + ceil(log2(amax / 448)), 0, 254), and 127 if amax = 0
  *   code_i = E4M3 code nearest to clamp(x_i * 2^(127 - scale), -448, 448),
