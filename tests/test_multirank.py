@@ -76,3 +76,31 @@ def test_single_rank_needs_no_process_group():
     assert bench.init_dist(1, use_cuda=False) is None
     assert bench.max_over_ranks(3.5, None, "cpu") == 3.5
     bench.barrier(None)
+
+
+def test_reference_arm_line_keeps_the_contract(capsys):
+    # rank 0 of one: one JSON line with the keys the measurement contract
+    # names, the CPU baseline describing this run and no host copies
+    import json
+    import bench
+
+    class Args:
+        workload = "square_256"
+        steps = 3
+        warmup = 3
+        ref_budget = 0.5
+
+    assert bench.run_reference(Args(), 1, 0) == 0
+    lines = [l for l in capsys.readouterr().out.splitlines() if l.strip()]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    for key in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better",
+                "scaling", "vs_baseline", "dtype", "data", "config", "cpu_baseline", "e2e"):
+        assert key in d, key
+    assert d["impl"] == "reference"
+    assert d["steps"] == 3 and d["warmup"] == 3 and d["n_gpus"] == 1
+    assert d["config"]["workload"] == "square_256"
+    assert d["value"] > 0 and d["ms_per_step"] > 0
+    cb = d["cpu_baseline"]
+    assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
+    assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
