@@ -329,3 +329,28 @@ def pack_elements(codes, nbits: int):
     out = np.zeros((g.shape[0], 16), dtype=np.uint8)
     out[:, :packed.shape[1]] = packed
     return torch.from_numpy(out.reshape(rows, n))
+
+
+def pattern_matrix(R: int, C: int, rows=None, device="cpu", chunk_rows: int = 1024) -> torch.Tensor:
+    """A deterministic R x C FP32 matrix, exact in FP32 and BF16 alike, for
+    problems too large to generate with a CPU random generator:
+
+        x[r, c] = (((7919 r + 104729 c) mod 255) - 127) / 8 * 2^e,
+        e = ((r + floor(c / 32)) mod 16) - 8,
+
+    integers of at most 8 significant bits times a power of two that changes
+    from block to block of 32 columns and from row to row (so the blocks'
+    scales vary).  Integer arithmetic in int64, then one exact conversion.
+    ``rows`` (a list of row indices) returns only those rows, computed the
+    same way, so that a sample can be rebuilt on the CPU."""
+    pow2 = torch.tensor([2.0 ** e for e in range(-8, 8)], dtype=torch.float32, device=device)
+    r_all = torch.arange(R, dtype=torch.int64, device=device) if rows is None else \
+        torch.as_tensor(rows, dtype=torch.int64, device=device)
+    out = torch.empty((r_all.numel(), C), dtype=torch.float32, device=device)
+    c = torch.arange(C, dtype=torch.int64, device=device)[None, :]
+    for i in range(0, r_all.numel(), chunk_rows):
+        r = r_all[i:i + chunk_rows, None]
+        k = (r * 7919 + c * 104729) % 255 - 127
+        e = (r + c // 32) % 16
+        out[i:i + chunk_rows] = k.to(torch.float32) * 0.125 * pow2[e]
+    return out
