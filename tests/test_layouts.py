@@ -44,3 +44,20 @@ def test_pack_elements_places_each_code_at_its_bits():
                 for i in range(16):
                     assert (value >> (nbits * i)) & ((1 << nbits) - 1) == c[r, 16 * grp + i] & ((1 << nbits) - 1)
                 assert value >> (16 * nbits) == 0
+
+
+def test_pattern_matrix_rows_and_exactness():
+    # the large-index tests rebuild sampled rows of this matrix on the CPU:
+    # a row subset must equal the same rows of the whole matrix, every value
+    # must be exact in BF16 (so the BF16 input holds the same numbers), and
+    # the blocks' magnitudes must vary (different scales)
+    x = mi.pattern_matrix(96, 160)
+    rows = [0, 31, 32, 95]
+    assert torch.equal(mi.pattern_matrix(96, 160, rows=rows), x[rows])
+    assert torch.equal(x.to(torch.bfloat16).float(), x)
+    r, c = 37, 70
+    k = ((7919 * r + 104729 * c) % 255) - 127
+    e = ((r + c // 32) % 16) - 8
+    assert x[r, c].item() == k / 8 * 2.0 ** e
+    amax = x.reshape(96, 5, 32).abs().amax(-1)
+    assert torch.unique(amax).numel() > 8
