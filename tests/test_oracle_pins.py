@@ -555,3 +555,23 @@ def test_stochastic_rounding_against_exact_rationals():
             mag = (n + 1) * q if int(r) < frac * 2 ** 32 else n * q
             want = sign | table[mag]
         assert oracle.e4m3_sr(float(yv), int(r)) == want, (float(yv), int(r))
+
+
+def test_nan_codes_and_scale_255_poison_exactly_their_rows_and_columns():
+    # E4M3 codes 0x7F / 0xFF and the E8M0 byte 255 are NaN (reading 2 of the
+    # readings; OCP MX v1.0): a NaN element or scale of A poisons its row of
+    # C, one of B its column, and nothing else changes
+    p = mi.random_problem(40, 48, 128, seed=5, kind="int")
+    ref0, _ = oracle.rows(p.A, p.As, p.B, p.Bs)
+    A, As, B, Bs = p.A.clone(), p.As.clone(), p.B.clone(), p.Bs.clone()
+    A[5, 17] = 0x7F
+    A[9, 100] = 0xFF
+    As[12, 2] = 255
+    B[33, 20] = 0x7F
+    Bs[30, 1] = 255
+    ref, _ = oracle.rows(A, As, B, Bs)
+    mask = np.zeros((40, 48), dtype=bool)
+    mask[[5, 9, 12], :] = True
+    mask[:, [20, 30]] = True
+    assert np.array_equal(np.isnan(ref), mask)
+    assert np.array_equal(ref[~mask], ref0[~mask])
